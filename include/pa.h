@@ -1,0 +1,197 @@
+/*
+ * pa.h - C ABI of libpagedattn: paged single-query decode attention and the
+ * two cache operations around it, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources restated (page title, then section / equation):
+ *  [P1] "論文解説: Efficient Memory Management for Large Language Model Serving
+ *       with PagedAttention" (0h-n0.github.io): "PagedAttentionのメモリ管理",
+ *       "Attention計算", "Copy-on-Write（CoW）によるメモリ共有",
+ *       "GPUカーネル最適化".
+ *  [P2] "KVキャッシュとPagedAttention — 推論メモリのすべて" (youngju.dev):
+ *       "PagedAttention: OS仮想メモリ式の管理", "prefix共有とcopy-on-write",
+ *       "KV量子化: FP8とINT8", "GQAとMQA".
+ *  [P3] "PagedAttention" notes (dihengye.cn): "分块 Attention 计算".
+ *  [P4] "メモリ予算内での言語モデルのサービング" (auturnal.com): equation (4).
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *    library allocates nothing and keeps no reference after the call returns.
+ *    The caller owns every buffer.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and enqueues its work on the current device.
+ *  - Host-side validation happens before anything is enqueued: a negative
+ *    pa_status is returned and nothing runs.  PA_ERR_CUDA reports a failed
+ *    launch or CUDA runtime call.
+ *  - Device-side checks never trap.  Out-of-range block ids, slots, pairs or
+ *    sequence lengths are skipped and recorded in a per-device error word
+ *    that pa_get_device_error() reads and clears.
+ *  - KV cache layout: two separate pools k_cache and v_cache, each
+ *    [num_blocks][num_kv_heads][block_size][head_dim], row-major.  One
+ *    (block, head) tile is block_size*head_dim contiguous elements.
+ *    Token position p of a sequence lives in physical block
+ *    block_tables[s][p / block_size], row p % block_size  ([P1]
+ *    "PagedAttentionのメモリ管理": the block table maps logical blocks to
+ *    physical blocks of B tokens).
+ *  - Supported shapes: head_dim in {64, 128} for 16-bit caches, 128 for FP8;
+ *    block_size in {16, 32}; num_heads = G * num_kv_heads with 1 <= G <= 8.
+ */
+#ifndef PAGEDATTN_PA_H
+#define PAGEDATTN_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_F32 = 0,
+  PA_F16 = 1,
+  PA_BF16 = 2,
+  PA_FP8_E4M3 = 3 /* OCP E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa; max 448 */
+} pa_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,        /* a required pointer is NULL */
+  PA_ERR_SHAPE = -2,       /* inconsistent or out-of-range sizes */
+  PA_ERR_DTYPE = -3,       /* dtype combination not accepted */
+  PA_ERR_UNSUPPORTED = -4, /* valid request outside the compiled variants */
+  PA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
+  PA_ERR_CUDA = -6,        /* CUDA runtime / launch failure */
+  PA_ERR_ALIGN = -7        /* a pointer or stride breaks the 16-byte rule */
+} pa_status;
+
+/* Bits of the per-device error word (pa_get_device_error). */
+#define PA_DEVERR_BLOCK_ID 1u /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT 2u     /* slot outside [0, num_blocks*block_size) */
+#define PA_DEVERR_SEQ_LEN 4u  /* seq_len < 0 or > max_blocks_per_seq*block_size */
+#define PA_DEVERR_TIMEOUT 8u  /* a bounded wait on an async copy gave up */
+#define PA_DEVERR_PAIR 16u    /* copy_blocks id outside [0, num_blocks) */
+
+/*
+ * pa_decode_workspace_bytes
+ *   Bytes of device workspace that pa_decode needs for these sizes on the
+ *   CURRENT device (the split-K partial records depend on the device's SM
+ *   count).  Returns 0 when the call needs no workspace (single pass) and
+ *   (size_t)-1 when the sizes are rejected or no device is usable.
+ *   The workspace must be zero-filled once before its first use; every
+ *   completed pa_decode leaves it ready for the next call.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int max_blocks_per_seq, int partition_size,
+                                 pa_dtype kv_dtype);
+
+/*
+ * pa_decode - one decode step of paged attention.
+ *
+ * For every sequence s and query head h (KV head kvh = h / G, G = num_heads /
+ * num_kv_heads, [P2] "GQAとMQA"):
+ *     out[s][h] = softmax(scale * K_s q[s][h]) V_s
+ * where K_s, V_s are the seq_lens[s] rows of KV head kvh gathered through
+ * block_tables[s] ([P1] "Attention計算"; [P3] "分块 Attention 计算").  The
+ * kernel reads the blocks one by one and merges them with the online-softmax
+ * recurrence ([P4] eq. (4)); long sequences are split across warps and the
+ * per-split states (m, l, acc) are merged with the same recurrence by the
+ * last split to finish ("split-K").  seq_lens[s] == 0 gives out[s] = 0.
+ * FP8 caches ([P2] "KV量子化") are dequantised in registers as
+ * float(e4m3) * k_scale[kvh] (resp. v_scale[kvh]).
+ *
+ *   out            [num_seqs][num_heads][head_dim], out_dtype F32/F16/BF16
+ *   q              [num_seqs][num_heads][head_dim] at q_stride elements per
+ *                  sequence (q_stride >= num_heads*head_dim), q_dtype F16/BF16;
+ *                  16-byte aligned base, q_stride*sizeof(q) % 16 == 0
+ *   k_cache/v_cache  pools as above, kv_dtype F16/BF16 (== q_dtype) or
+ *                  FP8_E4M3; 16-byte aligned; num_blocks blocks each
+ *   k_scale/v_scale  float32 [num_kv_heads]; required for FP8, else ignored
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; entries beyond
+ *                  ceil(seq_lens[s]/block_size) are never read
+ *   seq_lens       int32 [num_seqs]
+ *   scale          softmax scale (e.g. 1/sqrt(head_dim)), float32
+ *   partition_size 0   = balanced split: equal shares of all KV blocks to
+ *                        every resident warp (recommended);
+ *                  P>0 = fixed partitions of P tokens (P % block_size == 0),
+ *                        one warp each; P >= max_blocks_per_seq*block_size
+ *                        is a single pass that needs no workspace.
+ *   workspace      device buffer of >= pa_decode_workspace_bytes(...) bytes,
+ *                  zero-filled before first use; NULL allowed when 0 bytes
+ *                  are required.  Calls that share a workspace must not
+ *                  overlap on the GPU.
+ *   stream         cudaStream_t
+ */
+int pa_decode(void* out, pa_dtype out_dtype,
+              const void* q, pa_dtype q_dtype, int64_t q_stride,
+              const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+              const float* k_scale, const float* v_scale,
+              const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* seq_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+              float scale, int block_size, int partition_size,
+              void* workspace, size_t workspace_bytes,
+              void* stream);
+
+/*
+ * pa_reshape_and_cache - write new tokens' K and V rows into their slots.
+ *
+ * [P2] "PagedAttention: OS仮想メモリ式の管理": blocks are handed out as tokens
+ * accumulate and the block table maps token positions to physical blocks;
+ * the caller encodes that mapping as one slot per token,
+ *     slot = physical_block * block_size + position % block_size,
+ * and this call stores k[n][h][:] at k_cache[slot/block_size][h][slot%block_size][:]
+ * (v likewise) for every KV head h.  slot < 0 marks padding and is skipped.
+ * 16-bit caches receive the source bits (src_dtype == kv_dtype).  FP8 caches
+ * receive e4m3_rne_satfinite(float32(x) * inv_scale[h]) (product rounded in
+ * float32, round-to-nearest-even, magnitudes >= 448 saturate to 448).
+ *
+ *   k, v           [num_tokens][num_kv_heads][head_dim] rows at k_stride /
+ *                  v_stride elements per token (>= num_kv_heads*head_dim),
+ *                  src_dtype F16/BF16
+ *   k_cache/v_cache  pools as above (num_blocks blocks), kv_dtype
+ *   slot_mapping   int64 [num_tokens]
+ *   k_inv_scale/v_inv_scale  float32 [num_kv_heads]; FP8 only
+ * Two tokens must not share a slot (the surviving row is then unspecified).
+ */
+int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype,
+                         int64_t k_stride, int64_t v_stride,
+                         void* k_cache, void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                         const int64_t* slot_mapping, int num_tokens,
+                         int num_kv_heads, int head_dim, int block_size,
+                         const float* k_inv_scale, const float* v_inv_scale,
+                         void* stream);
+
+/*
+ * pa_copy_blocks - the device half of copy-on-write.
+ *
+ * [P1] "Copy-on-Write（CoW）によるメモリ共有": before a sequence writes into a
+ * block that other sequences still reference, the block manager allocates a
+ * fresh block and the old block's contents are copied into it.  For every
+ * pair i, physical block src_dst_pairs[2i+1] of both pools receives a copy
+ * of block src_dst_pairs[2i] (all KV heads, all slots; block_bytes bytes per
+ * pool, = num_kv_heads*block_size*head_dim*sizeof(element), a multiple of 16).
+ * Destinations must be distinct and must not be a source of any pair (a
+ * fresh block, as the pages' allocator hands out); otherwise the result is
+ * unspecified.  The copy is ordered before later work on `stream`.
+ *   src_dst_pairs  int32 [num_pairs][2], device
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, size_t block_bytes,
+                   const int32_t* src_dst_pairs, int num_pairs, void* stream);
+
+/* Human-readable name of a pa_status value (static string). */
+const char* pa_status_string(int status);
+
+/*
+ * Read and clear the current device's error word (PA_DEVERR_* bits) after
+ * the work already enqueued on `stream` has finished.  Synchronises `stream`.
+ * *error_bits (host pointer) receives the bits.
+ */
+int pa_get_device_error(void* stream, unsigned int* error_bits);
+
+/* Library ABI version (major*100 + minor). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_PA_H */

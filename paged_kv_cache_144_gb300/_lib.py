@@ -1,0 +1,218 @@
+"""ctypes binding of libpagedattn (include/pa.h): argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels.  If the library
+cannot be loaded the calls raise; there is no CPU or PyTorch fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libpagedattn.so")
+HEADER = os.path.join(os.path.dirname(PKG_DIR), "include", "pa.h")
+
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
+PA_OK = 0
+PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_DTYPE, PA_ERR_UNSUPPORTED = -1, -2, -3, -4
+PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_ALIGN = -5, -6, -7
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT, PA_DEVERR_PAIR = 1, 2, 4, 8, 16
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+_SIGNATURES = {
+    "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_decode": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
+                         _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp]),
+    "pa_reshape_and_cache": (_i32, [_vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32, _i64, _vp, _i32, _i32, _i32,
+                                    _i32, _vp, _vp, _vp]),
+    "pa_copy_blocks": (_i32, [_vp, _vp, _i64, _sz, _vp, _i32, _vp]),
+    "pa_status_string": (ctypes.c_char_p, [_i32]),
+    "pa_get_device_error": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+    "pa_version": (_i32, []),
+}
+
+_LIB = None
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions that include/pa.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libpagedattn.so."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        if not build_if_missing:
+            raise OSError(f"{LIB_PATH} is missing; run paged_kv_cache_144_gb300.build")
+        from .build import build
+        build()
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PA_OK:
+        raise PagedAttnError(fn, status, status_string(status))
+
+
+# ----------------------------------------------------------------------------- raw C-ABI calls
+
+def pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                              partition_size, kv_dtype) -> int:
+    return int(load().pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                max_blocks_per_seq, partition_size, kv_dtype))
+
+
+def pa_decode(*args) -> int:
+    return int(load().pa_decode(*args))
+
+
+def pa_reshape_and_cache(*args) -> int:
+    return int(load().pa_reshape_and_cache(*args))
+
+
+def pa_copy_blocks(*args) -> int:
+    return int(load().pa_copy_blocks(*args))
+
+
+def pa_get_device_error(stream) -> int:
+    bits = ctypes.c_uint(0)
+    _check("pa_get_device_error", int(load().pa_get_device_error(stream, ctypes.byref(bits))))
+    return int(bits.value)
+
+
+def pa_version() -> int:
+    return int(load().pa_version())
+
+
+# ----------------------------------------------------------------------------- torch marshalling
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3}
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is not None:
+        m[f8] = PA_FP8_E4M3
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(name, t, contiguous=True):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                           partition_size=0, kv_dtype=PA_BF16) -> int:
+    n = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                  partition_size, kv_dtype)
+    if n == SIZE_MAX:
+        raise PagedAttnError("pa_decode_workspace_bytes", PA_ERR_SHAPE, "sizes rejected or no usable device")
+    return n
+
+
+def new_workspace(nbytes: int, device):
+    """Zero-filled workspace (allocated by torch, not by the library)."""
+    torch = _torch()
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale, block_size, *,
+           k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None):
+    """out[s,h] = softmax(scale * K_s q[s,h]) V_s through the block tables (pa_decode)."""
+    for n, t in (("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
+                 ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _require_cuda(n, t)
+    _require_cuda("q", q, contiguous=False)
+    if q.stride(2) != 1 or q.stride(1) != q.shape[2]:
+        raise ValueError("q rows must be contiguous per sequence")
+    S, Hq, D = q.shape
+    NB = k_cache.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = pa_decode(_ptr(out), dtype_code(out), _ptr(q), dtype_code(q), q.stride(0),
+                   _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), NB,
+                   _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                   S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
+                   _ptr(workspace), ws_bytes, _stream(stream))
+    _check("pa_decode", st)
+    return out
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *, k_inv_scale=None, v_inv_scale=None,
+                      stream=None):
+    """Write rows k[n], v[n] ([N, H_kv, d]) to cache slots slot_mapping[n] (pa_reshape_and_cache)."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("slot_mapping", slot_mapping),
+                 ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale)):
+        _require_cuda(n, t)
+    _require_cuda("k", k, contiguous=False)
+    _require_cuda("v", v, contiguous=False)
+    N, Hkv, D = k.shape
+    for t in (k, v):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError("k/v rows must be contiguous per token")
+    st = pa_reshape_and_cache(_ptr(k), _ptr(v), dtype_code(k), k.stride(0), v.stride(0),
+                              _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), k_cache.shape[0],
+                              _ptr(slot_mapping), N, Hkv, D, int(block_size),
+                              _ptr(k_inv_scale), _ptr(v_inv_scale), _stream(stream))
+    _check("pa_reshape_and_cache", st)
+
+
+def copy_blocks(k_cache, v_cache, src_dst_pairs, *, stream=None):
+    """Copy whole physical blocks src -> dst in both pools (pa_copy_blocks)."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("src_dst_pairs", src_dst_pairs)):
+        _require_cuda(n, t)
+    n_pairs = src_dst_pairs.shape[0] if src_dst_pairs.numel() else 0
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    st = pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), k_cache.shape[0], block_bytes, _ptr(src_dst_pairs),
+                        n_pairs, _stream(stream))
+    _check("pa_copy_blocks", st)
+
+
+def get_device_error(stream=None) -> int:
+    return pa_get_device_error(_stream(stream))

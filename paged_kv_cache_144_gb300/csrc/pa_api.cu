@@ -1,0 +1,299 @@
+// pa_api.cu - the extern "C" entry points declared in include/pa.h: argument
+// validation, TMA descriptor encoding, workspace accounting and dispatch to
+// the kernels.  No call here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+
+#define PA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+// Per-device error word (PA_DEVERR_* bits).  Kernels receive its address.
+__device__ unsigned int g_device_error = 0u;
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_device_error on the current device (nullptr on failure).
+unsigned int* device_error_word() {
+  static unsigned int* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned int*>(p);
+  }
+  return addr[dev];
+}
+
+constexpr int kMaxSeqs = 16384;  // prefix sums of the batch live in shared memory
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int dtype_bytes(int dt) {
+  switch (dt) {
+    case PA_F32: return 4;
+    case PA_F16: return 2;
+    case PA_BF16: return 2;
+    case PA_FP8_E4M3: return 1;
+    default: return 0;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view of a cache pool: rows of head_dim elements, num_blocks*Hkv*B rows;
+// one TMA box = 128 bytes of a row x block_size rows, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, int num_kv_heads,
+                      int block_size, int head_dim, int elem_bytes) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim),
+                        static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elem_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(block_size)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                         const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int gmax_for_group(int g) { return g <= 1 ? 1 : (g <= 4 ? 4 : 8); }
+
+// Shape checks shared by pa_decode and pa_decode_workspace_bytes.
+int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       int max_blocks_per_seq, int partition_size, int kv_dtype) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+  if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+  if (num_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype == PA_FP8_E4M3 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (partition_size < 0 || (partition_size > 0 && partition_size % block_size != 0)) return PA_ERR_SHAPE;
+  if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_seqs) * num_kv_heads * max_blocks_per_seq >= (int64_t{1} << 31)) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+struct DecodePlan {
+  pa::DecodeKey key;
+  pa::DecodeGeometry geo;
+  int partition_blocks;     // as passed to the kernel (0 = balanced)
+  size_t counters_bytes;
+  size_t records;
+  size_t bytes;             // total workspace bytes required
+};
+
+// Resolves the variant, launch geometry and workspace need.  `have_ws` tells
+// whether the caller supplied a workspace (balanced mode needs one).
+int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+              int partition_size, int q_dtype, int kv_dtype, bool have_ws, DecodePlan* plan) {
+  plan->key.q_dtype = q_dtype;
+  plan->key.kv_dtype = kv_dtype;
+  plan->key.head_dim = head_dim;
+  plan->key.block_size = block_size;
+  plan->key.gmax = gmax_for_group(num_heads / num_kv_heads);
+  if (!pa::decode_geometry(plan->key, num_seqs, &plan->geo)) return PA_ERR_UNSUPPORTED;
+  int pb = partition_size / block_size;
+  if (partition_size == 0 && !have_ws) pb = max_blocks_per_seq;  // single pass without workspace
+  if (pb >= max_blocks_per_seq) pb = max_blocks_per_seq;
+  plan->partition_blocks = pb;
+  if (pb == max_blocks_per_seq) {  // one fragment per segment: no partial records
+    plan->counters_bytes = 0;
+    plan->records = 0;
+    plan->bytes = 0;
+    return PA_OK;
+  }
+  plan->counters_bytes = (static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int) + 255) / 256 * 256;
+  if (pb == 0) {
+    plan->records = 2ull * plan->geo.ctas * plan->geo.warps_per_cta;
+  } else {
+    plan->records = static_cast<size_t>(num_seqs) * num_kv_heads * ((max_blocks_per_seq + pb - 1) / pb);
+  }
+  plan->bytes = plan->counters_bytes + plan->records * plan->geo.record_floats * sizeof(float);
+  return PA_OK;
+}
+
+}  // namespace
+
+PA_EXPORT int pa_version(void) { return 100; }
+
+PA_EXPORT const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: inconsistent or out-of-range sizes";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype combination not accepted";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: outside the compiled variants";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime or launch failure";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    default: return "unknown pa_status";
+  }
+}
+
+PA_EXPORT size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                           int block_size, int max_blocks_per_seq, int partition_size,
+                                           pa_dtype kv_dtype) {
+  if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         partition_size, kv_dtype) != PA_OK)
+    return static_cast<size_t>(-1);
+  const int q_dtype = (kv_dtype == PA_FP8_E4M3) ? PA_BF16 : kv_dtype;
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16) return static_cast<size_t>(-1);
+  DecodePlan plan;
+  if (make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, partition_size, q_dtype,
+                kv_dtype, true, &plan) != PA_OK)
+    return static_cast<size_t>(-1);
+  return plan.bytes;
+}
+
+PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
+                        const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                    partition_size, kv_dtype);
+  if (sh != PA_OK) return sh;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_NULL;
+  if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
+  if (kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_NULL;
+  if (num_blocks <= 0 || num_blocks * num_kv_heads * block_size >= (int64_t{1} << 31)) return PA_ERR_SHAPE;
+  if (q_stride < static_cast<int64_t>(num_heads) * head_dim) return PA_ERR_SHAPE;
+  if (!aligned16(q) || (q_stride * 2) % 16 != 0 || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+
+  DecodePlan plan;
+  const bool have_ws = workspace != nullptr && workspace_bytes > 0;
+  const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                           partition_size, q_dtype, kv_dtype, have_ws, &plan);
+  if (pr != PA_OK) return pr;
+  if (plan.bytes > 0 && (!have_ws || workspace_bytes < plan.bytes || !aligned16(workspace))) return PA_ERR_WORKSPACE;
+
+  CUtensorMap tk, tv;
+  const int eb = dtype_bytes(kv_dtype);
+  if (!encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim, eb) ||
+      !encode_cache_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, eb))
+    return PA_ERR_CUDA;
+
+  unsigned int* err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  pa::DecodeParams p;
+  p.err = err;
+  p.out = out;
+  p.out_dtype = out_dtype;
+  p.q = q;
+  p.q_stride = q_stride;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.seq_lens = seq_lens;
+  p.num_blocks = num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.qk_scale_log2 = scale * 1.4426950408889634f;
+  p.partition_blocks = plan.partition_blocks;
+  p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
+  p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)
+                              : nullptr;
+  const cudaError_t e = pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype, int64_t k_stride,
+                                   int64_t v_stride, void* k_cache, void* v_cache, pa_dtype kv_dtype,
+                                   int64_t num_blocks, const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_dim, int block_size, const float* k_inv_scale,
+                                   const float* v_inv_scale, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
+  if (src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (kv_dtype != src_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
+  if (kv_dtype == PA_FP8_E4M3 && (!k_inv_scale || !v_inv_scale)) return PA_ERR_NULL;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_stride < row || v_stride < row) return PA_ERR_SHAPE;
+  if (!aligned16(k) || !aligned16(v) || (k_stride * 2) % 16 != 0 || (v_stride * 2) % 16 != 0 ||
+      !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ALIGN;
+  if (static_cast<int64_t>(num_tokens) * num_kv_heads * 2 / 8 >= (int64_t{1} << 31)) return PA_ERR_SHAPE;
+  unsigned int* err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  pa::ReshapeArgs a;
+  a.err = err;
+  a.k = k;
+  a.v = v;
+  a.src_dtype = src_dtype;
+  a.k_stride = k_stride;
+  a.v_stride = v_stride;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.kv_dtype = kv_dtype;
+  a.num_blocks = num_blocks;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.k_inv_scale = k_inv_scale;
+  a.v_inv_scale = v_inv_scale;
+  const cudaError_t e = pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, size_t block_bytes,
+                             const int32_t* src_dst_pairs, int num_pairs, void* stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || block_bytes == 0) return PA_ERR_SHAPE;
+  if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;
+  if (block_bytes % 16 != 0) return PA_ERR_ALIGN;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_NULL;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  unsigned int* err = device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, num_blocks, static_cast<int64_t>(block_bytes),
+                                               src_dst_pairs, num_pairs, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_EXPORT int pa_get_device_error(void* stream, unsigned int* error_bits) {
+  if (!error_bits) return PA_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int h = 0u;
+  if (cudaMemcpyFromSymbolAsync(&h, g_device_error, sizeof(h), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  const unsigned int zero = 0u;
+  if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  *error_bits = h;
+  return PA_OK;
+}

@@ -1,0 +1,83 @@
+// pa_kernels.h - internal launch interface between the C ABI (pa_api.cu) and
+// the kernels.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct ReshapeArgs {
+  const void* k;
+  const void* v;
+  int src_dtype;
+  int64_t k_stride;
+  int64_t v_stride;
+  void* k_cache;
+  void* v_cache;
+  int kv_dtype;
+  int64_t num_blocks;
+  const int64_t* slot_mapping;
+  int num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  const float* k_inv_scale;
+  const float* v_inv_scale;
+  unsigned int* err;
+};
+
+cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, int64_t block_bytes,
+                               const int32_t* pairs, int num_pairs, unsigned int* err, cudaStream_t stream);
+
+// Everything the decode kernel reads besides the two tensor maps.
+struct DecodeParams {
+  void* out;
+  int out_dtype;
+  const void* q;
+  int64_t q_stride;             // elements between consecutive sequences of q
+  const float* k_scale;         // FP8 only
+  const float* v_scale;         // FP8 only
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  int64_t num_blocks;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int group;                    // query heads per KV head (<= compiled maximum)
+  float qk_scale_log2;          // softmax scale * log2(e)
+  int partition_blocks;         // 0: balanced split; >0: fixed partitions of this many blocks
+  float* part_records;          // split-K partial records (workspace)
+  int* seg_counters;            // [num_seqs * num_kv_heads] arrival counters (workspace)
+  unsigned int* err;            // per-device error word
+};
+
+// Compile-time variant of the decode kernel.
+struct DecodeKey {
+  int q_dtype;    // PA_F16 / PA_BF16
+  int kv_dtype;   // PA_F16 / PA_BF16 / PA_FP8_E4M3
+  int head_dim;   // 64 / 128
+  int block_size; // 16 / 32
+  int gmax;       // 1 / 4 / 8 (query heads per KV head, rounded up)
+};
+
+// Launch geometry of one variant on the current device.
+struct DecodeGeometry {
+  int warps_per_cta;
+  int ctas;            // resident CTAs over the whole device
+  size_t smem_bytes;   // dynamic shared memory per CTA
+  int record_floats;   // floats per partial record
+};
+
+// Fills `geo` for `key` and `num_seqs` on the current device; false if the
+// variant is not compiled in or the device cannot run it.
+bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo);
+
+cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,
+                          const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,107 @@
+"""Helpers shared by the GPU tests, smoke() and bench: run one decode case on
+the CUDA path (through the C ABI) and on the oracle, from the same inputs."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import workloads
+
+TORCH_DT = {"f16": "float16", "bf16": "bfloat16", "e4m3": "uint8", "f32": "float32"}
+PA_TOL = 2e-3          # max-abs error bound for attention outputs (fp32 out)
+
+
+def to_torch(x: np.ndarray, fmt: str, device):
+    import torch
+    if fmt == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
+    if fmt == "e4m3":
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint8)).to(device)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def to_numpy(t, fmt: str) -> np.ndarray:
+    import torch
+    t = t.detach().cpu()
+    if fmt == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def out_tolerance(ref: np.ndarray, out_fmt: str) -> np.ndarray:
+    """2e-3 plus half an ulp of the reference in the output type."""
+    if out_fmt == "f32":
+        return np.full(ref.shape, PA_TOL)
+    if out_fmt == "f16":
+        spacing = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+    else:  # bf16: 8 significant bits
+        e = np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126)))
+        spacing = 2.0 ** (e - 7)
+    return PA_TOL + 0.5 * spacing
+
+
+def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda"):
+    """Fill the cache (FP8: quantising writes), append the new token, decode.
+
+    Returns (out float64 numpy, k_cache numpy, v_cache numpy, device error bits).
+    """
+    import torch
+    import paged_kv_cache_144_gb300 as pa
+
+    kv = batch.kv_fmt
+    B = batch.block_size
+    q = to_torch(vals["q"], batch.q_fmt, device)
+    kc = to_torch(vals["k_cache"], kv, device)
+    vc = to_torch(vals["v_cache"], kv, device)
+    src_fmt = batch.q_fmt if kv == "e4m3" else kv
+    ks = vs = kis = vis = None
+    if kv == "e4m3":
+        ks = torch.from_numpy(vals["k_scale"]).to(device)
+        vs = torch.from_numpy(vals["v_scale"]).to(device)
+        kis = torch.from_numpy(vals["k_inv_scale"]).to(device)
+        vis = torch.from_numpy(vals["v_inv_scale"]).to(device)
+        slots = torch.from_numpy(vals["src_slots"]).to(device)
+        pa.reshape_and_cache(to_torch(vals["k_src"], "bf16", device), to_torch(vals["v_src"], "bf16", device),
+                             kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis)
+    new_slots = torch.from_numpy(batch.new_slots).to(device)
+    pa.reshape_and_cache(to_torch(vals["k_new"], src_fmt, device), to_torch(vals["v_new"], src_fmt, device),
+                         kc, vc, new_slots, B, k_inv_scale=kis, v_inv_scale=vis)
+    tables = torch.from_numpy(batch.block_tables).to(device)
+    lens = torch.from_numpy(batch.seq_lens).to(device)
+    out = torch.empty((batch.num_seqs, batch.num_heads, batch.head_dim), dtype=getattr(torch, TORCH_DT[out_fmt]),
+                      device=device)
+    ws = None
+    if workspace == "auto":
+        n = pa.decode_workspace_bytes(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, B,
+                                      batch.max_blocks_per_seq, partition_size, pa.dtype_code(kc))
+        ws = pa.new_workspace(n, device) if n else None
+    pa.decode(out, q, kc, vc, tables, lens, batch.num_kv_heads, batch.scale, B, k_scale=ks, v_scale=vs,
+              partition_size=partition_size, workspace=ws)
+    err = pa.get_device_error()
+    return (out.float().cpu().numpy().astype(np.float64), to_numpy(kc, kv), to_numpy(vc, kv), err)
+
+
+def run_oracle(batch, vals):
+    """Oracle caches after the same writes, and the oracle attention output."""
+    kv = batch.kv_fmt
+    B = batch.block_size
+    kc, vc = vals["k_cache"], vals["v_cache"]
+    src_fmt = batch.q_fmt if kv == "e4m3" else kv
+    kis = vals.get("k_inv_scale")
+    vis = vals.get("v_inv_scale")
+    if kv == "e4m3":
+        kc, vc = oracle.reshape_and_cache(vals["k_src"], vals["v_src"], kc, vc, vals["src_slots"], B,
+                                          src_fmt="bf16", kv_fmt="e4m3", k_inv_scale=kis, v_inv_scale=vis)
+    kc, vc = oracle.reshape_and_cache(vals["k_new"], vals["v_new"], kc, vc, batch.new_slots, B,
+                                      src_fmt=src_fmt, kv_fmt=kv, k_inv_scale=kis, v_inv_scale=vis)
+    ref = oracle.paged_decode_attention(vals["q"], kc, vc, batch.block_tables, batch.seq_lens, batch.scale, B,
+                                        q_fmt=batch.q_fmt, kv_fmt=kv, k_scale=vals.get("k_scale"),
+                                        v_scale=vals.get("v_scale"))
+    return ref, kc, vc
+
+
+def bits_equal(a: np.ndarray, b: np.ndarray) -> bool:
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    return a.shape == b.shape and np.array_equal(a.view(np.uint8), b.view(np.uint8))
