@@ -288,7 +288,7 @@ def run_ours(args):
         del vals["k_src"], vals["v_src"]
     pool_bytes = 2 * vals["k_cache"].numel() * vals["k_cache"].element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    replicas = max(2, math.ceil(4 * l2 / pool_bytes) + 1)
+    replicas = args.replicas or max(2, math.ceil(4 * l2 / pool_bytes) + 1)
     caches = [(vals["k_cache"], vals["v_cache"])] + [(vals["k_cache"].clone(), vals["v_cache"].clone())
                                                      for _ in range(replicas - 1)]
     tables = torch.from_numpy(batch.block_tables).to(dev)
@@ -301,6 +301,8 @@ def run_ours(args):
     nws = pa.decode_workspace_bytes(S, Hq, Hkv, D, B, batch.max_blocks_per_seq, args.partition_size,
                                     pa.dtype_code(vals["k_cache"]))
     ws = pa.new_workspace(nws, dev) if nws else None
+    geometry = pa.pa_decode_launch_config(S, Hq, Hkv, D, B, batch.max_blocks_per_seq, args.partition_size,
+                                          pa.dtype_code(q), pa.dtype_code(vals["k_cache"]))
     no_pairs = torch.empty((0, 2), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -408,6 +410,7 @@ def run_ours(args):
             "step": "reshape_and_cache(1 new token/seq) + pa_decode",
             "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
             "seed": args.seed,
+            "launch": geometry,
         },
         "pct_of_hbm_peak": round(100.0 * value / peaks["hbm_gbs"], 2),
         "kv_read_gbps": round(total_kv / (ms_step * 1e-3) / 1e9, 2),
@@ -504,6 +507,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_32x4k", choices=["tiny", "gqa_32x4k", "long_32k", "fp8_mix"])
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--replicas", type=int, default=0, help="KV pool replicas to rotate (0 = enough for > 4x L2)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

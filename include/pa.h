@@ -33,7 +33,8 @@
  *    "PagedAttentionのメモリ管理": the block table maps logical blocks to
  *    physical blocks of B tokens).
  *  - Supported shapes: head_dim in {64, 128} for 16-bit caches, 128 for FP8;
- *    block_size in {16, 32}; num_heads = G * num_kv_heads with 1 <= G <= 8.
+ *    block_size a power of two from 8 to 1024 (16 and 32 are the usual sizes);
+ *    num_heads = G * num_kv_heads with 1 <= G <= 8.
  */
 #ifndef PAGEDATTN_PA_H
 #define PAGEDATTN_PA_H
@@ -132,6 +133,16 @@ int pa_decode(void* out, pa_dtype out_dtype,
               void* stream);
 
 /*
+ * pa_decode_launch_config - the launch geometry pa_decode uses for these
+ * sizes on the current device (introspection; nothing is launched).
+ * Outputs (host pointers): resident CTAs over the device, warps per CTA,
+ * K/V pipeline stages per warp and dynamic shared memory per CTA.
+ */
+int pa_decode_launch_config(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int partition_size, pa_dtype q_dtype, pa_dtype kv_dtype,
+                            int* ctas, int* warps_per_cta, int* stages, size_t* smem_bytes);
+
+/*
  * pa_reshape_and_cache - write new tokens' K and V rows into their slots.
  *
  * [P2] "PagedAttention: OS仮想メモリ式の管理": blocks are handed out as tokens
@@ -186,6 +197,10 @@ const char* pa_status_string(int status);
  * *error_bits (host pointer) receives the bits.
  */
 int pa_get_device_error(void* stream, unsigned int* error_bits);
+
+/* Text of the CUDA error behind the last PA_ERR_CUDA returned on this
+ * thread ("" if none); a static thread-local string. */
+const char* pa_last_error_detail(void);
 
 /* Library ABI version (major*100 + minor). */
 int pa_version(void);

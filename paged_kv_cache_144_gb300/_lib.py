@@ -33,6 +33,10 @@ _SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_get_device_error": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "pa_version": (_i32, []),
+    "pa_last_error_detail": (ctypes.c_char_p, []),
+    "pa_decode_launch_config": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                       ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]),
 }
 
 _LIB = None
@@ -77,7 +81,10 @@ def status_string(status: int) -> str:
 
 def _check(fn: str, status: int) -> None:
     if status != PA_OK:
-        raise PagedAttnError(fn, status, status_string(status))
+        msg = status_string(status)
+        if status == PA_ERR_CUDA:
+            msg += ": " + load().pa_last_error_detail().decode()
+        raise PagedAttnError(fn, status, msg)
 
 
 # ----------------------------------------------------------------------------- raw C-ABI calls
@@ -104,6 +111,15 @@ def pa_get_device_error(stream) -> int:
     bits = ctypes.c_uint(0)
     _check("pa_get_device_error", int(load().pa_get_device_error(stream, ctypes.byref(bits))))
     return int(bits.value)
+
+
+def pa_decode_launch_config(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                            partition_size, q_dtype, kv_dtype) -> dict:
+    c, w, ns, sm = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    _check("pa_decode_launch_config", int(load().pa_decode_launch_config(
+        num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, partition_size, q_dtype,
+        kv_dtype, ctypes.byref(c), ctypes.byref(w), ctypes.byref(ns), ctypes.byref(sm))))
+    return {"ctas": c.value, "warps_per_cta": w.value, "stages": ns.value, "smem_bytes": sm.value}
 
 
 def pa_version() -> int:

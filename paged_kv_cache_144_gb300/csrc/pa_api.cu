@@ -3,6 +3,8 @@
 // the kernels.  No call here allocates device memory.
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -30,6 +32,15 @@ unsigned int* device_error_word() {
     addr[dev] = static_cast<unsigned int*>(p);
   }
   return addr[dev];
+}
+
+// Text of the last CUDA error a call on this thread returned PA_ERR_CUDA for.
+thread_local char g_last_error[512] = "";
+
+int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return PA_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+  return PA_ERR_CUDA;
 }
 
 constexpr int kMaxSeqs = 16384;  // prefix sums of the batch live in shared memory
@@ -60,18 +71,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view of a cache pool: rows of head_dim elements, num_blocks*Hkv*B rows;
-// one TMA box = 128 bytes of a row x block_size rows, 128-byte swizzle.
+// 3-D view of a cache pool: {128-byte half of a row, halves, rows}, with
+// num_blocks*Hkv*B rows of head_dim elements.  One TMA box = box_rows whole
+// rows, 128-byte swizzle, landing in shared memory row after row.
 bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, int num_kv_heads,
-                      int block_size, int head_dim, int elem_bytes) {
+                      int block_size, int head_dim, int elem_bytes, int box_rows) {
+  if (box_rows % pa::kBoxRowQuantum != 0 || box_rows > 256) return false;
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim),
-                        static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elem_bytes};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(block_size)};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+  const int row_bytes = head_dim * elem_bytes;
+  if (row_bytes % 128 != 0) return false;
+  const cuuint32_t half_elems = static_cast<cuuint32_t>(128 / elem_bytes);
+  const cuuint32_t halves = static_cast<cuuint32_t>(row_bytes / 128);
+  cuuint64_t dims[3] = {half_elems, halves, static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[3] = {half_elems, halves, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                          const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -79,6 +95,15 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, i
 }
 
 int gmax_for_group(int g) { return g <= 1 ? 1 : (g <= 4 ? 4 : 8); }
+
+// Rows per work unit (measured on GB300): 16 for 16-bit caches (two lanes
+// per token in QK), 32 for FP8 caches (one lane per 128-byte row).
+// PA_DECODE_UNIT_ROWS (16 or 32) overrides it (tuning).
+int unit_rows_for(int kv_dtype, int /*gmax*/) {
+  const int env = pa::tuning_override("PA_DECODE_UNIT_ROWS");
+  if (env == 16 || env == 32) return env;
+  return kv_dtype == PA_FP8_E4M3 ? 32 : 16;
+}
 
 // Shape checks shared by pa_decode and pa_decode_workspace_bytes.
 int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -88,17 +113,20 @@ int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_d
   if (num_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (kv_dtype == PA_FP8_E4M3 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+  // a power of two from 8 to 1024: a work unit (16 or 32 rows) then covers
+  // whole blocks or a whole fraction of one
+  if (block_size < 8 || block_size > 1024 || (block_size & (block_size - 1)) != 0) return PA_ERR_UNSUPPORTED;
   if (partition_size < 0 || (partition_size > 0 && partition_size % block_size != 0)) return PA_ERR_SHAPE;
   if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(num_seqs) * num_kv_heads * max_blocks_per_seq >= (int64_t{1} << 31)) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(num_seqs) * num_kv_heads * max_blocks_per_seq * block_size / 8 >= (int64_t{1} << 31))
+    return PA_ERR_SHAPE;
   return PA_OK;
 }
 
 struct DecodePlan {
   pa::DecodeKey key;
   pa::DecodeGeometry geo;
-  int partition_blocks;     // as passed to the kernel (0 = balanced)
+  int partition_units;      // as passed to the kernel (0 = balanced), in 8-row units
   size_t counters_bytes;
   size_t records;
   size_t bytes;             // total workspace bytes required
@@ -111,24 +139,26 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
   plan->key.q_dtype = q_dtype;
   plan->key.kv_dtype = kv_dtype;
   plan->key.head_dim = head_dim;
-  plan->key.block_size = block_size;
   plan->key.gmax = gmax_for_group(num_heads / num_kv_heads);
+  plan->key.unit_rows = unit_rows_for(kv_dtype, plan->key.gmax);
   if (!pa::decode_geometry(plan->key, num_seqs, &plan->geo)) return PA_ERR_UNSUPPORTED;
-  int pb = partition_size / block_size;
-  if (partition_size == 0 && !have_ws) pb = max_blocks_per_seq;  // single pass without workspace
-  if (pb >= max_blocks_per_seq) pb = max_blocks_per_seq;
-  plan->partition_blocks = pb;
-  if (pb == max_blocks_per_seq) {  // one fragment per segment: no partial records
+  const int ur = plan->geo.unit_rows;
+  const int max_units = static_cast<int>((static_cast<int64_t>(max_blocks_per_seq) * block_size + ur - 1) / ur);
+  int pu = (partition_size + ur - 1) / ur;  // fixed partitions rounded up to whole units
+  if (partition_size == 0 && !have_ws) pu = max_units;  // single pass without workspace
+  if (pu >= max_units) pu = max_units;
+  plan->partition_units = pu;
+  if (pu == max_units) {  // one fragment per segment: no partial records
     plan->counters_bytes = 0;
     plan->records = 0;
     plan->bytes = 0;
     return PA_OK;
   }
   plan->counters_bytes = (static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int) + 255) / 256 * 256;
-  if (pb == 0) {
+  if (pu == 0) {
     plan->records = 2ull * plan->geo.ctas * plan->geo.warps_per_cta;
   } else {
-    plan->records = static_cast<size_t>(num_seqs) * num_kv_heads * ((max_blocks_per_seq + pb - 1) / pb);
+    plan->records = static_cast<size_t>(num_seqs) * num_kv_heads * ((max_units + pu - 1) / pu);
   }
   plan->bytes = plan->counters_bytes + plan->records * plan->geo.record_floats * sizeof(float);
   return PA_OK;
@@ -137,6 +167,8 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
 }  // namespace
 
 PA_EXPORT int pa_version(void) { return 100; }
+
+PA_EXPORT const char* pa_last_error_detail(void) { return g_last_error; }
 
 PA_EXPORT const char* pa_status_string(int status) {
   switch (status) {
@@ -167,6 +199,27 @@ PA_EXPORT size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_
   return plan.bytes;
 }
 
+PA_EXPORT int pa_decode_launch_config(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int partition_size, pa_dtype q_dtype,
+                                      pa_dtype kv_dtype, int* ctas, int* warps_per_cta, int* stages,
+                                      size_t* smem_bytes) {
+  const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                    partition_size, kv_dtype);
+  if (sh != PA_OK) return sh;
+  if (!ctas || !warps_per_cta || !stages || !smem_bytes) return PA_ERR_NULL;
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
+  DecodePlan plan;
+  const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                           partition_size, q_dtype, kv_dtype, true, &plan);
+  if (pr != PA_OK) return pr;
+  *ctas = plan.geo.ctas;
+  *warps_per_cta = plan.geo.warps_per_cta;
+  *stages = plan.geo.stages;
+  *smem_bytes = plan.geo.smem_bytes;
+  return PA_OK;
+}
+
 PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
                         const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
                         const float* k_scale, const float* v_scale, const int32_t* block_tables,
@@ -195,8 +248,9 @@ PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q
 
   CUtensorMap tk, tv;
   const int eb = dtype_bytes(kv_dtype);
-  if (!encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim, eb) ||
-      !encode_cache_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, eb))
+  const int box_rows = block_size < plan.geo.unit_rows ? block_size : plan.geo.unit_rows;
+  if (!encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim, eb, box_rows) ||
+      !encode_cache_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, eb, box_rows))
     return PA_ERR_CUDA;
 
   unsigned int* err = device_error_word();
@@ -218,12 +272,20 @@ PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q
   p.num_kv_heads = num_kv_heads;
   p.group = num_heads / num_kv_heads;
   p.qk_scale_log2 = scale * 1.4426950408889634f;
-  p.partition_blocks = plan.partition_blocks;
+  p.block_size = block_size;
+  p.block_shift = __builtin_ctz(static_cast<unsigned>(block_size));
+  p.partition_units = plan.partition_units;
+  p.stages = plan.geo.stages;
   p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)
                               : nullptr;
-  const cudaError_t e = pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const int st = cuda_status(pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream)),
+                              "pa_decode launch");
+  if (st != PA_OK) {
+    const size_t n = strlen(g_last_error);
+    snprintf(g_last_error + n, sizeof(g_last_error) - n, "; %s", pa::launch_failure_note());
+  }
+  return st;
 }
 
 PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype, int64_t k_stride,
@@ -264,8 +326,8 @@ PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dt
   a.block_size = block_size;
   a.k_inv_scale = k_inv_scale;
   a.v_inv_scale = v_inv_scale;
-  const cudaError_t e = pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return cuda_status(pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream)),
+                     "pa_reshape_and_cache launch");
 }
 
 PA_EXPORT int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, size_t block_bytes,
@@ -278,9 +340,9 @@ PA_EXPORT int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, s
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
   unsigned int* err = device_error_word();
   if (!err) return PA_ERR_CUDA;
-  const cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, num_blocks, static_cast<int64_t>(block_bytes),
-                                               src_dst_pairs, num_pairs, err, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return cuda_status(pa::launch_copy_blocks(k_cache, v_cache, num_blocks, static_cast<int64_t>(block_bytes),
+                                            src_dst_pairs, num_pairs, err, static_cast<cudaStream_t>(stream)),
+                     "pa_copy_blocks launch");
 }
 
 PA_EXPORT int pa_get_device_error(void* stream, unsigned int* error_bits) {

@@ -120,6 +120,7 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
       a.k, a.v, a.k_stride, a.v_stride, a.k_cache, a.v_cache, a.num_blocks, a.slot_mapping,     \
       a.num_tokens, a.num_kv_heads, a.block_size, a.k_inv_scale, a.v_inv_scale, a.err)
   const bool fp8 = a.kv_dtype == PA_FP8_E4M3;
+  (void)cudaGetLastError();
   if (a.src_dtype == PA_F16) {
     if (fp8) { if (a.head_dim == 128) PA_RC_LAUNCH(f16_t, true, 128); else PA_RC_LAUNCH(f16_t, true, 64); }
     else { if (a.head_dim == 128) PA_RC_LAUNCH(f16_t, false, 128); else PA_RC_LAUNCH(f16_t, false, 64); }
@@ -136,6 +137,7 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,
   if (num_pairs == 0) return cudaSuccess;
   const int64_t chunks = (block_bytes + kCopyBytesPerCta - 1) / kCopyBytesPerCta;
   dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(num_pairs), 2);
+  (void)cudaGetLastError();
   copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint8_t*>(k_cache),
                                                          static_cast<uint8_t*>(v_cache), num_blocks,
                                                          block_bytes, pairs, err);

@@ -5,30 +5,34 @@
 // sequence s and query head h,
 //     out[s,h] = softmax(scale * K_s q[s,h]) V_s,
 // where the rows of K_s / V_s are scattered over physical blocks of B tokens
-// that the sequence's block table names.  Blocks are consumed one at a time
+// that the sequence's block table names.  Rows are consumed a tile at a time
 // and folded into a running (m, l, acc) state with the online-softmax
 // recurrence (equation (4) of the auturnal.com review: m' = max(m, max s_j),
 // l' = e^{m-m'} l + sum e^{s_j-m'}, acc rescaled by the same factor); the
 // recurrence runs in base 2 with log2(e) folded into the query.
 //
 // How it is laid out on GB300 (this is not the pages' A100 kernel design):
-//  * Work unit = one (sequence, KV head, block) triple.  The units of the
-//    whole batch, ordered (s, kvh, block), are split into equal contiguous
-//    ranges, one per resident warp (152 SMs x occupancy x 4 warps), so long
-//    and short sequences load every SM equally ("balanced" mode).  A range
-//    crosses (s, kvh) segments freely.  Optionally each warp instead takes
-//    fixed partitions of P tokens (the pages' "V2" style).
-//  * Each warp owns a private ring of NS stages in shared memory and streams
-//    the K and V tiles of its units into it with 2-D TMA copies
-//    (cp.async.bulk.tensor, 128-byte swizzle) completing on one mbarrier per
-//    stage; the query group of a new segment rides on the same barrier as a
-//    1-D bulk copy.  No CTA-wide barrier is used after the prologue.
-//  * QK: each lane owns one token of the 16/32-token tile (two lanes per
-//    token for B=16, one d-half each) and forms the dot products of all G
-//    query heads of the group with packed fp32x2 FMAs; the query group sits
-//    pre-scaled in fp32 in shared memory (broadcast reads); the swizzle makes
-//    the per-lane K row reads bank-conflict free.
-//  * PV: each lane owns D/32 output columns for all G heads (fp32 registers)
+//  * Work unit = UR (16 or 32) consecutive rows of one (sequence, KV head).
+//    A unit is filled by 3-D TMA boxes of min(UR, B) whole rows (each row is
+//    one or two 128-byte halves, 128-byte swizzle): part of one block when
+//    B >= UR, one box per block when a unit spans several blocks; one TMA
+//    instruction per box for K and one for V.  The units of the whole
+//    batch, ordered (s, kvh, unit), are split into equal contiguous ranges, one
+//    per resident warp, so long and short sequences load every SM equally
+//    ("balanced" mode).  A range crosses (s, kvh) segments freely.  Optionally
+//    each warp instead takes fixed partitions of P tokens.
+//  * Each warp owns a private ring of stages in shared memory (one unit of K
+//    and of V per stage) filled by TMA copies (cp.async.bulk.tensor) that
+//    complete on one mbarrier per stage; the query group of a new segment
+//    rides on the same barrier as a 1-D bulk copy.  No CTA-wide barrier is
+//    used after the prologue.
+//  * QK: 32/UR lanes per token (one for UR=32), each a part of the row, form
+//    the dot products with all G query heads of the group in packed fp32x2
+//    FMAs (several independent accumulators per head); the pre-scaled fp32
+//    query group is read from shared memory with broadcasts; the lane ->
+//    (token, half) order is chosen so that, with the swizzle, every quarter
+//    warp's K reads hit distinct banks.
+//  * PV: each lane owns D/32 output columns of all G heads (fp32 registers)
 //    and walks the tile's valid tokens, reading p from shared memory.
 //  * FP8 tiles are widened in registers (e4m3 -> f16x2 -> f32); the per-head
 //    K scale is folded into the query and the V scale into the final divide.
@@ -42,51 +46,68 @@
 //    returns.
 #pragma once
 
+#include <type_traits>
+
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
 namespace pa {
 
-constexpr int kMinUnitsPerWarp = 8;
+constexpr int kMinUnitsPerWarp = 16;           // smallest balanced share (128 rows)
+constexpr int kStageBytesPerWarp = 12 * 1024;  // default K/V pipeline bytes per warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Integer tuning override from the environment (read once per name), or -1.
+int tuning_override(const char* name);
+
+// Records the geometry and kernel attributes of a rejected launch (error detail).
+void note_launch_failure(int ctas, int threads, size_t smem, int stages, int max_threads, int max_dyn_smem,
+                         int regs, size_t local_bytes);
 
 __host__ __device__ constexpr int align_up_c(int x, int a) { return (x + a - 1) / a * a; }
 
-template <typename QT, typename KVT, int D, int BS, int GM>
+template <typename QT, typename KVT, int D, int GM, int UR_>
 struct DecodeTraits {
   static constexpr int KVB = elem<KVT>::bytes;
   static constexpr int ROW = D * KVB;  // bytes of one cache row
   static_assert(ROW == 128 || ROW == 256, "cache rows must be 128 or 256 bytes");
-  static_assert(BS == 16 || BS == 32, "block size 16 or 32");
-  static constexpr int NSUB = ROW / 128;         // 128-byte sub-tiles per row
-  static constexpr int SUB_ELEMS = 128 / KVB;    // elements per sub-tile row
-  static constexpr int TILE = BS * ROW;          // bytes of one (block, head) tile
+  static constexpr int UR = UR_;                 // rows per work unit (16 or 32)
+  static_assert(UR == 16 || UR == 32, "unit rows");
+  static constexpr int NSUB = ROW / 128;         // 128-byte halves per row
+  static constexpr int SUB_ELEMS = 128 / KVB;    // elements per half
+  static constexpr int TILE = UR * ROW;          // bytes of one unit of K (or V)
   static constexpr int STAGE = 2 * TILE;         // K tile + V tile
-  static constexpr int NS = (STAGE <= 4096) ? 4 : (STAGE <= 8192 ? 2 : 2);
-  static constexpr int W = 4;                    // warps per CTA
-  static constexpr int LPT = 32 / BS;            // lanes per token in QK
+  static constexpr int MAX_NS = 8;               // stages per warp (chosen at launch, 2..MAX_NS)
+  static constexpr int MAX_W = 8;                // warps per CTA (chosen at launch, <= MAX_W)
+  static constexpr int LPT = 32 / UR;            // lanes per token in QK (2 or 1)
   static constexpr int CHUNKS = ROW / 16;        // 16-byte chunks per row
-  static constexpr int CPL = CHUNKS / LPT;       // chunks per lane in QK
   static constexpr int EPC = 16 / KVB;           // elements per chunk
   static constexpr int EPL = D / 32;             // PV columns per lane
-  static constexpr int HALF = D / LPT;           // row elements one QK lane covers
-  static constexpr int QPAD = (LPT == 2) ? 4 : 0;  // keeps the two halves in other banks
-  static constexpr int QROW = LPT * (HALF + QPAD);  // floats per head in q smem
+  // The query group lives in shared memory as NPART padded parts per head:
+  // the part a QK lane reads (LPT = 2) or the half it reads (LPT = 1).
+  static constexpr int NPART = (LPT == 2 || NSUB == 2) ? 2 : 1;
+  static constexpr int PART = D / NPART;         // elements per part
+  static constexpr int CPP = CHUNKS / NPART;     // chunks per part
+  static constexpr int QROW = NPART * (PART + 4);  // floats per head (4 floats of padding per part)
   static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
-  static constexpr int OFF_QRAW = NS * STAGE;
-  static constexpr int OFF_QF32 = OFF_QRAW + 2 * align_up_c(QRAW, 128);
+  static constexpr int NACC = (GM >= 8) ? 2 : 4;  // independent QK accumulators per head
+  // per-warp shared memory: [raw q x2 | fp32 q | p | mbarriers | NS stages]
+  static constexpr int OFF_QRAW = 0;
+  static constexpr int QRAW_STRIDE = align_up_c(QRAW, 128);
+  static constexpr int OFF_QF32 = OFF_QRAW + 2 * QRAW_STRIDE;
   static constexpr int OFF_PBUF = OFF_QF32 + GM * QROW * 4;
-  static constexpr int OFF_BAR = OFF_PBUF + BS * GM * 8;
-  static constexpr int WARP_SMEM = align_up_c(OFF_BAR + NS * 8, 1024);
+  static constexpr int OFF_BAR = OFF_PBUF + UR * GM * 8;
+  static constexpr int OFF_STAGES = align_up_c(OFF_BAR + MAX_NS * 8, 1024);
+  __host__ __device__ static constexpr int warp_smem(int ns) { return OFF_STAGES + ns * STAGE; }
   static constexpr int REC = align_up_c(GM * (D + 2), 4);  // floats per partial record
   static_assert(EPL == 2 || EPL == 4, "D/32 columns per lane");
+  static_assert(EPC % 4 == 0 && PART % 4 == 0, "chunk split");
 };
 
 // Length of sequence s clamped to the table's capacity (error bit if outside).
-template <int BS>
 __device__ __forceinline__ int clamped_len(const DecodeParams& p, int s, bool report) {
   int T = __ldg(p.seq_lens + s);
-  const int cap = p.max_blocks_per_seq * BS;
+  const int cap = p.max_blocks_per_seq * p.block_size;
   if (T < 0 || T > cap) {
     if (report) raise_error(p.err, PA_DEVERR_SEQ_LEN);
     T = T < 0 ? 0 : cap;
@@ -94,16 +115,17 @@ __device__ __forceinline__ int clamped_len(const DecodeParams& p, int s, bool re
   return T;
 }
 
-// Fragment = a run of consecutive blocks [j, jend) of segment (s, kvh) that a
+// Fragment = a run of consecutive units [j, jend) of segment (s, kvh) that a
 // warp processes.  Walks either the warp's balanced unit range or its fixed
 // partitions.
 struct WorkIter {
-  int s, kvh, j, jend, j0, nb, T;
+  int s, kvh, j, jend, j0, nu, T;
+  int nblk;       // blocks that hold rows of sequence s
   int frag_idx;   // ordinal of the current fragment within this warp
   int slot;       // partial-record slot, -1 when the fragment is a whole segment
   bool valid;
   // balanced mode
-  long long u, u1;  // unit of block j0 of the current fragment; end of the warp's range
+  long long u, u1;  // unit index of unit j0 of the current fragment; end of the warp's range
   int gw;           // global warp id
   // fixed mode
   int r, rstride, R;
@@ -119,28 +141,27 @@ __device__ __forceinline__ int find_seq(const int* prefix, int S, long long u) {
   return lo;
 }
 
-template <int BS>
 __device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p) {
   const int Hkv = p.num_kv_heads;
   const int s = find_seq(prefix, p.num_seqs, it.u);
-  const int nb = (prefix[s + 1] - prefix[s]) / Hkv;
+  const int nu = (prefix[s + 1] - prefix[s]) / Hkv;
   const long long r = it.u - prefix[s];
   it.s = s;
-  it.nb = nb;
-  it.kvh = static_cast<int>(r / nb);
-  it.j0 = static_cast<int>(r % nb);
+  it.nu = nu;
+  it.kvh = static_cast<int>(r / nu);
+  it.j0 = static_cast<int>(r % nu);
   it.j = it.j0;
-  const long long seg_start = prefix[s] + static_cast<long long>(it.kvh) * nb;
-  const long long seg_end = seg_start + nb;
+  const long long seg_start = prefix[s] + static_cast<long long>(it.kvh) * nu;
+  const long long seg_end = seg_start + nu;
   const long long fend = min(it.u1, seg_end);
   it.jend = it.j0 + static_cast<int>(fend - it.u);
   const bool whole = (it.u == seg_start) && (fend == seg_end);
   it.slot = whole ? -1 : it.gw * 2 + (it.frag_idx == 0 ? 0 : 1);
-  it.T = clamped_len<BS>(p, s, false);
+  it.T = clamped_len(p, s, false);
+  it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
 }
 
-template <int BS>
-__device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, const DecodeParams& p) {
+__device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, const DecodeParams& p, int UR) {
   const int Hkv = p.num_kv_heads;
   const int s = find_seq(prefix, p.num_seqs, it.r);
   const int parts = (prefix[s + 1] - prefix[s]) / Hkv;
@@ -148,47 +169,58 @@ __device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, cons
   it.s = s;
   it.kvh = rr / parts;
   const int part = rr % parts;
-  it.T = clamped_len<BS>(p, s, false);
-  it.nb = (it.T + BS - 1) / BS;
-  it.j0 = part * p.partition_blocks;
+  it.T = clamped_len(p, s, false);
+  it.nu = (it.T + UR - 1) / UR;
+  it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
+  it.j0 = part * p.partition_units;
   it.j = it.j0;
-  it.jend = min(it.nb, it.j0 + p.partition_blocks);
+  it.jend = min(it.nu, it.j0 + p.partition_units);
   it.slot = (parts == 1) ? -1 : it.r;
 }
 
-template <int BS>
 __device__ __forceinline__ void iter_next_fragment(WorkIter& it, const int* prefix, const DecodeParams& p,
-                                                   bool fixed) {
+                                                   bool fixed, int UR) {
   it.frag_idx++;
   if (fixed) {
     it.r += it.rstride;
     if (it.r >= it.R) { it.valid = false; return; }
-    frag_fixed<BS>(it, prefix, p);
+    frag_fixed(it, prefix, p, UR);
   } else {
     it.u += it.jend - it.j0;
     if (it.u >= it.u1) { it.valid = false; return; }
-    frag_balanced<BS>(it, prefix, p);
+    frag_balanced(it, prefix, p);
   }
 }
 
-template <typename QT, typename KVT, int D, int BS, int GM>
-__global__ void __launch_bounds__(DecodeTraits<QT, KVT, D, BS, GM>::W * 32)
+template <typename QT, typename KVT, int D, int GM, int UR_>
+__global__ void __launch_bounds__(DecodeTraits<QT, KVT, D, GM, UR_>::MAX_W * 32, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const DecodeParams p) {
-  using Tr = DecodeTraits<QT, KVT, D, BS, GM>;
+  using Tr = DecodeTraits<QT, KVT, D, GM, UR_>;
   constexpr bool kFp8 = elem<KVT>::bytes == 1;
+  constexpr int UR = Tr::UR;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int W = blockDim.x >> 5;  // warps per CTA
   const int S = p.num_seqs;
   const int Hkv = p.num_kv_heads;
   const int G = p.group;
-  const bool fixed = p.partition_blocks > 0;
+  const int B = p.block_size;
+  // A unit spans part of one block (B >= UR) or several whole blocks (B < UR);
+  // one TMA box per block it touches, BOX rows high.  B is a power of two.
+  const bool unit_in_block = B >= UR;
+  const int BOX = unit_in_block ? UR : B;
+  const int upb_shift = unit_in_block ? p.block_shift - (UR == 32 ? 5 : 4) : 0;  // log2(units per block)
+  const int bpu_shift = unit_in_block ? 0 : (UR == 32 ? 5 : 4) - p.block_shift;  // log2(blocks per unit)
+  const bool fixed = p.partition_units > 0;
 
-  int* prefix = reinterpret_cast<int*>(base + Tr::W * Tr::WARP_SMEM);
+  const int NS = p.stages;  // pipeline depth per warp
+  const int wsm = Tr::warp_smem(NS);
+  int* prefix = reinterpret_cast<int*>(base + W * wsm);
   int* scan_tmp = prefix + (S + 1);
 
   if (threadIdx.x == 0) {
@@ -203,9 +235,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       const int s = b0 + threadIdx.x;
       int units = 0;
       if (s < S) {
-        const int T = clamped_len<BS>(p, s, blockIdx.x == 0);
-        const int nb = (T + BS - 1) / BS;
-        units = (fixed ? (nb + p.partition_blocks - 1) / p.partition_blocks : nb) * Hkv;
+        const int T = clamped_len(p, s, blockIdx.x == 0);
+        const int nu = (T + UR - 1) / UR;
+        units = (fixed ? (nu + p.partition_units - 1) / p.partition_units : nu) * Hkv;
       }
       int x = units;
 #pragma unroll
@@ -216,8 +248,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       if (lane == 31) scan_tmp[warp] = x;
       __syncthreads();
       int wo = 0, tot = 0;
-#pragma unroll
-      for (int w = 0; w < Tr::W; ++w) {
+      for (int w = 0; w < W; ++w) {
         const int v = scan_tmp[w];
         wo += (w < warp) ? v : 0;
         tot += v;
@@ -231,7 +262,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
   // ---- 2. empty sequences attend to nothing: their outputs are zero
   for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
-    if (clamped_len<BS>(p, s, false) == 0) {
+    if (clamped_len(p, s, false) == 0) {
       const int64_t n = static_cast<int64_t>(p.num_heads) * D;
       for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
     }
@@ -239,8 +270,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   __syncthreads();
 
   // ---- 3. this warp's share of the work
-  const int nw_total = gridDim.x * Tr::W;
-  const int gw = blockIdx.x * Tr::W + warp;
+  const int nw_total = gridDim.x * W;
+  const int gw = blockIdx.x * W + warp;
   const long long U = prefix[S];
   WorkIter it;
   it.frag_idx = 0;
@@ -251,7 +282,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     it.R = static_cast<int>(U);
     it.rstride = nw_total;
     it.r = gw;
-    if (it.r < it.R) { it.valid = true; frag_fixed<BS>(it, prefix, p); }
+    if (it.r < it.R) { it.valid = true; frag_fixed(it, prefix, p, UR); }
   } else if (U > 0) {
     const long long want = (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp;
     nw_eff = static_cast<int>(want < nw_total ? want : static_cast<long long>(nw_total));
@@ -259,17 +290,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     if (gw < nw_eff) {
       it.u = gw * U / nw_eff;
       it.u1 = (gw + 1) * U / nw_eff;
-      if (it.u < it.u1) { it.valid = true; frag_balanced<BS>(it, prefix, p); }
+      if (it.u < it.u1) { it.valid = true; frag_balanced(it, prefix, p); }
     }
   }
   if (!it.valid) return;
 
-  uint8_t* wbase = base + warp * Tr::WARP_SMEM;
-  const uint32_t wbase_u32 = base_u32 + warp * Tr::WARP_SMEM;
+  uint8_t* wbase = base + warp * wsm;
+  const uint32_t wbase_u32 = base_u32 + warp * wsm;
   const uint32_t bar0 = wbase_u32 + Tr::OFF_BAR;
   if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < Tr::NS; ++i) mbar_init(bar0 + 8 * i, 1);
+    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8 * i, 1);
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -279,70 +309,233 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   float2* pbuf = reinterpret_cast<float2*>(wbase + Tr::OFF_PBUF);
   const uint8_t* qraw_base = wbase + Tr::OFF_QRAW;
   const uint32_t qraw_u32 = wbase_u32 + Tr::OFF_QRAW;
-  constexpr int kQrawStride = align_up_c(Tr::QRAW, 128);
 
-  // producer state
+  // ---- producer: one TMA unit per free stage, up to NS ahead of the consumer
   WorkIter prod = it;
-  int tb_seq = -1, tb_base = 0, tb_val = -1;  // cached table slice: lane i holds entry tb_base+i
+  int tb_seq = -1, tb_base = 0, tb_val = -1;  // cached table slice: lane i holds block entry tb_base+i
   int issued = 0, consumed = 0;
+  int pst = 0;              // stage the producer fills next
+  int cst = 0, cpar = 0;    // stage and phase parity the consumer waits on next
   bool timed_out = false;
 
+  int tn_base = -1, tn_val = -1;  // next table slice, loaded ahead into registers
+  auto table_entry = [&](int bj) -> int {
+    // warp-collective: physical block of block bj of the producer's sequence
+    const int nb = prod.nblk;
+    const int32_t* row = p.block_tables + static_cast<int64_t>(prod.s) * p.max_blocks_per_seq;
+    if (prod.s != tb_seq || bj < tb_base || bj >= tb_base + 32) {
+      if (prod.s == tb_seq && tn_base == tb_base + 32 && bj >= tn_base && bj < tn_base + 32) {
+        tb_base = tn_base;
+        tb_val = tn_val;
+      } else {
+        tb_seq = prod.s;
+        tb_base = bj;
+        tb_val = (bj + lane < nb) ? __ldg(row + bj + lane) : -1;
+      }
+      tn_base = -1;
+    }
+    if (tn_base < 0 && bj >= tb_base + 8 && tb_base + 32 < nb) {
+      tn_base = tb_base + 32;  // issue the next slice now; it is first used 24 blocks later
+      tn_val = (tn_base + lane < nb) ? __ldg(row + tn_base + lane) : -1;
+    }
+    int phys = __shfl_sync(0xffffffffu, tb_val, bj - tb_base);
+    if (phys < 0 || phys >= p.num_blocks) {
+      if (lane == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+      phys = 0;
+    }
+    return phys;
+  };
+
   auto produce = [&](void) {
-    // Fill free stages while the producer has units and the query slot is free.
-    while (prod.valid && issued - consumed < Tr::NS) {
+    while (prod.valid && issued - consumed < NS) {
       const bool new_frag = (prod.j == prod.j0);
       if (new_frag && prod.frag_idx >= it.frag_idx + 2) break;  // raw-q double buffer busy
-      // block-table entry (warp-collective cached slice)
-      if (prod.s != tb_seq || prod.j < tb_base || prod.j >= tb_base + 32) {
-        tb_seq = prod.s;
-        tb_base = prod.j;
-        const int jj = prod.j + lane;
-        tb_val = (jj < prod.nb) ? __ldg(p.block_tables + static_cast<int64_t>(prod.s) * p.max_blocks_per_seq + jj) : -1;
-      }
-      int phys = __shfl_sync(0xffffffffu, tb_val, prod.j - tb_base);
-      if (phys < 0 || phys >= p.num_blocks) {
-        if (lane == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
-        phys = 0;
-      }
-      if (lane == 0) {
-        const int st = issued % Tr::NS;
-        const uint32_t bar = bar0 + 8 * st;
-        const uint32_t kdst = wbase_u32 + st * Tr::STAGE;
-        const uint32_t vdst = kdst + Tr::TILE;
-        const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
-        mbar_arrive_expect_tx(bar, 2u * Tr::TILE + qbytes);
-        const int row = (phys * Hkv + prod.kvh) * BS;
-#pragma unroll
-        for (int sub = 0; sub < Tr::NSUB; ++sub) {
-          tma_load_2d(kdst + sub * (BS * 128), &tmap_k, sub * Tr::SUB_ELEMS, row, bar);
-          tma_load_2d(vdst + sub * (BS * 128), &tmap_v, sub * Tr::SUB_ELEMS, row, bar);
+      const uint32_t bar = bar0 + 8 * pst;
+      const uint32_t kdst = wbase_u32 + Tr::OFF_STAGES + pst * Tr::STAGE;
+      const uint32_t vdst = kdst + Tr::TILE;
+      // blocks of this unit that hold rows of the sequence (later ones are skipped)
+      const int bj0 = unit_in_block ? (prod.j >> upb_shift) : (prod.j << bpu_shift);
+      const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, prod.nblk - bj0);
+      const int row_in_block = unit_in_block ? (prod.j - (bj0 << upb_shift)) * UR : 0;
+      const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
+      if (lane == 0) mbar_arrive_expect_tx(bar, 2u * nbox * BOX * Tr::ROW + qbytes);
+      for (int i = 0; i < nbox; ++i) {
+        const int phys = table_entry(bj0 + i);
+        if (lane == 0) {
+          const int z = (phys * Hkv + prod.kvh) * B + row_in_block;
+          tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, 0, z, bar);
+          tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, 0, z, bar);
         }
-        if (new_frag) {
-          const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
-                                (static_cast<int64_t>(prod.s) * p.q_stride + static_cast<int64_t>(prod.kvh) * G * D) * 2;
-          bulk_load(qraw_u32 + (prod.frag_idx & 1) * kQrawStride, qsrc, qbytes, bar);
-        }
+      }
+      if (lane == 0 && new_frag) {
+        const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
+                              (static_cast<int64_t>(prod.s) * p.q_stride + static_cast<int64_t>(prod.kvh) * G * D) * 2;
+        bulk_load(qraw_u32 + (prod.frag_idx & 1) * Tr::QRAW_STRIDE, qsrc, qbytes, bar);
       }
       ++issued;
-      if (++prod.j == prod.jend) iter_next_fragment<BS>(prod, prefix, p, fixed);
+      if (++pst == NS) pst = 0;
+      if (++prod.j == prod.jend) iter_next_fragment(prod, prefix, p, fixed, UR);
     }
   };
 
   produce();
 
-  const int t = lane % BS;     // token of this lane in QK
-  const int half = lane / BS;  // d-half of this lane in QK (B=16)
+  // QK lane roles.  LPT = 2: lane pairs share a token (t = lane/2), each one
+  // part of the row (qd = lane & 1).  LPT = 1: one token per lane, visiting
+  // the halves of a 256-byte row in an order rotated by bit 2 of the token.
+  const int t = (Tr::LPT == 2) ? (lane >> 1) : lane;
+  const int qd = (Tr::LPT == 2) ? (lane & 1) : 0;
+  const int rot = (Tr::LPT == 1 && Tr::NPART == 2) ? ((t >> 2) & 1) : 0;
   const int e0 = lane * Tr::EPL;  // first PV column of this lane
-  const int vsub = e0 / Tr::SUB_ELEMS;
-  const int vbyte = (e0 % Tr::SUB_ELEMS) * Tr::KVB;
+  // byte offset of K chunk ch of half h in row t of a stage (128-byte swizzle)
+  auto kaddr = [&](int h, int ch) -> uint32_t {
+    return t * Tr::ROW + h * 128 + (((ch ^ (t * Tr::NSUB + h)) & 7) << 4);
+  };
+  // V: this lane's columns of row r; the swizzle phase repeats every 8/NSUB rows
+  constexpr int VPER = 8 / Tr::NSUB;
+  const int vbyte = e0 * Tr::KVB;
+  const int vh = vbyte >> 7;
+  const int vch = (vbyte & 127) >> 4;
+  uint32_t vofs[VPER];
+#pragma unroll
+  for (int k = 0; k < VPER; ++k) vofs[k] = Tr::TILE + vh * 128 + (((vch ^ (k * Tr::NSUB + vh)) & 7) << 4) + (vbyte & 15);
+  // q parts this lane reads: LPT = 2 -> part qd; LPT = 1 -> parts (pi ^ rot)
+  const float* qpart0 = qf + ((Tr::LPT == 2 ? qd : rot) * (Tr::PART + 4));
+  const float* qpart1 = qf + ((Tr::LPT == 2 ? qd : (rot ^ 1)) * (Tr::PART + 4));
 
   float m[GM], l[GM];
   float2 acc[GM][Tr::EPL / 2];
 
+  // V row -> EPL floats as float2 pairs
+  auto load_v = [&](const uint8_t* row_ptr, float2* vf) {
+    if constexpr (Tr::KVB == 2) {
+      if constexpr (Tr::EPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row_ptr);
+        vf[0] = widen2<KVT>(w.x);
+        vf[1] = widen2<KVT>(w.y);
+      } else {
+        vf[0] = widen2<KVT>(*reinterpret_cast<const uint32_t*>(row_ptr));
+      }
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(row_ptr);
+      vf[0] = widen2_e4m3(w & 0xffffu);
+      vf[1] = widen2_e4m3(w >> 16);
+    }
+  };
+  // acc[g] += p[tok][g] * v for all heads (p stored as (p, p) pairs)
+  auto accumulate = [&](const float2* prow, const float2* vf) {
+#pragma unroll
+    for (int g = 0; g < GM; g += 2) {
+      if (g + 1 < GM) {
+        const float4 pp = *reinterpret_cast<const float4*>(prow + g);
+#pragma unroll
+        for (int i = 0; i < Tr::EPL / 2; ++i) {
+          acc[g][i] = ffma2(make_float2(pp.x, pp.y), vf[i], acc[g][i]);
+          acc[g + 1][i] = ffma2(make_float2(pp.z, pp.w), vf[i], acc[g + 1][i]);
+        }
+      } else {
+        const float2 pp = prow[g];
+#pragma unroll
+        for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = ffma2(pp, vf[i], acc[g][i]);
+      }
+    }
+  };
+
+  // One unit (8 rows): scores, online-softmax update, p . V.  FULL: all 8 rows valid.
+  auto unit_step = [&](auto full_tag, const uint8_t* stage, int n_valid) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    // ---- scores: the lane dots its part(s) of token t's K row with all G query heads
+    float2 sacc[Tr::NACC][GM];
+#pragma unroll
+    for (int a = 0; a < Tr::NACC; ++a)
+#pragma unroll
+      for (int g = 0; g < GM; ++g) sacc[a][g] = make_float2(0.f, 0.f);
+    constexpr int NPI = (Tr::LPT == 2) ? 1 : Tr::NPART;  // parts this lane visits
+#pragma unroll
+    for (int pi = 0; pi < NPI; ++pi) {
+      const int pp = (Tr::LPT == 2) ? qd : (pi ^ rot);   // part index
+      const float* qp0 = pi == 0 ? qpart0 : qpart1;
+#pragma unroll
+      for (int c = 0; c < Tr::CPP; ++c) {
+        // chunk c of part pp -> half h, chunk-in-half ch
+        const int cb = pp * Tr::CPP + c;                  // chunk within the row
+        const uint4 raw = *reinterpret_cast<const uint4*>(stage + kaddr(cb >> 3, cb & 7));
+        float2 kf[Tr::EPC / 2];
+        Chunk<KVT>::cvt(raw, kf);
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+          const float4* qp = reinterpret_cast<const float4*>(qp0 + g * Tr::QROW + c * Tr::EPC);
+#pragma unroll
+          for (int i = 0; i < Tr::EPC / 4; ++i) {
+            const float4 q4 = qp[i];
+            float2& sa = sacc[(2 * i) % Tr::NACC][g];
+            sa = ffma2(make_float2(q4.x, q4.y), kf[2 * i], sa);
+            float2& sb = sacc[(2 * i + 1) % Tr::NACC][g];
+            sb = ffma2(make_float2(q4.z, q4.w), kf[2 * i + 1], sb);
+          }
+        }
+      }
+    }
+    float sv[GM];
+    bool up = false;
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+      float2 s2 = sacc[0][g];
+#pragma unroll
+      for (int a = 1; a < Tr::NACC; ++a) s2 = make_float2(s2.x + sacc[a][g].x, s2.y + sacc[a][g].y);
+      float x = s2.x + s2.y;
+      if constexpr (Tr::LPT == 2) x += __shfl_xor_sync(0xffffffffu, x, 1);
+      if constexpr (!FULL) x = (t < n_valid) ? x : -INFINITY;
+      sv[g] = x;
+      up |= x > m[g];
+    }
+    // ---- online softmax: the running maximum only moves when some score exceeds it
+    if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        float bm = sv[g];
+#pragma unroll
+        for (int o = Tr::LPT; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+        const float mn = fmaxf(m[g], bm);
+        const float alpha = fast_exp2(m[g] - mn);
+        m[g] = mn;
+        l[g] *= alpha;
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = fmul2(acc[g][i], a2);
+      }
+    }
+    float pg[GM];
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+      pg[g] = fast_exp2(sv[g] - m[g]);
+      l[g] += (qd == 0) ? pg[g] : 0.f;
+    }
+    if (qd == 0) {
+      float2* prow = pbuf + t * GM;
+#pragma unroll
+      for (int g = 0; g < GM; g += 2) {
+        if (g + 1 < GM) {
+          *reinterpret_cast<float4*>(prow + g) = make_float4(pg[g], pg[g], pg[g + 1], pg[g + 1]);
+        } else {
+          prow[g] = make_float2(pg[g], pg[g]);
+        }
+      }
+    }
+    __syncwarp();
+    // ---- p . V: lane owns columns e0..e0+EPL-1 of all G heads
+#pragma unroll
+    for (int tt = 0; tt < UR; ++tt) {
+      if (FULL || tt < n_valid) {
+        float2 vf[Tr::EPL / 2];
+        load_v(stage + vofs[tt % VPER] + tt * Tr::ROW, vf);
+        accumulate(pbuf + tt * GM, vf);
+      }
+    }
+  };
+
   while (it.valid) {
-    const int st = consumed % Tr::NS;
-    const uint32_t parity = (consumed / Tr::NS) & 1;
-    if (!mbar_wait_bounded(bar0 + 8 * st, parity, kWaitLimitNs)) {
+    if (!mbar_wait_bounded(bar0 + 8 * cst, cpar, kWaitLimitNs)) {
       timed_out = true;
       break;
     }
@@ -350,7 +543,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       // new fragment: widen + pre-scale the query group, reset the state
       float qs = p.qk_scale_log2;
       if constexpr (kFp8) qs *= __ldg(p.k_scale + it.kvh);
-      const uint8_t* qr = qraw_base + (it.frag_idx & 1) * kQrawStride;
+      const uint8_t* qr = qraw_base + (it.frag_idx & 1) * Tr::QRAW_STRIDE;
       for (int idx = lane; idx < GM * D / 2; idx += 32) {
         const int e = 2 * idx;
         const int g = e / D;
@@ -362,7 +555,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           v2.x *= qs;
           v2.y *= qs;
         }
-        *reinterpret_cast<float2*>(qf + g * Tr::QROW + (ed / Tr::HALF) * (Tr::HALF + Tr::QPAD) + ed % Tr::HALF) = v2;
+        *reinterpret_cast<float2*>(qf + g * Tr::QROW + (ed / Tr::PART) * (Tr::PART + 4) + ed % Tr::PART) = v2;
       }
 #pragma unroll
       for (int g = 0; g < GM; ++g) {
@@ -374,114 +567,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       __syncwarp();
     }
 
-    const int n_valid = min(BS, it.T - it.j * BS);
-    const uint32_t kst = wbase_u32 + st * Tr::STAGE;
-    const uint32_t vst = kst + Tr::TILE;
-
-    // ---- scores: lane (t, half) dots its half-row of K with all G query heads
-    float2 sacc[GM];
-#pragma unroll
-    for (int g = 0; g < GM; ++g) sacc[g] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < Tr::CPL; ++c) {
-      const int cg = half * Tr::CPL + c;
-      const uint32_t kaddr = kst + (cg >> 3) * (BS * 128) + t * 128 + (((cg & 7) ^ (t & 7)) << 4);
-      const uint4 raw = lds128(kaddr);
-      float2 kf[Tr::EPC / 2];
-      Chunk<KVT>::cvt(raw, kf);
-      const int qoff = half * (Tr::HALF + Tr::QPAD) + c * Tr::EPC;
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        const float4* qp = reinterpret_cast<const float4*>(qf + g * Tr::QROW + qoff);
-#pragma unroll
-        for (int i = 0; i < Tr::EPC / 4; ++i) {
-          const float4 q4 = qp[i];
-          sacc[g] = ffma2(make_float2(q4.x, q4.y), kf[2 * i], sacc[g]);
-          sacc[g] = ffma2(make_float2(q4.z, q4.w), kf[2 * i + 1], sacc[g]);
-        }
-      }
-    }
-    const bool tok_ok = t < n_valid;
-    float alpha[GM];
-    bool rescale = false;
-#pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      float sv = sacc[g].x + sacc[g].y;
-      if constexpr (Tr::LPT == 2) sv += __shfl_xor_sync(0xffffffffu, sv, 16);
-      sv = tok_ok ? sv : -INFINITY;
-      float bm = sv;
-#pragma unroll
-      for (int o = 1; o < BS; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-      const float mn = fmaxf(m[g], bm);
-      alpha[g] = exp2f(m[g] - mn);
-      rescale |= (alpha[g] != 1.f);
-      m[g] = mn;
-      const float pg = tok_ok ? exp2f(sv - mn) : 0.f;
-      l[g] = l[g] * alpha[g] + (half == 0 ? pg : 0.f);
-      sacc[g].x = pg;  // keep p for the store below
-    }
-    if (half == 0) {
-#pragma unroll
-      for (int g = 0; g < GM; g += 2) {
-        const float pa = sacc[g].x;
-        const float pb = (g + 1 < GM) ? sacc[g + 1].x : 0.f;
-        if (g + 1 < GM) {
-          *reinterpret_cast<float4*>(pbuf + t * GM + g) = make_float4(pa, pa, pb, pb);
-        } else {
-          pbuf[t * GM + g] = make_float2(pa, pa);
-        }
-      }
-    }
-    __syncwarp();
-    if (rescale) {
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        const float2 a2 = make_float2(alpha[g], alpha[g]);
-#pragma unroll
-        for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = fmul2(acc[g][i], a2);
-      }
-    }
-
-    // ---- p . V: lane owns columns e0..e0+EPL-1 of all G heads
-    for (int tt = 0; tt < n_valid; ++tt) {
-      const uint32_t vaddr = vst + vsub * (BS * 128) + tt * 128 + ((((vbyte >> 4) ^ (tt & 7))) << 4) + (vbyte & 15);
-      float2 vf[Tr::EPL / 2];
-      if constexpr (Tr::KVB == 2) {
-        if constexpr (Tr::EPL == 4) {
-          uint32_t w0, w1;
-          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(vaddr));
-          vf[0] = widen2<KVT>(w0);
-          vf[1] = widen2<KVT>(w1);
-        } else {
-          uint32_t w0;
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vaddr));
-          vf[0] = widen2<KVT>(w0);
-        }
-      } else {
-        static_assert(Tr::EPL == 4 || Tr::KVB == 2, "fp8 path needs 4 columns per lane");
-        uint32_t w0;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vaddr));
-        vf[0] = widen2_e4m3(w0 & 0xffffu);
-        vf[1] = widen2_e4m3(w0 >> 16);
-      }
-#pragma unroll
-      for (int g = 0; g < GM; g += 2) {
-        if (g + 1 < GM) {
-          const float4 pp = *reinterpret_cast<const float4*>(pbuf + tt * GM + g);
-#pragma unroll
-          for (int i = 0; i < Tr::EPL / 2; ++i) {
-            acc[g][i] = ffma2(make_float2(pp.x, pp.y), vf[i], acc[g][i]);
-            acc[g + 1][i] = ffma2(make_float2(pp.z, pp.w), vf[i], acc[g + 1][i]);
-          }
-        } else {
-          const float2 pp = pbuf[tt * GM + g];
-#pragma unroll
-          for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = ffma2(pp, vf[i], acc[g][i]);
-        }
-      }
+    const int n_valid = min(UR, it.T - it.j * UR);
+    const uint8_t* stage = wbase + Tr::OFF_STAGES + cst * Tr::STAGE;
+    if (n_valid == UR) {
+      unit_step(std::true_type{}, stage, UR);
+    } else {
+      unit_step(std::false_type{}, stage, n_valid);
     }
     __syncwarp();
     ++consumed;
+    if (++cst == NS) {
+      cst = 0;
+      cpar ^= 1;
+    }
 
     // ---- end of fragment: write the output or a partial record
     if (it.j + 1 == it.jend) {
@@ -533,8 +631,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           parts = (prefix[it.s + 1] - prefix[it.s]) / Hkv;
           nfr = parts;
         } else {
-          seg_start = prefix[it.s] + static_cast<long long>(it.kvh) * it.nb;
-          const long long seg_last = seg_start + it.nb - 1;
+          seg_start = prefix[it.s] + static_cast<long long>(it.kvh) * it.nu;
+          const long long seg_last = seg_start + it.nu - 1;
           const int wf = static_cast<int>(((seg_start + 1) * nw_eff - 1) / U);
           const int wl = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U);
           nfr = wl - wf + 1;
@@ -589,7 +687,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         }
       }
     }
-    if (++it.j == it.jend) iter_next_fragment<BS>(it, prefix, p, fixed);
+    if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, UR);
     produce();
   }
 
@@ -597,44 +695,78 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
     // let this warp's copies in flight land before the CTA can exit
     for (int k = consumed; k < issued; ++k)
-      (void)mbar_wait_bounded(bar0 + 8 * (k % Tr::NS), (k / Tr::NS) & 1, kWaitLimitNs);
+      (void)mbar_wait_bounded(bar0 + 8 * (k % NS), (k / NS) & 1, kWaitLimitNs);
   }
 }
 
 // ----------------------------------------------------------------- host side of one variant
 
-template <typename QT, typename KVT, int D, int BS, int GM>
+template <typename QT, typename KVT, int D, int GM, int UR>
 struct DecodeVariant {
-  using Tr = DecodeTraits<QT, KVT, D, BS, GM>;
+  using Tr = DecodeTraits<QT, KVT, D, GM, UR>;
 
-  static size_t smem_bytes(int num_seqs) {
-    return 1024 + static_cast<size_t>(Tr::W) * Tr::WARP_SMEM +
-           static_cast<size_t>(align_up_c((num_seqs + 1 + Tr::W) * 4, 16));
+  static size_t smem_bytes(int num_seqs, int warps, int stages) {
+    return 1024 + static_cast<size_t>(warps) * Tr::warp_smem(stages) +
+           static_cast<size_t>(align_up_c((num_seqs + 1 + warps) * 4, 16));
   }
 
+  // Launch geometry: pipeline depth (stages per warp) and warps per CTA.
+  // Default depth keeps about kStageBytesPerWarp of K/V per warp; the warps
+  // per CTA maximise resident warps per SM (ties: more warps per CTA, i.e.
+  // fewer CTAs running the prologue).  PA_DECODE_STAGES / PA_DECODE_WARPS
+  // override both (tuning).
   static bool geometry(int num_seqs, DecodeGeometry* g) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    const size_t smem = smem_bytes(num_seqs);
-    auto kern = paged_decode_kernel<QT, KVT, D, BS, GM>;
+    auto kern = paged_decode_kernel<QT, KVT, D, GM, UR>;
+    int ns = kStageBytesPerWarp / Tr::STAGE;
+    ns = ns < 2 ? 2 : (ns > Tr::MAX_NS ? Tr::MAX_NS : ns);
+    const int env_ns = tuning_override("PA_DECODE_STAGES");
+    if (env_ns >= 2 && env_ns <= Tr::MAX_NS) ns = env_ns;
+    const int env_w = tuning_override("PA_DECODE_WARPS");
+    int best_w = 0, best_occ = 0, best_warps = 0;
+    for (int w = 1; w <= Tr::MAX_W; w *= 2) {
+      if (env_w > 0 && w != env_w) continue;
+      const size_t smem = smem_bytes(num_seqs, w, ns);
+      if (smem > 227 * 1024) break;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess)
+        return false;
+      int occ = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, w * 32, smem) != cudaSuccess) return false;
+      if (occ * w >= best_warps && occ > 0) {
+        best_warps = occ * w;
+        best_w = w;
+        best_occ = occ;
+      }
+    }
+    if (best_w == 0) return false;
+    const size_t smem = smem_bytes(num_seqs, best_w, ns);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
       return false;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Tr::W * 32, smem) != cudaSuccess || occ < 1)
-      return false;
-    g->warps_per_cta = Tr::W;
-    g->ctas = sms * occ;
+    g->warps_per_cta = best_w;
+    g->stages = ns;
+    g->ctas = sms * best_occ;
     g->smem_bytes = smem;
     g->record_floats = Tr::REC;
+    g->unit_rows = UR;
     return true;
   }
 
   static cudaError_t launch(const DecodeGeometry& g, const DecodeParams& p, const CUtensorMap& tk,
                             const CUtensorMap& tv, cudaStream_t stream) {
-    paged_decode_kernel<QT, KVT, D, BS, GM><<<g.ctas, Tr::W * 32, g.smem_bytes, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    (void)cudaGetLastError();  // an earlier unrelated error must not be reported as this launch's
+    paged_decode_kernel<QT, KVT, D, GM, UR><<<g.ctas, g.warps_per_cta * 32, g.smem_bytes, stream>>>(tk, tv, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, paged_decode_kernel<QT, KVT, D, GM, UR>) == cudaSuccess)
+        note_launch_failure(g.ctas, g.warps_per_cta * 32, g.smem_bytes, g.stages, fa.maxThreadsPerBlock,
+                            fa.maxDynamicSharedSizeBytes, fa.numRegs, fa.localSizeBytes);
+    }
+    return e;
   }
 };
 

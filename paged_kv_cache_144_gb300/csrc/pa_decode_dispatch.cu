@@ -1,25 +1,53 @@
 // pa_decode_dispatch.cu - maps a runtime DecodeKey to its compiled variant.
-#include "pa_decode.cuh"
 #include "pa_decode_variants.h"
+
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+#include <unordered_map>
 
 namespace pa {
 
-#define PA_EXTERN(QT, KVT, D, BS, GM) extern template struct DecodeVariant<QT, KVT, D, BS, GM>;
-PA_DECODE_VARIANTS(PA_EXTERN)
-#undef PA_EXTERN
+int tuning_override(const char* name) {
+  static std::mutex mu;
+  static std::unordered_map<std::string, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(name);
+  if (it != cache.end()) return it->second;
+  const char* v = std::getenv(name);
+  const int x = v ? std::atoi(v) : -1;
+  cache.emplace(name, x);
+  return x;
+}
+
+namespace {
+thread_local char g_launch_note[256] = "";
+}
+
+void note_launch_failure(int ctas, int threads, size_t smem, int stages, int max_threads, int max_dyn_smem,
+                         int regs, size_t local_bytes) {
+  snprintf(g_launch_note, sizeof(g_launch_note),
+           "grid %d x %d threads, dyn smem %zu, stages %d; kernel: max threads %d, max dyn smem %d, regs %d, "
+           "local %zu",
+           ctas, threads, smem, stages, max_threads, max_dyn_smem, regs, local_bytes);
+}
+
+const char* launch_failure_note() { return g_launch_note; }
+
 
 template <typename T> constexpr int dtype_code();
 template <> constexpr int dtype_code<f16_t>() { return PA_F16; }
 template <> constexpr int dtype_code<bf16_t>() { return PA_BF16; }
 template <> constexpr int dtype_code<e4m3_t>() { return PA_FP8_E4M3; }
 
-#define PA_MATCH(QT, KVT, D, BS, GM)                                                        \
-  (key.q_dtype == dtype_code<QT>() && key.kv_dtype == dtype_code<KVT>() && key.head_dim == D && \
-   key.block_size == BS && key.gmax == GM)
+#define PA_MATCH(QT, KVT, D, GM, UR)                                                        \
+  (key.q_dtype == dtype_code<QT>() && key.kv_dtype == dtype_code<KVT>() && key.head_dim == D && key.gmax == GM && \
+   key.unit_rows == UR)
 
 bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
-#define PA_GEO(QT, KVT, D, BS, GM) \
-  if (PA_MATCH(QT, KVT, D, BS, GM)) return DecodeVariant<QT, KVT, D, BS, GM>::geometry(num_seqs, geo);
+#define PA_GEO(QT, KVT, D, GM, UR) \
+  if (PA_MATCH(QT, KVT, D, GM, UR)) return decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(num_seqs, geo);
   PA_DECODE_VARIANTS(PA_GEO)
 #undef PA_GEO
   return false;
@@ -27,8 +55,8 @@ bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
 
 cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,
                           const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-#define PA_LAUNCH(QT, KVT, D, BS, GM) \
-  if (PA_MATCH(QT, KVT, D, BS, GM)) return DecodeVariant<QT, KVT, D, BS, GM>::launch(geo, p, tk, tv, stream);
+#define PA_LAUNCH(QT, KVT, D, GM, UR) \
+  if (PA_MATCH(QT, KVT, D, GM, UR)) return decode_launch_##QT##_##KVT##_##D##_##GM##_##UR(geo, p, tk, tv, stream);
   PA_DECODE_VARIANTS(PA_LAUNCH)
 #undef PA_LAUNCH
   return cudaErrorInvalidValue;

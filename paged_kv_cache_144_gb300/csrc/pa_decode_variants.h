@@ -1,24 +1,52 @@
-// pa_decode_variants.h - the compiled (q dtype, kv dtype, head_dim, block_size,
-// max group) variants of the decode kernel.  A group G is served by the
+// pa_decode_variants.h - the compiled (q dtype, kv dtype, head_dim, max group,
+// unit rows) variants of the decode kernel (the block size is a runtime
+// parameter).  A group G is served by the
 // smallest compiled maximum >= G (1, 4 or 8).
 #pragma once
 
-#define PA_DECODE_VARIANTS_F16(X)                                                    \
-  X(f16_t, f16_t, 64, 16, 1) X(f16_t, f16_t, 64, 16, 4) X(f16_t, f16_t, 64, 16, 8)   \
-  X(f16_t, f16_t, 64, 32, 1) X(f16_t, f16_t, 64, 32, 4) X(f16_t, f16_t, 64, 32, 8)   \
-  X(f16_t, f16_t, 128, 16, 1) X(f16_t, f16_t, 128, 16, 4) X(f16_t, f16_t, 128, 16, 8) \
-  X(f16_t, f16_t, 128, 32, 1) X(f16_t, f16_t, 128, 32, 4) X(f16_t, f16_t, 128, 32, 8)
+#include "pa_common.cuh"
+#include "pa_kernels.h"
 
-#define PA_DECODE_VARIANTS_BF16(X)                                                        \
-  X(bf16_t, bf16_t, 64, 16, 1) X(bf16_t, bf16_t, 64, 16, 4) X(bf16_t, bf16_t, 64, 16, 8)   \
-  X(bf16_t, bf16_t, 64, 32, 1) X(bf16_t, bf16_t, 64, 32, 4) X(bf16_t, bf16_t, 64, 32, 8)   \
-  X(bf16_t, bf16_t, 128, 16, 1) X(bf16_t, bf16_t, 128, 16, 4) X(bf16_t, bf16_t, 128, 16, 8) \
-  X(bf16_t, bf16_t, 128, 32, 1) X(bf16_t, bf16_t, 128, 32, 4) X(bf16_t, bf16_t, 128, 32, 8)
+#define PA_DECODE_VARIANTS_F16(X) \
+  X(f16_t, f16_t, 64, 1, 16) X(f16_t, f16_t, 64, 1, 32) X(f16_t, f16_t, 64, 4, 16) X(f16_t, f16_t, 64, 4, 32) \
+  X(f16_t, f16_t, 64, 8, 16) X(f16_t, f16_t, 64, 8, 32) X(f16_t, f16_t, 128, 1, 16) \
+  X(f16_t, f16_t, 128, 1, 32) X(f16_t, f16_t, 128, 4, 16) X(f16_t, f16_t, 128, 4, 32) \
+  X(f16_t, f16_t, 128, 8, 16) X(f16_t, f16_t, 128, 8, 32)
 
-#define PA_DECODE_VARIANTS_FP8(X)                                                         \
-  X(bf16_t, e4m3_t, 128, 16, 1) X(bf16_t, e4m3_t, 128, 16, 4) X(bf16_t, e4m3_t, 128, 16, 8) \
-  X(bf16_t, e4m3_t, 128, 32, 1) X(bf16_t, e4m3_t, 128, 32, 4) X(bf16_t, e4m3_t, 128, 32, 8) \
-  X(f16_t, e4m3_t, 128, 16, 1) X(f16_t, e4m3_t, 128, 16, 4) X(f16_t, e4m3_t, 128, 16, 8)    \
-  X(f16_t, e4m3_t, 128, 32, 1) X(f16_t, e4m3_t, 128, 32, 4) X(f16_t, e4m3_t, 128, 32, 8)
+#define PA_DECODE_VARIANTS_BF16(X) \
+  X(bf16_t, bf16_t, 64, 1, 16) X(bf16_t, bf16_t, 64, 1, 32) X(bf16_t, bf16_t, 64, 4, 16) \
+  X(bf16_t, bf16_t, 64, 4, 32) X(bf16_t, bf16_t, 64, 8, 16) X(bf16_t, bf16_t, 64, 8, 32) \
+  X(bf16_t, bf16_t, 128, 1, 16) X(bf16_t, bf16_t, 128, 1, 32) X(bf16_t, bf16_t, 128, 4, 16) \
+  X(bf16_t, bf16_t, 128, 4, 32) X(bf16_t, bf16_t, 128, 8, 16) X(bf16_t, bf16_t, 128, 8, 32)
+
+#define PA_DECODE_VARIANTS_FP8(X) \
+  X(bf16_t, e4m3_t, 128, 1, 16) X(bf16_t, e4m3_t, 128, 1, 32) X(bf16_t, e4m3_t, 128, 4, 16) \
+  X(bf16_t, e4m3_t, 128, 4, 32) X(bf16_t, e4m3_t, 128, 8, 16) X(bf16_t, e4m3_t, 128, 8, 32) \
+  X(f16_t, e4m3_t, 128, 1, 16) X(f16_t, e4m3_t, 128, 1, 32) X(f16_t, e4m3_t, 128, 4, 16) \
+  X(f16_t, e4m3_t, 128, 4, 32) X(f16_t, e4m3_t, 128, 8, 16) X(f16_t, e4m3_t, 128, 8, 32)
 
 #define PA_DECODE_VARIANTS(X) PA_DECODE_VARIANTS_F16(X) PA_DECODE_VARIANTS_BF16(X) PA_DECODE_VARIANTS_FP8(X)
+
+// Each variant translation unit defines these two plain functions; the
+// dispatcher sees only the declarations, so every kernel is instantiated and
+// registered in exactly one translation unit.
+#define PA_DECLARE_VARIANT(QT, KVT, D, GM, UR)                                                   \
+  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(int num_seqs, DecodeGeometry* geo);      \
+  cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR(const DecodeGeometry& geo,           \
+                                                              const DecodeParams& p,              \
+                                                              const CUtensorMap& tk,              \
+                                                              const CUtensorMap& tv, cudaStream_t stream);
+#define PA_DEFINE_VARIANT(QT, KVT, D, GM, UR)                                                      \
+  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(int num_seqs, DecodeGeometry* geo) {      \
+    return DecodeVariant<QT, KVT, D, GM, UR>::geometry(num_seqs, geo);                             \
+  }                                                                                                \
+  cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR(const DecodeGeometry& geo,           \
+                                                              const DecodeParams& p,              \
+                                                              const CUtensorMap& tk,              \
+                                                              const CUtensorMap& tv, cudaStream_t stream) { \
+    return DecodeVariant<QT, KVT, D, GM, UR>::launch(geo, p, tk, tv, stream);                      \
+  }
+
+namespace pa {
+PA_DECODE_VARIANTS(PA_DECLARE_VARIANT)
+}  // namespace pa

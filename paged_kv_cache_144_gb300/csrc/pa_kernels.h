@@ -9,6 +9,13 @@
 
 namespace pa {
 
+// K/V TMA boxes are min(unit rows, block_size) whole rows; both are
+// multiples of this (one 128-byte-swizzle atom is 8 x 128 bytes).
+constexpr int kBoxRowQuantum = 8;
+
+// Integer tuning override from the environment (read once per name), or -1.
+int tuning_override(const char* name);
+
 struct ReshapeArgs {
   const void* k;
   const void* v;
@@ -50,10 +57,13 @@ struct DecodeParams {
   int num_kv_heads;
   int group;                    // query heads per KV head (<= compiled maximum)
   float qk_scale_log2;          // softmax scale * log2(e)
-  int partition_blocks;         // 0: balanced split; >0: fixed partitions of this many blocks
+  int block_size;               // tokens per cache block (a power of two >= 8)
+  int block_shift;              // log2(block_size)
+  int partition_units;          // 0: balanced split; >0: fixed partitions of this many 8-row units
   float* part_records;          // split-K partial records (workspace)
   int* seg_counters;            // [num_seqs * num_kv_heads] arrival counters (workspace)
   unsigned int* err;            // per-device error word
+  int stages;                   // K/V pipeline stages per warp
 };
 
 // Compile-time variant of the decode kernel.
@@ -61,21 +71,26 @@ struct DecodeKey {
   int q_dtype;    // PA_F16 / PA_BF16
   int kv_dtype;   // PA_F16 / PA_BF16 / PA_FP8_E4M3
   int head_dim;   // 64 / 128
-  int block_size; // 16 / 32
-  int gmax;       // 1 / 4 / 8 (query heads per KV head, rounded up)
+  int gmax;
+  int unit_rows;  // 16 / 32 rows per work unit       // 1 / 4 / 8 (query heads per KV head, rounded up)
 };
 
 // Launch geometry of one variant on the current device.
 struct DecodeGeometry {
   int warps_per_cta;
+  int stages;          // K/V pipeline stages per warp
   int ctas;            // resident CTAs over the whole device
   size_t smem_bytes;   // dynamic shared memory per CTA
   int record_floats;   // floats per partial record
+  int unit_rows;       // rows per work unit (TMA box height = min(unit_rows, block_size))
 };
 
 // Fills `geo` for `key` and `num_seqs` on the current device; false if the
 // variant is not compiled in or the device cannot run it.
 bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo);
+
+// Geometry and kernel attributes of the last rejected decode launch on this thread.
+const char* launch_failure_note();
 
 cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,
                           const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);

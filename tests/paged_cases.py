@@ -54,7 +54,7 @@ def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", d
     q = to_torch(vals["q"], batch.q_fmt, device)
     kc = to_torch(vals["k_cache"], kv, device)
     vc = to_torch(vals["v_cache"], kv, device)
-    src_fmt = batch.q_fmt if kv == "e4m3" else kv
+    src_fmt = "bf16" if kv == "e4m3" else kv   # FP8 sources are bf16 rows
     ks = vs = kis = vis = None
     if kv == "e4m3":
         ks = torch.from_numpy(vals["k_scale"]).to(device)
@@ -87,7 +87,7 @@ def run_oracle(batch, vals):
     kv = batch.kv_fmt
     B = batch.block_size
     kc, vc = vals["k_cache"], vals["v_cache"]
-    src_fmt = batch.q_fmt if kv == "e4m3" else kv
+    src_fmt = "bf16" if kv == "e4m3" else kv
     kis = vals.get("k_inv_scale")
     vis = vals.get("v_inv_scale")
     if kv == "e4m3":

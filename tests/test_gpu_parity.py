@@ -52,7 +52,7 @@ def test_long_group8_extreme_logits(q_mult):
 
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (6, 2), (16, 4), (10, 2), (16, 2)])
 def test_shapes_grid(fmt, D, B, Hq, Hkv):
     b = workloads.make_batch("gqa_32x4k", seed=3, num_seqs=5, num_heads=Hq, num_kv_heads=Hkv, head_dim=D,

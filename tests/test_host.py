@@ -51,7 +51,10 @@ def test_decode_validation(lib):
     assert _decode(Hq=30) == pa.PA_ERR_SHAPE             # H_q not a multiple of H_kv
     assert _decode(Hq=128) == pa.PA_ERR_UNSUPPORTED      # G = 16
     assert _decode(D=96, q_stride=32 * 96) == pa.PA_ERR_UNSUPPORTED
-    assert _decode(B=8) == pa.PA_ERR_UNSUPPORTED
+    assert _decode(B=12) == pa.PA_ERR_UNSUPPORTED         # block size: a power of two from 8 to 1024
+    assert _decode(B=96) == pa.PA_ERR_UNSUPPORTED
+    assert _decode(B=4) == pa.PA_ERR_UNSUPPORTED
+    assert _decode(B=2048) == pa.PA_ERR_UNSUPPORTED
     assert _decode(P=100) == pa.PA_ERR_SHAPE             # not a multiple of B
     assert _decode(mb=0) == pa.PA_ERR_SHAPE
     assert _decode(out=None) == pa.PA_ERR_NULL
