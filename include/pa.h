@@ -188,6 +188,43 @@ int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype,
 int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, size_t block_bytes,
                    const int32_t* src_dst_pairs, int num_pairs, void* stream);
 
+/*
+ * pa_decode_noalloc - pa_decode for callers that cannot allocate device
+ * memory (no counterpart in the pages: an engineering addition).
+ *
+ * A caller that runs where cudaMalloc is unavailable or forbidden at decode
+ * time (an allocator-free serving loop, a process whose device memory pool
+ * belongs to another framework, a plugin that is handed only its input and
+ * output buffers) cannot supply pa_decode's workspace.  This entry point
+ * takes the same arguments minus the workspace and uses a fixed 16 MiB
+ * array that the library defines in device memory instead
+ * (pa_decode_noalloc_capacity() returns its size).  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call clears the array's arrival counters on `stream`
+ *     (cudaMemsetAsync) and then runs pa_decode on it.
+ *   - All calls share the one array per device: calls whose kernels overlap
+ *     on the GPU (different streams without ordering) race and give wrong
+ *     results.  Order them on one stream or use pa_decode with workspaces.
+ *   - Returns PA_ERR_WORKSPACE (detail in pa_last_error_detail) when the
+ *     sizes need more split workspace than the array holds; other errors as
+ *     pa_decode.
+ */
+int pa_decode_noalloc(void* out, pa_dtype out_dtype,
+                      const void* q, pa_dtype q_dtype, int64_t q_stride,
+                      const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                      const float* k_scale, const float* v_scale,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* seq_lens,
+                      int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                      float scale, int block_size, int partition_size,
+                      void* stream);
+
+/* Size in bytes of the fixed device array pa_decode_noalloc uses. */
+size_t pa_decode_noalloc_capacity(void);
+
 /* Human-readable name of a pa_status value (static string). */
 const char* pa_status_string(int status);
 

@@ -34,6 +34,9 @@ _SIGNATURES = {
     "pa_get_device_error": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "pa_version": (_i32, []),
     "pa_last_error_detail": (ctypes.c_char_p, []),
+    "pa_decode_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
+                                 _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp]),
+    "pa_decode_noalloc_capacity": (_sz, []),
     "pa_decode_launch_config": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]),
@@ -97,6 +100,14 @@ def pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block
 
 def pa_decode(*args) -> int:
     return int(load().pa_decode(*args))
+
+
+def pa_decode_noalloc(*args) -> int:
+    return int(load().pa_decode_noalloc(*args))
+
+
+def pa_decode_noalloc_capacity() -> int:
+    return int(load().pa_decode_noalloc_capacity())
 
 
 def pa_reshape_and_cache(*args) -> int:
@@ -197,6 +208,25 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
                    S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
                    _ptr(workspace), ws_bytes, _stream(stream))
     _check("pa_decode", st)
+    return out
+
+
+def decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale, block_size, *,
+                   k_scale=None, v_scale=None, partition_size=0, stream=None):
+    """pa_decode on the library's fixed device array (for callers that cannot allocate)."""
+    for n, t in (("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
+                 ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _require_cuda(n, t)
+    _require_cuda("q", q, contiguous=False)
+    if q.stride(2) != 1 or q.stride(1) != q.shape[2]:
+        raise ValueError("q rows must be contiguous per sequence")
+    S, Hq, D = q.shape
+    st = pa_decode_noalloc(_ptr(out), dtype_code(out), _ptr(q), dtype_code(q), q.stride(0),
+                           _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), k_cache.shape[0],
+                           _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                           S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
+                           _stream(stream))
+    _check("pa_decode_noalloc", st)
     return out
 
 

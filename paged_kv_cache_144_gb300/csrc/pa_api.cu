@@ -359,3 +359,82 @@ PA_EXPORT int pa_get_device_error(void* stream, unsigned int* error_bits) {
   *error_bits = h;
   return PA_OK;
 }
+
+// ----------------------------------------------------------------- allocation-free decode
+//
+// Some callers cannot allocate device memory at decode time: code that runs
+// where cudaMalloc is not allowed or would stall (inside a real-time serving
+// loop that must not touch the allocator, in a process whose memory pool is
+// owned and locked by another framework, or in a plugin that only receives
+// its input and output buffers).  For them pa_decode_noalloc keeps the split
+// workspace in a fixed array that the library itself defines in device
+// memory, so the caller passes only inputs and outputs.
+
+namespace {
+
+// Device memory for the split records and arrival counters of
+// pa_decode_noalloc.  Every device that loads the library holds this array
+// until the process exits.  Host code must not use its name as an address:
+// the device address is looked up per device (noalloc_scratch_address).
+constexpr size_t kNoallocScratchBytes = size_t{16} << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.  nullptr if the lookup fails.
+void* noalloc_scratch_address() {
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      cuda_status(e, "pa_decode_noalloc scratch lookup");
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+PA_EXPORT size_t pa_decode_noalloc_capacity(void) { return kNoallocScratchBytes; }
+
+PA_EXPORT int pa_decode_noalloc(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
+                                const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                                const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
+                                void* stream) {
+  const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                    partition_size, kv_dtype);
+  if (sh != PA_OK) return sh;
+  if (num_seqs == 0) return PA_OK;
+  if ((q_dtype != PA_F16 && q_dtype != PA_BF16) || (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3))
+    return PA_ERR_DTYPE;
+  DecodePlan plan;
+  const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                           partition_size, q_dtype, kv_dtype, true, &plan);
+  if (pr != PA_OK) return pr;
+  if (plan.bytes > kNoallocScratchBytes) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "pa_decode_noalloc: this call needs %zu bytes of split workspace, more than the fixed %zu",
+             plan.bytes, kNoallocScratchBytes);
+    return PA_ERR_WORKSPACE;
+  }
+  void* scratch = noalloc_scratch_address();
+  if (!scratch) return PA_ERR_CUDA;
+  // the arrival counters must start at zero; the records need no clearing
+  if (plan.counters_bytes > 0) {
+    const int st = cuda_status(
+        cudaMemsetAsync(scratch, 0, plan.counters_bytes, static_cast<cudaStream_t>(stream)), "pa_decode_noalloc memset");
+    if (st != PA_OK) return st;
+  }
+  return pa_decode(out, out_dtype, q, q_dtype, q_stride, k_cache, v_cache, kv_dtype, num_blocks, k_scale, v_scale,
+                   block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads, num_kv_heads, head_dim, scale,
+                   block_size, partition_size, plan.bytes ? scratch : nullptr, plan.bytes ? kNoallocScratchBytes : 0,
+                   stream);
+}
