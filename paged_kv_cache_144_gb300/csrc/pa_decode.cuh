@@ -53,7 +53,7 @@
 
 namespace pa {
 
-constexpr int kMinUnitsPerWarp = 16;           // smallest balanced share (128 rows)
+constexpr int kMinUnitsPerWarp = 2;            // smallest balanced share (small batches spread wide)
 constexpr int kStageBytesPerWarp = 12 * 1024;  // default K/V pipeline bytes per warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
