@@ -21,11 +21,14 @@
 //    per resident warp, so long and short sequences load every SM equally
 //    ("balanced" mode).  A range crosses (s, kvh) segments freely.  Optionally
 //    each warp instead takes fixed partitions of P tokens.
-//  * Each warp owns a private ring of stages in shared memory (one unit of K
-//    and of V per stage) filled by TMA copies (cp.async.bulk.tensor) that
-//    complete on one mbarrier per stage; the query group of a new segment
-//    rides on the same barrier as a 1-D bulk copy.  No CTA-wide barrier is
-//    used after the prologue.
+//  * Warp specialisation: each CTA has W consumer warps and one producer
+//    warp.  Consumer warp c owns a ring of stages in shared memory (one unit
+//    of K, of V and, at a segment start, the query group per stage).  Lane c
+//    of the producer warp walks consumer c's units: it waits for the stage's
+//    "empty" mbarrier, reads the block table, and issues the TMA copies
+//    (cp.async.bulk.tensor) plus a 1-D bulk copy of the query group, all
+//    completing on the stage's "full" mbarrier.  Consumers only wait, compute
+//    and release.  No CTA-wide barrier is used after the prologue.
 //  * QK: 32/UR lanes per token (one for UR=32), each a part of the row, form
 //    the dot products with all G query heads of the group in packed fp32x2
 //    FMAs (several independent accumulators per head); the pre-scaled fp32
@@ -54,7 +57,7 @@
 namespace pa {
 
 constexpr int kMinUnitsPerWarp = 2;            // smallest balanced share (small batches spread wide)
-constexpr int kStageBytesPerWarp = 12 * 1024;  // default K/V pipeline bytes per warp
+constexpr int kStageBytesPerWarp = 24 * 1024;  // default K/V pipeline bytes per consumer warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Integer tuning override from the environment (read once per name), or -1.
@@ -76,9 +79,10 @@ struct DecodeTraits {
   static constexpr int NSUB = ROW / 128;         // 128-byte halves per row
   static constexpr int SUB_ELEMS = 128 / KVB;    // elements per half
   static constexpr int TILE = UR * ROW;          // bytes of one unit of K (or V)
-  static constexpr int STAGE = 2 * TILE;         // K tile + V tile
-  static constexpr int MAX_NS = 8;               // stages per warp (chosen at launch, 2..MAX_NS)
-  static constexpr int MAX_W = 8;                // warps per CTA (chosen at launch, <= MAX_W)
+  static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
+  static constexpr int STAGE = align_up_c(2 * TILE + QRAW, 1024);  // K tile + V tile + raw q
+  static constexpr int MAX_NS = 8;               // stages per consumer (chosen at launch, 2..MAX_NS)
+  static constexpr int MAX_W = 8;                // consumer warps per CTA (chosen at launch)
   static constexpr int LPT = 32 / UR;            // lanes per token in QK (2 or 1)
   static constexpr int CHUNKS = ROW / 16;        // 16-byte chunks per row
   static constexpr int EPC = 16 / KVB;           // elements per chunk
@@ -89,15 +93,13 @@ struct DecodeTraits {
   static constexpr int PART = D / NPART;         // elements per part
   static constexpr int CPP = CHUNKS / NPART;     // chunks per part
   static constexpr int QROW = NPART * (PART + 4);  // floats per head (4 floats of padding per part)
-  static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
   static constexpr int NACC = (GM >= 8) ? 2 : 4;  // independent QK accumulators per head
-  // per-warp shared memory: [raw q x2 | fp32 q | p | mbarriers | NS stages]
-  static constexpr int OFF_QRAW = 0;
-  static constexpr int QRAW_STRIDE = align_up_c(QRAW, 128);
-  static constexpr int OFF_QF32 = OFF_QRAW + 2 * QRAW_STRIDE;
+  // per-consumer shared memory: [fp32 q | p | full[MAX_NS] | empty[MAX_NS] | NS stages]
+  static constexpr int OFF_QF32 = 0;
   static constexpr int OFF_PBUF = OFF_QF32 + GM * QROW * 4;
-  static constexpr int OFF_BAR = OFF_PBUF + UR * GM * 8;
-  static constexpr int OFF_STAGES = align_up_c(OFF_BAR + MAX_NS * 8, 1024);
+  static constexpr int OFF_FULL = align_up_c(OFF_PBUF + UR * GM * 8, 8);
+  static constexpr int OFF_EMPTY = OFF_FULL + MAX_NS * 8;
+  static constexpr int OFF_STAGES = align_up_c(OFF_EMPTY + MAX_NS * 8, 1024);
   __host__ __device__ static constexpr int warp_smem(int ns) { return OFF_STAGES + ns * STAGE; }
   static constexpr int REC = align_up_c(GM * (D + 2), 4);  // floats per partial record
   static_assert(EPL == 2 || EPL == 4, "D/32 columns per lane");
@@ -193,7 +195,7 @@ __device__ __forceinline__ void iter_next_fragment(WorkIter& it, const int* pref
 }
 
 template <typename QT, typename KVT, int D, int GM, int UR_>
-__global__ void __launch_bounds__(DecodeTraits<QT, KVT, D, GM, UR_>::MAX_W * 32, 1)
+__global__ void __launch_bounds__((DecodeTraits<QT, KVT, D, GM, UR_>::MAX_W + 1) * 32, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const DecodeParams p) {
   using Tr = DecodeTraits<QT, KVT, D, GM, UR_>;
@@ -205,7 +207,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int W = blockDim.x >> 5;  // warps per CTA
+  const int NWARP = blockDim.x >> 5;
+  const int W = NWARP - 1;         // consumer warps (warp 0 produces)
   const int S = p.num_seqs;
   const int Hkv = p.num_kv_heads;
   const int G = p.group;
@@ -218,7 +221,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   const int bpu_shift = unit_in_block ? 0 : (UR == 32 ? 5 : 4) - p.block_shift;  // log2(blocks per unit)
   const bool fixed = p.partition_units > 0;
 
-  const int NS = p.stages;  // pipeline depth per warp
+  const int NS = p.stages;  // pipeline depth per consumer
   const int wsm = Tr::warp_smem(NS);
   int* prefix = reinterpret_cast<int*>(base + W * wsm);
   int* scan_tmp = prefix + (S + 1);
@@ -248,7 +251,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       if (lane == 31) scan_tmp[warp] = x;
       __syncthreads();
       int wo = 0, tot = 0;
-      for (int w = 0; w < W; ++w) {
+      for (int w = 0; w < NWARP; ++w) {
         const int v = scan_tmp[w];
         wo += (w < warp) ? v : 0;
         tot += v;
@@ -267,119 +270,144 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
     }
   }
-  __syncthreads();
 
-  // ---- 3. this warp's share of the work
-  const int nw_total = gridDim.x * W;
-  const int gw = blockIdx.x * W + warp;
-  const long long U = prefix[S];
-  WorkIter it;
-  it.frag_idx = 0;
-  it.gw = gw;
-  it.valid = false;
-  int nw_eff = nw_total;
-  if (fixed) {
-    it.R = static_cast<int>(U);
-    it.rstride = nw_total;
-    it.r = gw;
-    if (it.r < it.R) { it.valid = true; frag_fixed(it, prefix, p, UR); }
-  } else if (U > 0) {
-    const long long want = (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp;
-    nw_eff = static_cast<int>(want < nw_total ? want : static_cast<long long>(nw_total));
-    if (nw_eff < 1) nw_eff = 1;
-    if (gw < nw_eff) {
-      it.u = gw * U / nw_eff;
-      it.u1 = (gw + 1) * U / nw_eff;
-      if (it.u < it.u1) { it.valid = true; frag_balanced(it, prefix, p); }
+  // ---- 3. barriers of every consumer ring
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < W; ++c) {
+      const uint32_t cb = base_u32 + c * wsm;
+      for (int i = 0; i < NS; ++i) {
+        mbar_init(cb + Tr::OFF_FULL + 8 * i, 1);
+        mbar_init(cb + Tr::OFF_EMPTY + 8 * i, 1);
+      }
     }
-  }
-  if (!it.valid) return;
-
-  uint8_t* wbase = base + warp * wsm;
-  const uint32_t wbase_u32 = base_u32 + warp * wsm;
-  const uint32_t bar0 = wbase_u32 + Tr::OFF_BAR;
-  if (lane == 0) {
-    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8 * i, 1);
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  __syncwarp();
+  __syncthreads();
 
-  float* qf = reinterpret_cast<float*>(wbase + Tr::OFF_QF32);
-  float2* pbuf = reinterpret_cast<float2*>(wbase + Tr::OFF_PBUF);
-  const uint8_t* qraw_base = wbase + Tr::OFF_QRAW;
-  const uint32_t qraw_u32 = wbase_u32 + Tr::OFF_QRAW;
-
-  // ---- producer: one TMA unit per free stage, up to NS ahead of the consumer
-  WorkIter prod = it;
-  int tb_seq = -1, tb_base = 0, tb_val = -1;  // cached table slice: lane i holds block entry tb_base+i
-  int issued = 0, consumed = 0;
-  int pst = 0;              // stage the producer fills next
-  int cst = 0, cpar = 0;    // stage and phase parity the consumer waits on next
-  bool timed_out = false;
-
-  int tn_base = -1, tn_val = -1;  // next table slice, loaded ahead into registers
-  auto table_entry = [&](int bj) -> int {
-    // warp-collective: physical block of block bj of the producer's sequence
-    const int nb = prod.nblk;
-    const int32_t* row = p.block_tables + static_cast<int64_t>(prod.s) * p.max_blocks_per_seq;
-    if (prod.s != tb_seq || bj < tb_base || bj >= tb_base + 32) {
-      if (prod.s == tb_seq && tn_base == tb_base + 32 && bj >= tn_base && bj < tn_base + 32) {
-        tb_base = tn_base;
-        tb_val = tn_val;
-      } else {
-        tb_seq = prod.s;
-        tb_base = bj;
-        tb_val = (bj + lane < nb) ? __ldg(row + bj + lane) : -1;
-      }
-      tn_base = -1;
+  // ---- 4. the share of consumer c (global consumer id gc)
+  const int nw_total = gridDim.x * W;
+  const long long U = prefix[S];
+  long long want = (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp;
+  const int nw_eff = fixed ? nw_total : static_cast<int>(want < 1 ? 1 : (want < nw_total ? want : nw_total));
+  auto start_iter = [&](WorkIter& w, int gc) {
+    w.frag_idx = 0;
+    w.gw = gc;
+    w.valid = false;
+    if (fixed) {
+      w.R = static_cast<int>(U);
+      w.rstride = nw_total;
+      w.r = gc;
+      if (w.r < w.R) { w.valid = true; frag_fixed(w, prefix, p, UR); }
+    } else if (U > 0 && gc < nw_eff) {
+      w.u = gc * U / nw_eff;
+      w.u1 = (gc + 1) * U / nw_eff;
+      if (w.u < w.u1) { w.valid = true; frag_balanced(w, prefix, p); }
     }
-    if (tn_base < 0 && bj >= tb_base + 8 && tb_base + 32 < nb) {
-      tn_base = tb_base + 32;  // issue the next slice now; it is first used 24 blocks later
-      tn_val = (tn_base + lane < nb) ? __ldg(row + tn_base + lane) : -1;
-    }
-    int phys = __shfl_sync(0xffffffffu, tb_val, bj - tb_base);
-    if (phys < 0 || phys >= p.num_blocks) {
-      if (lane == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
-      phys = 0;
-    }
-    return phys;
   };
 
-  auto produce = [&](void) {
-    while (prod.valid && issued - consumed < NS) {
-      const bool new_frag = (prod.j == prod.j0);
-      if (new_frag && prod.frag_idx >= it.frag_idx + 2) break;  // raw-q double buffer busy
-      const uint32_t bar = bar0 + 8 * pst;
-      const uint32_t kdst = wbase_u32 + Tr::OFF_STAGES + pst * Tr::STAGE;
-      const uint32_t vdst = kdst + Tr::TILE;
-      // blocks of this unit that hold rows of the sequence (later ones are skipped)
-      const int bj0 = unit_in_block ? (prod.j >> upb_shift) : (prod.j << bpu_shift);
-      const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, prod.nblk - bj0);
-      const int row_in_block = unit_in_block ? (prod.j - (bj0 << upb_shift)) * UR : 0;
-      const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
-      if (lane == 0) mbar_arrive_expect_tx(bar, 2u * nbox * BOX * Tr::ROW + qbytes);
-      for (int i = 0; i < nbox; ++i) {
-        const int phys = table_entry(bj0 + i);
-        if (lane == 0) {
-          const int z = (phys * Hkv + prod.kvh) * B + row_in_block;
-          tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, 0, z, bar);
-          tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, 0, z, bar);
+  if (warp == 0) {
+    // =================================================================== producer
+    // Lane c feeds consumer c: one unit per free stage of its ring.
+    WorkIter it;
+    it.valid = false;
+    if (lane < W) start_iter(it, blockIdx.x * W + lane);
+    const uint32_t cbase = base_u32 + (lane < W ? lane : 0) * wsm;
+    int pst = 0, pph = 1, issued = 0;
+    uint64_t wait_since = 0;
+    int nx_s = -1, nx_bj = -1;  // table entries of the next unit, loaded ahead
+    int nx_phys[4] = {0, 0, 0, 0};
+    while (__any_sync(0xffffffffu, it.valid)) {
+      bool did = false;
+      if (it.valid) {
+        bool ready = issued < NS || mbar_test_wait(cbase + Tr::OFF_EMPTY + 8 * pst, pph);
+        if (!ready) {
+          const uint64_t now = global_timer_ns();
+          if (wait_since == 0) {
+            wait_since = now;
+          } else if (now - wait_since > kWaitLimitNs) {
+            raise_error(p.err, PA_DEVERR_TIMEOUT);
+            it.valid = false;  // give up on this consumer; it times out on its own
+          }
+        } else {
+          wait_since = 0;
+          const bool new_frag = (it.j == it.j0);
+          const uint32_t bar = cbase + Tr::OFF_FULL + 8 * pst;
+          const uint32_t kdst = cbase + Tr::OFF_STAGES + pst * Tr::STAGE;
+          const uint32_t vdst = kdst + Tr::TILE;
+          const int bj0 = unit_in_block ? (it.j >> upb_shift) : (it.j << bpu_shift);
+          const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
+          const int row_in_block = unit_in_block ? (it.j - (bj0 << upb_shift)) * UR : 0;
+          const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
+          int phys[4];
+          if (nx_s == it.s && nx_bj == bj0) {  // entries loaded while issuing the previous unit
+#pragma unroll
+            for (int i = 0; i < 4; ++i) phys[i] = nx_phys[i];
+          } else {
+            const int32_t* trow = p.block_tables + static_cast<int64_t>(it.s) * p.max_blocks_per_seq + bj0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) phys[i] = (i < nbox) ? __ldg(trow + i) : 0;
+          }
+          mbar_arrive_expect_tx(bar, 2u * nbox * BOX * Tr::ROW + qbytes);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (i < nbox) {
+              int pb = phys[i];
+              if (pb < 0 || pb >= p.num_blocks) {
+                raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                pb = 0;
+              }
+              const int z = (pb * Hkv + it.kvh) * B + row_in_block;
+              tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, 0, z, bar);
+              tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, 0, z, bar);
+            }
+          }
+          if (new_frag) {
+            const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
+                                  (static_cast<int64_t>(it.s) * p.q_stride + static_cast<int64_t>(it.kvh) * G * D) * 2;
+            bulk_load(kdst + 2 * Tr::TILE, qsrc, qbytes, bar);
+          }
+          ++issued;
+          if (++pst == NS) {
+            pst = 0;
+            pph ^= 1;
+          }
+          // load the next unit's table entries now; they are used one refill later
+          nx_s = -1;
+          if (it.j + 1 < it.jend) {
+            const int nj = it.j + 1;
+            const int nbj0 = unit_in_block ? (nj >> upb_shift) : (nj << bpu_shift);
+            if (nbj0 != bj0) {
+              const int nnbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - nbj0);
+              const int32_t* trow = p.block_tables + static_cast<int64_t>(it.s) * p.max_blocks_per_seq + nbj0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) nx_phys[i] = (i < nnbox) ? __ldg(trow + i) : 0;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) nx_phys[i] = phys[i];
+            }
+            nx_s = it.s;
+            nx_bj = nbj0;
+          }
+          if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, UR);
+          did = true;
         }
       }
-      if (lane == 0 && new_frag) {
-        const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
-                              (static_cast<int64_t>(prod.s) * p.q_stride + static_cast<int64_t>(prod.kvh) * G * D) * 2;
-        bulk_load(qraw_u32 + (prod.frag_idx & 1) * Tr::QRAW_STRIDE, qsrc, qbytes, bar);
-      }
-      ++issued;
-      if (++pst == NS) pst = 0;
-      if (++prod.j == prod.jend) iter_next_fragment(prod, prefix, p, fixed, UR);
+      if (!__any_sync(0xffffffffu, did)) __nanosleep(64);
     }
-  };
+    return;
+  }
 
-  produce();
-
+  // ===================================================================== consumer
+  const int c = warp - 1;
+  WorkIter it;
+  start_iter(it, blockIdx.x * W + c);
+  if (!it.valid) return;
+  uint8_t* wbase = base + c * wsm;
+  const uint32_t wbase_u32 = base_u32 + c * wsm;
+  float* qf = reinterpret_cast<float*>(wbase + Tr::OFF_QF32);
+  float2* pbuf = reinterpret_cast<float2*>(wbase + Tr::OFF_PBUF);
+  int cst = 0, cpar = 0;
   // QK lane roles.  LPT = 2: lane pairs share a token (t = lane/2), each one
   // part of the row (qd = lane & 1).  LPT = 1: one token per lane, visiting
   // the halves of a 256-byte row in an order rotated by bit 2 of the token.
@@ -535,15 +563,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   };
 
   while (it.valid) {
-    if (!mbar_wait_bounded(bar0 + 8 * cst, cpar, kWaitLimitNs)) {
-      timed_out = true;
-      break;
+    if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
+      if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
+      break;  // the producer stops feeding this ring when its empty barrier times out
     }
+    const uint8_t* stage = wbase + Tr::OFF_STAGES + cst * Tr::STAGE;
     if (it.j == it.j0) {
       // new fragment: widen + pre-scale the query group, reset the state
       float qs = p.qk_scale_log2;
       if constexpr (kFp8) qs *= __ldg(p.k_scale + it.kvh);
-      const uint8_t* qr = qraw_base + (it.frag_idx & 1) * Tr::QRAW_STRIDE;
+      const uint8_t* qr = stage + 2 * Tr::TILE;  // the query group rode on this stage
       for (int idx = lane; idx < GM * D / 2; idx += 32) {
         const int e = 2 * idx;
         const int g = e / D;
@@ -568,14 +597,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     }
 
     const int n_valid = min(UR, it.T - it.j * UR);
-    const uint8_t* stage = wbase + Tr::OFF_STAGES + cst * Tr::STAGE;
     if (n_valid == UR) {
       unit_step(std::true_type{}, stage, UR);
     } else {
       unit_step(std::false_type{}, stage, n_valid);
     }
     __syncwarp();
-    ++consumed;
+    if (lane == 0) mbar_arrive(wbase_u32 + Tr::OFF_EMPTY + 8 * cst);  // the stage may be refilled
     if (++cst == NS) {
       cst = 0;
       cpar ^= 1;
@@ -688,16 +716,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
     }
     if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, UR);
-    produce();
-  }
-
-  if (timed_out) {
-    if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
-    // let this warp's copies in flight land before the CTA can exit
-    for (int k = consumed; k < issued; ++k)
-      (void)mbar_wait_bounded(bar0 + 8 * (k % NS), (k / NS) & 1, kWaitLimitNs);
   }
 }
+
 
 // ----------------------------------------------------------------- host side of one variant
 
@@ -707,14 +728,14 @@ struct DecodeVariant {
 
   static size_t smem_bytes(int num_seqs, int warps, int stages) {
     return 1024 + static_cast<size_t>(warps) * Tr::warp_smem(stages) +
-           static_cast<size_t>(align_up_c((num_seqs + 1 + warps) * 4, 16));
+           static_cast<size_t>(align_up_c((num_seqs + 1 + warps + 1) * 4, 16));
   }
 
-  // Launch geometry: pipeline depth (stages per warp) and warps per CTA.
-  // Default depth keeps about kStageBytesPerWarp of K/V per warp; the warps
-  // per CTA maximise resident warps per SM (ties: more warps per CTA, i.e.
-  // fewer CTAs running the prologue).  PA_DECODE_STAGES / PA_DECODE_WARPS
-  // override both (tuning).
+  // Launch geometry: pipeline depth (stages per consumer) and consumer warps
+  // per CTA (plus one producer warp).  Default depth keeps about
+  // kStageBytesPerWarp of K/V per consumer; the consumers per CTA maximise
+  // resident consumer warps per SM (ties: more per CTA, i.e. fewer producer
+  // warps).  PA_DECODE_STAGES / PA_DECODE_WARPS override both (tuning).
   static bool geometry(int num_seqs, DecodeGeometry* g) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -727,7 +748,7 @@ struct DecodeVariant {
     if (env_ns >= 2 && env_ns <= Tr::MAX_NS) ns = env_ns;
     const int env_w = tuning_override("PA_DECODE_WARPS");
     int best_w = 0, best_occ = 0, best_warps = 0;
-    for (int w = 1; w <= Tr::MAX_W; w *= 2) {
+    for (int w = 1; w <= Tr::MAX_W; ++w) {
       if (env_w > 0 && w != env_w) continue;
       const size_t smem = smem_bytes(num_seqs, w, ns);
       if (smem > 227 * 1024) break;
@@ -735,7 +756,7 @@ struct DecodeVariant {
           cudaSuccess)
         return false;
       int occ = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, w * 32, smem) != cudaSuccess) return false;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (w + 1) * 32, smem) != cudaSuccess) return false;
       if (occ * w >= best_warps && occ > 0) {
         best_warps = occ * w;
         best_w = w;
@@ -758,12 +779,12 @@ struct DecodeVariant {
   static cudaError_t launch(const DecodeGeometry& g, const DecodeParams& p, const CUtensorMap& tk,
                             const CUtensorMap& tv, cudaStream_t stream) {
     (void)cudaGetLastError();  // an earlier unrelated error must not be reported as this launch's
-    paged_decode_kernel<QT, KVT, D, GM, UR><<<g.ctas, g.warps_per_cta * 32, g.smem_bytes, stream>>>(tk, tv, p);
+    paged_decode_kernel<QT, KVT, D, GM, UR><<<g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, stream>>>(tk, tv, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       cudaFuncAttributes fa;
       if (cudaFuncGetAttributes(&fa, paged_decode_kernel<QT, KVT, D, GM, UR>) == cudaSuccess)
-        note_launch_failure(g.ctas, g.warps_per_cta * 32, g.smem_bytes, g.stages, fa.maxThreadsPerBlock,
+        note_launch_failure(g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, g.stages, fa.maxThreadsPerBlock,
                             fa.maxDynamicSharedSizeBytes, fa.numRegs, fa.localSizeBytes);
     }
     return e;
