@@ -71,9 +71,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D view of a cache pool: {128-byte half of a row, halves, rows}, with
-// num_blocks*Hkv*B rows of head_dim elements.  One TMA box = box_rows whole
-// rows, 128-byte swizzle, landing in shared memory row after row.
+// 3-D view of a cache pool: {128 bytes of a row, rows, 128-byte halves of a
+// row}, with num_blocks*Hkv*B rows of head_dim elements.  One TMA box =
+// box_rows whole rows with the 128-byte swizzle, landing in shared memory as
+// [half][row][128 bytes], so that each half-plane is swizzled by row.
 bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, int num_kv_heads,
                       int block_size, int head_dim, int elem_bytes, int box_rows) {
   if (box_rows % pa::kBoxRowQuantum != 0 || box_rows > 256) return false;
@@ -83,9 +84,9 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, i
   if (row_bytes % 128 != 0) return false;
   const cuuint32_t half_elems = static_cast<cuuint32_t>(128 / elem_bytes);
   const cuuint32_t halves = static_cast<cuuint32_t>(row_bytes / 128);
-  cuuint64_t dims[3] = {half_elems, halves, static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size};
-  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(row_bytes)};
-  cuuint32_t box[3] = {half_elems, halves, static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t dims[3] = {half_elems, static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size, halves};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), 128};
+  cuuint32_t box[3] = {half_elems, static_cast<cuuint32_t>(box_rows), halves};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                          const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -96,13 +97,13 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, i
 
 int gmax_for_group(int g) { return g <= 1 ? 1 : (g <= 4 ? 4 : 8); }
 
-// Rows per work unit (measured on GB300): 16 for 16-bit caches (two lanes
-// per token in QK), 32 for FP8 caches (one lane per 128-byte row).
-// PA_DECODE_UNIT_ROWS (16 or 32) overrides it (tuning).
-int unit_rows_for(int kv_dtype, int /*gmax*/) {
+// Rows per work unit: 32 (four 8-token MMA n-tiles per pipeline stage; on
+// GB300 it beat 16 rows for every dtype measured).  PA_DECODE_UNIT_ROWS (16
+// or 32) overrides it (tuning).
+int unit_rows_for(int /*kv_dtype*/, int /*gmax*/) {
   const int env = pa::tuning_override("PA_DECODE_UNIT_ROWS");
   if (env == 16 || env == 32) return env;
-  return kv_dtype == PA_FP8_E4M3 ? 32 : 16;
+  return 32;
 }
 
 // Shape checks shared by pa_decode and pa_decode_workspace_bytes.

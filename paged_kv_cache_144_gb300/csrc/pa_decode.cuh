@@ -9,18 +9,19 @@
 // and folded into a running (m, l, acc) state with the online-softmax
 // recurrence (equation (4) of the auturnal.com review: m' = max(m, max s_j),
 // l' = e^{m-m'} l + sum e^{s_j-m'}, acc rescaled by the same factor); the
-// recurrence runs in base 2 with log2(e) folded into the query.
+// recurrence runs in base 2 with log2(e) folded into the scale.
 //
 // How it is laid out on GB300 (this is not the pages' A100 kernel design):
 //  * Work unit = UR (16 or 32) consecutive rows of one (sequence, KV head).
-//    A unit is filled by 3-D TMA boxes of min(UR, B) whole rows (each row is
-//    one or two 128-byte halves, 128-byte swizzle): part of one block when
-//    B >= UR, one box per block when a unit spans several blocks; one TMA
-//    instruction per box for K and one for V.  The units of the whole
-//    batch, ordered (s, kvh, unit), are split into equal contiguous ranges, one
-//    per resident warp, so long and short sequences load every SM equally
-//    ("balanced" mode).  A range crosses (s, kvh) segments freely.  Optionally
-//    each warp instead takes fixed partitions of P tokens.
+//    A unit is filled by 3-D TMA boxes of min(UR, B) whole rows: part of one
+//    block when B >= UR, one box per block when a unit spans several blocks;
+//    one TMA instruction per box for K and one for V.  A box lands as
+//    [128-byte half of the row][row][128 bytes] with the 128-byte swizzle, so
+//    each half-plane is swizzled by row.  The units of the whole batch,
+//    ordered (s, kvh, unit), are split into equal contiguous ranges, one per
+//    resident warp, so long and short sequences load every SM equally
+//    ("balanced" mode).  A range crosses (s, kvh) segments freely.
+//    Optionally each warp instead takes fixed partitions of P tokens.
 //  * Warp specialisation: each CTA has W consumer warps and one producer
 //    warp.  Consumer warp c owns a ring of stages in shared memory (one unit
 //    of K, of V and, at a segment start, the query group per stage).  Lane c
@@ -29,16 +30,22 @@
 //    (cp.async.bulk.tensor) plus a 1-D bulk copy of the query group, all
 //    completing on the stage's "full" mbarrier.  Consumers only wait, compute
 //    and release.  No CTA-wide barrier is used after the prologue.
-//  * QK: 32/UR lanes per token (one for UR=32), each a part of the row, form
-//    the dot products with all G query heads of the group in packed fp32x2
-//    FMAs (several independent accumulators per head); the pre-scaled fp32
-//    query group is read from shared memory with broadcasts; the lane ->
-//    (token, half) order is chosen so that, with the swizzle, every quarter
-//    warp's K reads hit distinct banks.
-//  * PV: each lane owns D/32 output columns of all G heads (fp32 registers)
-//    and walks the tile's valid tokens, reading p from shared memory.
-//  * FP8 tiles are widened in registers (e4m3 -> f16x2 -> f32); the per-head
-//    K scale is folded into the query and the V scale into the final divide.
+//  * The two contractions of a unit run on the tensor cores (mma.sync
+//    m16n8k16, fp32 accumulate) in the register layout of that instruction:
+//    S^T = Q K^T with the query group as the 16-row A operand (rows >= G are
+//    zero) and 8 tokens per n-tile, then O^T += V^T P^T with 16 head_dim
+//    columns per m-tile, whose B operand (P^T) is exactly the C fragment of
+//    S^T after the softmax.  At the GB300's ratio of issue slots to HBM bytes
+//    the fp32-FMA formulation of these products is instruction-bound; the
+//    tensor-core one is not.  The probabilities enter the second product as
+//    a hi + lo pair of 16-bit values (two MMAs), which keeps their rounding
+//    error near 2^-16 relative.
+//  * 16-bit caches feed the MMAs with ldmatrix (K) and ldmatrix.trans (V)
+//    straight from the swizzled tiles.  FP8 caches are widened in registers
+//    (e4m3 -> f16x2, exact) with the head_dim order of QK permuted so that a
+//    lane reads 16 contiguous bytes of a K row, and V transposed in registers
+//    with byte permutes; the per-head K scale multiplies the scores, the V
+//    scale the final divide, and q is rounded to f16 for the product.
 //  * Split segments: a warp whose range covers only part of a segment writes
 //    its (m, l, acc) record to the workspace and bumps the segment's arrival
 //    counter; the warp that arrives last merges all records with the same
@@ -77,33 +84,25 @@ struct DecodeTraits {
   static constexpr int UR = UR_;                 // rows per work unit (16 or 32)
   static_assert(UR == 16 || UR == 32, "unit rows");
   static constexpr int NSUB = ROW / 128;         // 128-byte halves per row
-  static constexpr int SUB_ELEMS = 128 / KVB;    // elements per half
   static constexpr int TILE = UR * ROW;          // bytes of one unit of K (or V)
   static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
   static constexpr int STAGE = align_up_c(2 * TILE + QRAW, 1024);  // K tile + V tile + raw q
   static constexpr int MAX_NS = 8;               // stages per consumer (chosen at launch, 2..MAX_NS)
-  static constexpr int MAX_W = 8;                // consumer warps per CTA (chosen at launch)
-  static constexpr int LPT = 32 / UR;            // lanes per token in QK (2 or 1)
-  static constexpr int CHUNKS = ROW / 16;        // 16-byte chunks per row
-  static constexpr int EPC = 16 / KVB;           // elements per chunk
-  static constexpr int EPL = D / 32;             // PV columns per lane
-  // The query group lives in shared memory as NPART padded parts per head:
-  // the part a QK lane reads (LPT = 2) or the half it reads (LPT = 1).
-  static constexpr int NPART = (LPT == 2 || NSUB == 2) ? 2 : 1;
-  static constexpr int PART = D / NPART;         // elements per part
-  static constexpr int CPP = CHUNKS / NPART;     // chunks per part
-  static constexpr int QROW = NPART * (PART + 4);  // floats per head (4 floats of padding per part)
-  static constexpr int NACC = (GM >= 8) ? 2 : 4;  // independent QK accumulators per head
-  // per-consumer shared memory: [fp32 q | p | full[MAX_NS] | empty[MAX_NS] | NS stages]
-  static constexpr int OFF_QF32 = 0;
-  static constexpr int OFF_PBUF = OFF_QF32 + GM * QROW * 4;
-  static constexpr int OFF_FULL = align_up_c(OFF_PBUF + UR * GM * 8, 8);
+  static constexpr int MAX_W = 7;                // consumer warps per CTA (with the producer: 8 warps, up to 255 registers)
+  static constexpr int KS = D / 16;              // k-steps of S^T = Q K^T, m-tiles of O^T
+  static constexpr int NT = UR / 8;              // 8-token n-tiles of a unit
+  static constexpr int NSB = UR / 16;            // 16-token sub-tiles (one PV k-step each)
+  static constexpr bool FP8 = KVB == 1;
+  static constexpr bool MMA_BF16 = !FP8 && std::is_same<KVT, bf16_t>::value;  // else f16
+  static_assert(!FP8 || D == 128, "FP8 caches: head_dim 128");
+  // per-consumer shared memory: [full[MAX_NS] | empty[MAX_NS] | NS stages]
+  static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + MAX_NS * 8;
-  static constexpr int OFF_STAGES = align_up_c(OFF_EMPTY + MAX_NS * 8, 1024);
+  static constexpr int OFF_STAGES = 1024;
+  static_assert(OFF_EMPTY + MAX_NS * 8 <= OFF_STAGES, "barriers");
   __host__ __device__ static constexpr int warp_smem(int ns) { return OFF_STAGES + ns * STAGE; }
-  static constexpr int REC = align_up_c(GM * (D + 2), 4);  // floats per partial record
-  static_assert(EPL == 2 || EPL == 4, "D/32 columns per lane");
-  static_assert(EPC % 4 == 0 && PART % 4 == 0, "chunk split");
+  // partial record: acc as [D][GM] (head fastest), then m[GM], l[GM]
+  static constexpr int REC = align_up_c(GM * (D + 2), 4);
 };
 
 // Length of sequence s clamped to the table's capacity (error bit if outside).
@@ -191,6 +190,124 @@ __device__ __forceinline__ void iter_next_fragment(WorkIter& it, const int* pref
     it.u += it.jend - it.j0;
     if (it.u >= it.u1) { it.valid = false; return; }
     frag_balanced(it, prefix, p);
+  }
+}
+
+// Where the partial record of fragment f of a split segment lives.
+struct MergeSlots {
+  bool fixed;
+  int fixed_base;       // fixed partitions: slot of partition 0 of the segment
+  int first_w;          // balanced split: global warp id of the first fragment
+  long long U;          // balanced split: total units
+  int nw_eff;           // balanced split: warps sharing the units
+  long long seg_start;  // balanced split: first unit of the segment
+  __device__ __forceinline__ int slot(int f) const {
+    if (fixed) return fixed_base + f;
+    const int w = first_w + f;
+    const long long rs = static_cast<long long>(w) * U / nw_eff;
+    return 2 * w + (rs < seg_start ? 1 : 0);
+  }
+};
+
+// Merges the nfr partial (m, l, acc) records of one segment with the
+// online-softmax recurrence and writes out[orow .. orow+G-1].  Run by the
+// warp that arrived last.  Lane f first holds record f's weights e^(m_f - M);
+// the warp then walks the records RB at a time with all their loads in
+// flight, lane i owning head_dim columns [i*D/32, (i+1)*D/32) of every head.
+template <int GM, int D, int REC>
+__device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int G,
+                                              float vs, void* out, int out_dtype, int64_t orow) {
+  constexpr int EPL = D / 32;       // columns per lane
+  constexpr int NF = EPL * GM;      // floats per lane per record (contiguous)
+  constexpr int RB = NF >= 32 ? 2 : (NF >= 16 ? 4 : 8);
+  const int e0 = lane * EPL;
+  float M[GM], L[GM];
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+    M[g] = -INFINITY;
+    L[g] = 0.f;
+  }
+  for (int f0 = 0; f0 < nfr; f0 += 32) {
+    if (f0 + lane < nfr) {
+      const float* rf = records + static_cast<int64_t>(ms.slot(f0 + lane)) * REC + GM * D;
+#pragma unroll
+      for (int g = 0; g < GM; ++g) M[g] = fmaxf(M[g], __ldcg(rf + g));
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < GM; ++g)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
+  float o[NF];
+#pragma unroll
+  for (int i = 0; i < NF; ++i) o[i] = 0.f;
+  for (int f0 = 0; f0 < nfr; f0 += 32) {
+    const int nb = min(32, nfr - f0);
+    float wf[GM];
+    int my_slot = 0;
+    if (lane < nb) {
+      my_slot = ms.slot(f0 + lane);
+      const float* rf = records + static_cast<int64_t>(my_slot) * REC + GM * D;
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        // M is finite: every record covers at least one valid row
+        wf[g] = exp2f(__ldcg(rf + g) - M[g]);
+        L[g] += wf[g] * __ldcg(rf + GM + g);
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < GM; ++g) wf[g] = 0.f;
+    }
+    for (int k = 0; k < nb; k += RB) {
+      float v[RB][NF];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const int sr = __shfl_sync(0xffffffffu, my_slot, (k + r) & 31);
+        if (k + r < nb) {
+          const float* rf = records + static_cast<int64_t>(sr) * REC + e0 * GM;
+          if constexpr (NF % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < NF; i += 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(rf + i));
+              v[r][i] = x.x;
+              v[r][i + 1] = x.y;
+              v[r][i + 2] = x.z;
+              v[r][i + 3] = x.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < NF; i += 2) {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(rf + i));
+              v[r][i] = x.x;
+              v[r][i + 1] = x.y;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+          const float w = __shfl_sync(0xffffffffu, wf[g], (k + r) & 31);
+          if (k + r < nb) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e * GM + g] = fmaf(w, v[r][e * GM + g], o[e * GM + g]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < GM; ++g)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) L[g] += __shfl_xor_sync(0xffffffffu, L[g], off);
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+    if (g < G) {
+      const float inv = vs / L[g];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, (orow + g) * D + e0 + e, o[e * GM + g] * inv);
+    }
   }
 }
 
@@ -358,8 +475,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                 pb = 0;
               }
               const int z = (pb * Hkv + it.kvh) * B + row_in_block;
-              tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, 0, z, bar);
-              tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, 0, z, bar);
+              tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, z, 0, bar);
+              tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, z, 0, bar);
             }
           }
           if (new_frag) {
@@ -399,252 +516,293 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   }
 
   // ===================================================================== consumer
+  constexpr bool MB = Tr::MMA_BF16;
   const int c = warp - 1;
   WorkIter it;
   start_iter(it, blockIdx.x * W + c);
   if (!it.valid) return;
-  uint8_t* wbase = base + c * wsm;
+  const uint8_t* wbase = base + c * wsm;
   const uint32_t wbase_u32 = base_u32 + c * wsm;
-  float* qf = reinterpret_cast<float*>(wbase + Tr::OFF_QF32);
-  float2* pbuf = reinterpret_cast<float2*>(wbase + Tr::OFF_PBUF);
   int cst = 0, cpar = 0;
-  // QK lane roles.  LPT = 2: lane pairs share a token (t = lane/2), each one
-  // part of the row (qd = lane & 1).  LPT = 1: one token per lane, visiting
-  // the halves of a 256-byte row in an order rotated by bit 2 of the token.
-  const int t = (Tr::LPT == 2) ? (lane >> 1) : lane;
-  const int qd = (Tr::LPT == 2) ? (lane & 1) : 0;
-  const int rot = (Tr::LPT == 1 && Tr::NPART == 2) ? ((t >> 2) & 1) : 0;
-  const int e0 = lane * Tr::EPL;  // first PV column of this lane
-  // byte offset of K chunk ch of half h in row t of a stage (128-byte swizzle)
-  auto kaddr = [&](int h, int ch) -> uint32_t {
-    return t * Tr::ROW + h * 128 + (((ch ^ (t * Tr::NSUB + h)) & 7) << 4);
+  const int gid = lane >> 2;  // fragment row group: query head of S^T, column of O^T
+  const int tig = lane & 3;
+
+  // Byte offset of 16-byte chunk ch of row t in a K or V tile: a box of BOX
+  // rows per block is stored as NSUB half-planes [BOX rows][128 B], each
+  // swizzled by row (chunk ^ row % 8).
+  const int bshift = unit_in_block ? (UR == 32 ? 5 : 4) : p.block_shift;  // log2(BOX)
+  const int plane = BOX * 128;
+  auto chunk_off = [&](int t, int ch) -> uint32_t {
+    return static_cast<uint32_t>(((t >> bshift) * Tr::NSUB + (ch >> 3)) * plane + (t & (BOX - 1)) * 128 +
+                                 (((ch & 7) ^ (t & 7)) << 4));
   };
-  // V: this lane's columns of row r; the swizzle phase repeats every 8/NSUB rows
-  constexpr int VPER = 8 / Tr::NSUB;
-  const int vbyte = e0 * Tr::KVB;
-  const int vh = vbyte >> 7;
-  const int vch = (vbyte & 127) >> 4;
-  uint32_t vofs[VPER];
+  // offset between the two 16-row sub-tiles of a 32-row unit (same for every lane)
+  const uint32_t sub_delta = BOX >= 32 ? 2048u : static_cast<uint32_t>(Tr::NSUB * 2048);
+
+  // 16-bit tiles: the row address this lane gives to ldmatrix at k-step s
+  // (K) or m-tile s (V).  Matrices 0..3 = (rows 0-7, cols lo), (rows 0-7,
+  // cols hi), (rows 8-15, cols lo), (rows 8-15, cols hi) of a 16x16 block.
+  uint32_t moff[Tr::KS];
+  // FP8 tiles: n-position j of an 8-token n-tile holds token j ^ 4(j & 1),
+  // which keeps both the K and the V loads below free of bank conflicts.
+  auto sigma = [](int j) { return j ^ ((j & 1) << 2); };
+  uint32_t kb8[2], vb8[2][Tr::KS / 2];
+  if constexpr (!kFp8) {
+    const int lt = (lane & 7) + ((lane >> 4) << 3);
+    const int lhi = (lane >> 3) & 1;
 #pragma unroll
-  for (int k = 0; k < VPER; ++k) vofs[k] = Tr::TILE + vh * 128 + (((vch ^ (k * Tr::NSUB + vh)) & 7) << 4) + (vbyte & 15);
-  // q parts this lane reads: LPT = 2 -> part qd; LPT = 1 -> parts (pi ^ rot)
-  const float* qpart0 = qf + ((Tr::LPT == 2 ? qd : rot) * (Tr::PART + 4));
-  const float* qpart1 = qf + ((Tr::LPT == 2 ? qd : (rot ^ 1)) * (Tr::PART + 4));
+    for (int s = 0; s < Tr::KS; ++s) moff[s] = chunk_off(lt, 2 * s + lhi);
+  } else {
+    // K: token sigma(gid) of each n-tile, chunks tig and 4 + tig (16 head_dim
+    // values each, consumed as 4 k-steps of 4 values).
+    const int sg = sigma(gid);
+#pragma unroll
+    for (int g = 0; g < 2; ++g) kb8[g] = chunk_off(sg, 4 * g + tig);
+    // V: tokens sigma(2t), sigma(2t+1); 4 bytes at head_dim column 32 jj + 4 gid.
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int st = sigma(2 * tig + e);
+#pragma unroll
+      for (int jj = 0; jj < Tr::KS / 2; ++jj) vb8[e][jj] = chunk_off(st, 2 * jj + (gid >> 2)) + 4 * (gid & 3);
+    }
+  }
+  // head_dim column of accumulator row (m-tile i, half hf) of O^T
+  auto dim_of = [&](int i, int hf) -> int {
+    if constexpr (!kFp8) return 16 * i + gid + 8 * hf;
+    return 32 * (i >> 1) + 4 * gid + 2 * (i & 1) + hf;
+  };
 
-  float m[GM], l[GM];
-  float2 acc[GM][Tr::EPL / 2];
+  uint32_t qa0[Tr::KS], qa1[Tr::KS];  // A operand (query group), rows gid < G; rows g+8 are zero
+  float m = -INFINITY, l = 0.f;       // running max / sum of head gid (log2 domain)
+  float acc[Tr::KS][4];               // O^T: rows = head_dim columns, cols = heads 2t, 2t+1
+  float score_scale = p.qk_scale_log2;
 
-  // V row -> EPL floats as float2 pairs
-  auto load_v = [&](const uint8_t* row_ptr, float2* vf) {
-    if constexpr (Tr::KVB == 2) {
-      if constexpr (Tr::EPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(row_ptr);
-        vf[0] = widen2<KVT>(w.x);
-        vf[1] = widen2<KVT>(w.y);
-      } else {
-        vf[0] = widen2<KVT>(*reinterpret_cast<const uint32_t*>(row_ptr));
+  // One unit: S^T = Q K^T, online-softmax update, O^T += V^T P^T.
+  // FULL: all UR rows valid.
+  auto unit_step = [&](auto full_tag, uint32_t kt, int n_valid) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const uint32_t vt = kt + Tr::TILE;
+    float sc[Tr::NT][4];
+#pragma unroll
+    for (int nt = 0; nt < Tr::NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    // ---- scores
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int sb = 0; sb < Tr::NSB; ++sb) {
+#pragma unroll
+        for (int s = 0; s < Tr::KS; ++s) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kt + sb * sub_delta + moff[s], b0, b1, b2, b3);
+          mma16816<MB>(sc[2 * sb], qa0[s], 0u, qa1[s], 0u, b0, b1);
+          mma16816<MB>(sc[2 * sb + 1], qa0[s], 0u, qa1[s], 0u, b2, b3);
+        }
       }
     } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(row_ptr);
-      vf[0] = widen2_e4m3(w & 0xffffu);
-      vf[1] = widen2_e4m3(w >> 16);
-    }
-  };
-  // acc[g] += p[tok][g] * v for all heads (p stored as (p, p) pairs)
-  auto accumulate = [&](const float2* prow, const float2* vf) {
 #pragma unroll
-    for (int g = 0; g < GM; g += 2) {
-      if (g + 1 < GM) {
-        const float4 pp = *reinterpret_cast<const float4*>(prow + g);
+      for (int nt = 0; nt < Tr::NT; ++nt) {
 #pragma unroll
-        for (int i = 0; i < Tr::EPL / 2; ++i) {
-          acc[g][i] = ffma2(make_float2(pp.x, pp.y), vf[i], acc[g][i]);
-          acc[g + 1][i] = ffma2(make_float2(pp.z, pp.w), vf[i], acc[g + 1][i]);
-        }
-      } else {
-        const float2 pp = prow[g];
+        for (int g = 0; g < 2; ++g) {
+          const uint4 w = lds128(kt + nt * 1024 + kb8[g]);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = ffma2(pp, vf[i], acc[g][i]);
-      }
-    }
-  };
-
-  // One unit (8 rows): scores, online-softmax update, p . V.  FULL: all 8 rows valid.
-  auto unit_step = [&](auto full_tag, const uint8_t* stage, int n_valid) {
-    constexpr bool FULL = decltype(full_tag)::value;
-    // ---- scores: the lane dots its part(s) of token t's K row with all G query heads
-    float2 sacc[Tr::NACC][GM];
-#pragma unroll
-    for (int a = 0; a < Tr::NACC; ++a)
-#pragma unroll
-      for (int g = 0; g < GM; ++g) sacc[a][g] = make_float2(0.f, 0.f);
-    constexpr int NPI = (Tr::LPT == 2) ? 1 : Tr::NPART;  // parts this lane visits
-#pragma unroll
-    for (int pi = 0; pi < NPI; ++pi) {
-      const int pp = (Tr::LPT == 2) ? qd : (pi ^ rot);   // part index
-      const float* qp0 = pi == 0 ? qpart0 : qpart1;
-#pragma unroll
-      for (int c = 0; c < Tr::CPP; ++c) {
-        // chunk c of part pp -> half h, chunk-in-half ch
-        const int cb = pp * Tr::CPP + c;                  // chunk within the row
-        const uint4 raw = *reinterpret_cast<const uint4*>(stage + kaddr(cb >> 3, cb & 7));
-        float2 kf[Tr::EPC / 2];
-        Chunk<KVT>::cvt(raw, kf);
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          const float4* qp = reinterpret_cast<const float4*>(qp0 + g * Tr::QROW + c * Tr::EPC);
-#pragma unroll
-          for (int i = 0; i < Tr::EPC / 4; ++i) {
-            const float4 q4 = qp[i];
-            float2& sa = sacc[(2 * i) % Tr::NACC][g];
-            sa = ffma2(make_float2(q4.x, q4.y), kf[2 * i], sa);
-            float2& sb = sacc[(2 * i + 1) % Tr::NACC][g];
-            sb = ffma2(make_float2(q4.z, q4.w), kf[2 * i + 1], sb);
+          for (int r = 0; r < 4; ++r) {
+            const int s = 4 * g + r;
+            mma16816<false>(sc[nt], qa0[s], 0u, qa1[s], 0u, e4m3x2_to_f16x2(ws[r] & 0xffffu),
+                            e4m3x2_to_f16x2(ws[r] >> 16));
           }
         }
       }
     }
-    float sv[GM];
-    bool up = false;
+    // ---- online softmax on head gid's scores (quad lanes share a head)
+    float mx = -INFINITY;
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      float2 s2 = sacc[0][g];
+    for (int nt = 0; nt < Tr::NT; ++nt) {
 #pragma unroll
-      for (int a = 1; a < Tr::NACC; ++a) s2 = make_float2(s2.x + sacc[a][g].x, s2.y + sacc[a][g].y);
-      float x = s2.x + s2.y;
-      if constexpr (Tr::LPT == 2) x += __shfl_xor_sync(0xffffffffu, x, 1);
-      if constexpr (!FULL) x = (t < n_valid) ? x : -INFINITY;
-      sv[g] = x;
-      up |= x > m[g];
-    }
-    // ---- online softmax: the running maximum only moves when some score exceeds it
-    if (__any_sync(0xffffffffu, up)) {
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        float bm = sv[g];
-#pragma unroll
-        for (int o = Tr::LPT; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-        const float mn = fmaxf(m[g], bm);
-        const float alpha = fast_exp2(m[g] - mn);
-        m[g] = mn;
-        l[g] *= alpha;
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = fmul2(acc[g][i], a2);
+      for (int e = 0; e < 2; ++e) {
+        float x = sc[nt][e] * score_scale;
+        if constexpr (!FULL) {
+          const int tok = nt * 8 + (kFp8 ? sigma(2 * tig + e) : 2 * tig + e);
+          x = tok < n_valid ? x : -INFINITY;
+        }
+        sc[nt][e] = x;
+        mx = fmaxf(mx, x);
       }
     }
-    float pg[GM];
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (__any_sync(0xffffffffu, mx > m)) {
+      const float mn = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - mn);
+      m = mn;
+      l *= alpha;
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);      // head 2t
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);  // head 2t+1
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      pg[g] = fast_exp2(sv[g] - m[g]);
-      l[g] += (qd == 0) ? pg[g] : 0.f;
+      for (int i = 0; i < Tr::KS; ++i) {
+        acc[i][0] *= a0;
+        acc[i][1] *= a1;
+        acc[i][2] *= a0;
+        acc[i][3] *= a1;
+      }
     }
-    if (qd == 0) {
-      float2* prow = pbuf + t * GM;
+    // P^T as the B operand of each 16-token k-step, split hi + lo
+    uint32_t ph[Tr::NSB][2], pl[Tr::NSB][2];
 #pragma unroll
-      for (int g = 0; g < GM; g += 2) {
-        if (g + 1 < GM) {
-          *reinterpret_cast<float4*>(prow + g) = make_float4(pg[g], pg[g], pg[g + 1], pg[g + 1]);
-        } else {
-          prow[g] = make_float2(pg[g], pg[g]);
+    for (int nt = 0; nt < Tr::NT; ++nt) {
+      const float p0 = fast_exp2(sc[nt][0] - m);
+      const float p1 = fast_exp2(sc[nt][1] - m);
+      l += p0 + p1;
+      const uint32_t h = pack2<MB>(p0, p1);
+      const float2 hf = unpack2<MB>(h);
+      ph[nt >> 1][nt & 1] = h;
+      pl[nt >> 1][nt & 1] = pack2<MB>(p0 - hf.x, p1 - hf.y);
+    }
+    // rows past the end of the sequence may hold anything: zero them in V
+    if constexpr (!FULL) {
+      const int nz = (UR - n_valid) * Tr::NSUB * 8;
+      for (int k = lane; k < nz; k += 32) {
+        const int r = n_valid + k / (Tr::NSUB * 8);
+        const int ch = k % (Tr::NSUB * 8);
+        sts128_zero(vt + chunk_off(r, ch));
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+    // ---- O^T += V^T P^T
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int sb = 0; sb < Tr::NSB; ++sb) {
+#pragma unroll
+        for (int i = 0; i < Tr::KS; ++i) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vt + sb * sub_delta + moff[i], a0, a1, a2, a3);
+          mma16816<MB>(acc[i], a0, a1, a2, a3, ph[sb][0], ph[sb][1]);
+          mma16816<MB>(acc[i], a0, a1, a2, a3, pl[sb][0], pl[sb][1]);
         }
       }
-    }
-    __syncwarp();
-    // ---- p . V: lane owns columns e0..e0+EPL-1 of all G heads
+    } else {
 #pragma unroll
-    for (int tt = 0; tt < UR; ++tt) {
-      if (FULL || tt < n_valid) {
-        float2 vf[Tr::EPL / 2];
-        load_v(stage + vofs[tt % VPER] + tt * Tr::ROW, vf);
-        accumulate(pbuf + tt * GM, vf);
+      for (int sb = 0; sb < Tr::NSB; ++sb) {
+#pragma unroll
+        for (int jj = 0; jj < Tr::KS / 2; ++jj) {
+          // tokens of k 2t, 2t+1 (n-tile 2 sb) and k 2t+8, 2t+9 (n-tile 2 sb + 1)
+          const uint32_t x0 = lds32(vt + (2 * sb) * 1024 + vb8[0][jj]);
+          const uint32_t x1 = lds32(vt + (2 * sb) * 1024 + vb8[1][jj]);
+          const uint32_t y0 = lds32(vt + (2 * sb + 1) * 1024 + vb8[0][jj]);
+          const uint32_t y1 = lds32(vt + (2 * sb + 1) * 1024 + vb8[1][jj]);
+          const uint32_t lo01 = prmt(x0, x1, 0x5140u), lo23 = prmt(x0, x1, 0x7362u);
+          const uint32_t hi01 = prmt(y0, y1, 0x5140u), hi23 = prmt(y0, y1, 0x7362u);
+          const uint32_t d0l = e4m3x2_to_f16x2(lo01 & 0xffffu), d1l = e4m3x2_to_f16x2(lo01 >> 16);
+          const uint32_t d2l = e4m3x2_to_f16x2(lo23 & 0xffffu), d3l = e4m3x2_to_f16x2(lo23 >> 16);
+          const uint32_t d0h = e4m3x2_to_f16x2(hi01 & 0xffffu), d1h = e4m3x2_to_f16x2(hi01 >> 16);
+          const uint32_t d2h = e4m3x2_to_f16x2(hi23 & 0xffffu), d3h = e4m3x2_to_f16x2(hi23 >> 16);
+          mma16816<false>(acc[2 * jj], d0l, d1l, d0h, d1h, ph[sb][0], ph[sb][1]);
+          mma16816<false>(acc[2 * jj], d0l, d1l, d0h, d1h, pl[sb][0], pl[sb][1]);
+          mma16816<false>(acc[2 * jj + 1], d2l, d3l, d2h, d3h, ph[sb][0], ph[sb][1]);
+          mma16816<false>(acc[2 * jj + 1], d2l, d3l, d2h, d3h, pl[sb][0], pl[sb][1]);
+        }
       }
     }
   };
 
   while (it.valid) {
+    // ---- one fragment: units j0 .. jend-1 of segment (s, kvh)
     if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
       if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
       break;  // the producer stops feeding this ring when its empty barrier times out
     }
-    const uint8_t* stage = wbase + Tr::OFF_STAGES + cst * Tr::STAGE;
-    if (it.j == it.j0) {
-      // new fragment: widen + pre-scale the query group, reset the state
-      float qs = p.qk_scale_log2;
-      if constexpr (kFp8) qs *= __ldg(p.k_scale + it.kvh);
-      const uint8_t* qr = stage + 2 * Tr::TILE;  // the query group rode on this stage
-      for (int idx = lane; idx < GM * D / 2; idx += 32) {
-        const int e = 2 * idx;
-        const int g = e / D;
-        const int ed = e % D;
-        float2 v2 = make_float2(0.f, 0.f);
-        if (g < G) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(qr + 4 * idx);
-          v2 = widen2<QT>(w);
-          v2.x *= qs;
-          v2.y *= qs;
+    {
+      // the query group rode on the fragment's first stage
+      const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * Tr::STAGE + 2 * Tr::TILE;
+      const bool row_ok = gid < G;
+#pragma unroll
+      for (int s = 0; s < Tr::KS; ++s) {
+        // columns of k-step s held by this lane: (d, d+1) for a0, (d2, d2+1) for a2
+        const int d = kFp8 ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 16 * s + 2 * tig;
+        const int d2 = kFp8 ? d + 2 : d + 8;
+        uint32_t w0 = 0u, w1 = 0u;
+        if (row_ok) {
+          w0 = *reinterpret_cast<const uint32_t*>(qr + (gid * D + d) * 2);
+          w1 = *reinterpret_cast<const uint32_t*>(qr + (gid * D + d2) * 2);
         }
-        *reinterpret_cast<float2*>(qf + g * Tr::QROW + (ed / Tr::PART) * (Tr::PART + 4) + ed % Tr::PART) = v2;
+        if constexpr (kFp8 && std::is_same<QT, bf16_t>::value) {
+          const float2 f0 = widen2<bf16_t>(w0), f1 = widen2<bf16_t>(w1);
+          w0 = pack2<false>(f0.x, f0.y);
+          w1 = pack2<false>(f1.x, f1.y);
+        }
+        qa0[s] = w0;
+        qa1[s] = w1;
       }
+    }
+    score_scale = p.qk_scale_log2;
+    if constexpr (kFp8) score_scale *= __ldg(p.k_scale + it.kvh);
+    m = -INFINITY;
+    l = 0.f;
 #pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < Tr::EPL / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
+    for (int i = 0; i < Tr::KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    bool timed_out = false;
+    for (;;) {
+      const uint32_t stage_u32 = wbase_u32 + Tr::OFF_STAGES + cst * Tr::STAGE;
+      const int n_valid = min(UR, it.T - it.j * UR);
+      if (n_valid == UR) {
+        unit_step(std::true_type{}, stage_u32, UR);
+      } else {
+        unit_step(std::false_type{}, stage_u32, n_valid);
       }
       __syncwarp();
+      if (lane == 0) mbar_arrive(wbase_u32 + Tr::OFF_EMPTY + 8 * cst);  // the stage may be refilled
+      if (++cst == NS) {
+        cst = 0;
+        cpar ^= 1;
+      }
+      if (it.j + 1 == it.jend) break;
+      ++it.j;
+      if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
+        if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
+        timed_out = true;
+        break;
+      }
     }
-
-    const int n_valid = min(UR, it.T - it.j * UR);
-    if (n_valid == UR) {
-      unit_step(std::true_type{}, stage, UR);
-    } else {
-      unit_step(std::false_type{}, stage, n_valid);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(wbase_u32 + Tr::OFF_EMPTY + 8 * cst);  // the stage may be refilled
-    if (++cst == NS) {
-      cst = 0;
-      cpar ^= 1;
-    }
+    if (timed_out) break;
 
     // ---- end of fragment: write the output or a partial record
-    if (it.j + 1 == it.jend) {
-      float lt[GM];
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        float x = l[g];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        lt[g] = x;
-      }
+    {
+      float lt = l + __shfl_xor_sync(0xffffffffu, l, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);            // head gid's sum
+      const float l0 = __shfl_sync(0xffffffffu, lt, 8 * tig);      // head 2t
+      const float l1 = __shfl_sync(0xffffffffu, lt, 8 * tig + 4);  // head 2t+1
+      const int h0 = 2 * tig, h1 = 2 * tig + 1;
       float vs = 1.f;
       if constexpr (kFp8) vs = __ldg(p.v_scale + it.kvh);
       const int64_t orow = static_cast<int64_t>(it.s) * p.num_heads + static_cast<int64_t>(it.kvh) * G;
       if (it.slot < 0) {
+        const float i0 = vs / l0, i1 = vs / l1;
 #pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          if (g < G) {
-            const float inv = vs / lt[g];
+        for (int i = 0; i < Tr::KS; ++i) {
 #pragma unroll
-            for (int i = 0; i < Tr::EPL / 2; ++i) {
-              store_out(p.out, p.out_dtype, (orow + g) * D + e0 + 2 * i, acc[g][i].x * inv);
-              store_out(p.out, p.out_dtype, (orow + g) * D + e0 + 2 * i + 1, acc[g][i].y * inv);
-            }
+          for (int hf = 0; hf < 2; ++hf) {
+            const int d = dim_of(i, hf);
+            if (h0 < G) store_out(p.out, p.out_dtype, (orow + h0) * D + d, acc[i][2 * hf] * i0);
+            if (h1 < G) store_out(p.out, p.out_dtype, (orow + h1) * D + d, acc[i][2 * hf + 1] * i1);
           }
         }
       } else {
         float* rec = p.part_records + static_cast<int64_t>(it.slot) * Tr::REC;
 #pragma unroll
-        for (int g = 0; g < GM; ++g) {
+        for (int i = 0; i < Tr::KS; ++i) {
 #pragma unroll
-          for (int i = 0; i < Tr::EPL / 2; ++i)
-            *reinterpret_cast<float2*>(rec + g * D + e0 + 2 * i) = acc[g][i];
-          if (lane == g) {
-            rec[GM * D + g] = m[g];
-            rec[GM * D + GM + g] = lt[g];
+          for (int hf = 0; hf < 2; ++hf) {
+            const int d = dim_of(i, hf);
+            if constexpr (GM == 1) {
+              if (tig == 0) rec[d] = acc[i][2 * hf];
+            } else {
+              if (h0 < GM) *reinterpret_cast<float2*>(rec + d * GM + h0) = make_float2(acc[i][2 * hf], acc[i][2 * hf + 1]);
+            }
           }
+        }
+        if (tig == 0 && gid < GM) {
+          rec[GM * D + gid] = m;
+          rec[GM * D + GM + gid] = lt;
         }
         __threadfence();
         __syncwarp();
@@ -668,54 +826,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         }
         if (old == nfr - 1) {
           __threadfence();
-          float M[GM], L[GM];
-          float2 o2[GM][Tr::EPL / 2];
-#pragma unroll
-          for (int g = 0; g < GM; ++g) {
-            M[g] = -INFINITY;
-            L[g] = 0.f;
-#pragma unroll
-            for (int i = 0; i < Tr::EPL / 2; ++i) o2[g][i] = make_float2(0.f, 0.f);
-          }
-          auto slot_of = [&](int f) -> int {
-            if (fixed) return prefix[it.s] + it.kvh * parts + f;
-            const int w = first_slot_w + f;
-            const long long rs = static_cast<long long>(w) * U / nw_eff;
-            return 2 * w + (rs < seg_start ? 1 : 0);
-          };
-          for (int f = 0; f < nfr; ++f) {
-            const float* rf = p.part_records + static_cast<int64_t>(slot_of(f)) * Tr::REC;
-#pragma unroll
-            for (int g = 0; g < GM; ++g) M[g] = fmaxf(M[g], __ldcg(rf + GM * D + g));
-          }
-          for (int f = 0; f < nfr; ++f) {
-            const float* rf = p.part_records + static_cast<int64_t>(slot_of(f)) * Tr::REC;
-#pragma unroll
-            for (int g = 0; g < GM; ++g) {
-              const float w = exp2f(__ldcg(rf + GM * D + g) - M[g]);
-              L[g] += w * __ldcg(rf + GM * D + GM + g);
-              const float2 w2 = make_float2(w, w);
-#pragma unroll
-              for (int i = 0; i < Tr::EPL / 2; ++i)
-                o2[g][i] = ffma2(w2, __ldcg(reinterpret_cast<const float2*>(rf + g * D + e0 + 2 * i)), o2[g][i]);
-            }
-          }
-#pragma unroll
-          for (int g = 0; g < GM; ++g) {
-            if (g < G) {
-              const float inv = vs / L[g];
-#pragma unroll
-              for (int i = 0; i < Tr::EPL / 2; ++i) {
-                store_out(p.out, p.out_dtype, (orow + g) * D + e0 + 2 * i, o2[g][i].x * inv);
-                store_out(p.out, p.out_dtype, (orow + g) * D + e0 + 2 * i + 1, o2[g][i].y * inv);
-              }
-            }
-          }
+          MergeSlots ms;
+          ms.fixed = fixed;
+          ms.fixed_base = fixed ? prefix[it.s] + it.kvh * parts : 0;
+          ms.first_w = first_slot_w;
+          ms.U = U;
+          ms.nw_eff = nw_eff;
+          ms.seg_start = seg_start;
+          merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, G, vs, p.out, p.out_dtype, orow);
           if (lane == 0) p.seg_counters[it.s * Hkv + it.kvh] = 0;
         }
       }
     }
-    if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, UR);
+    ++it.j;
+    iter_next_fragment(it, prefix, p, fixed, UR);
   }
 }
 
