@@ -97,13 +97,17 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, i
 
 int gmax_for_group(int g) { return g <= 1 ? 1 : (g <= 4 ? 4 : 8); }
 
-// Rows per work unit: 32 (four 8-token MMA n-tiles per pipeline stage; on
-// GB300 it beat 16 rows for every dtype measured).  PA_DECODE_UNIT_ROWS (16
-// or 32) overrides it (tuning).
-int unit_rows_for(int /*kv_dtype*/, int /*gmax*/) {
+// Rows per work unit: 32 for 16-bit caches (16 KB of K + V per stage at
+// d = 128), 64 for FP8 caches with B >= 16 (the same 16 KB per stage, half
+// the refills per byte of 32 rows).  A unit spans at most four blocks, so
+// 64-row units need B >= 16.  PA_DECODE_UNIT_ROWS (16, 32; 64 for FP8)
+// overrides it (tuning).
+int unit_rows_for(int kv_dtype, int block_size) {
+  const bool fp8 = kv_dtype == PA_FP8_E4M3;
   const int env = pa::tuning_override("PA_DECODE_UNIT_ROWS");
   if (env == 16 || env == 32) return env;
-  return 32;
+  if (env == 64 && fp8 && block_size >= 16) return 64;
+  return fp8 && block_size >= 16 ? 64 : 32;
 }
 
 // Shape checks shared by pa_decode and pa_decode_workspace_bytes.
@@ -114,7 +118,7 @@ int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_d
   if (num_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (kv_dtype == PA_FP8_E4M3 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  // a power of two from 8 to 1024: a work unit (16 or 32 rows) then covers
+  // a power of two from 8 to 1024: a work unit (16, 32 or 64 rows) then covers
   // whole blocks or a whole fraction of one
   if (block_size < 8 || block_size > 1024 || (block_size & (block_size - 1)) != 0) return PA_ERR_UNSUPPORTED;
   if (partition_size < 0 || (partition_size > 0 && partition_size % block_size != 0)) return PA_ERR_SHAPE;
@@ -141,7 +145,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
   plan->key.kv_dtype = kv_dtype;
   plan->key.head_dim = head_dim;
   plan->key.gmax = gmax_for_group(num_heads / num_kv_heads);
-  plan->key.unit_rows = unit_rows_for(kv_dtype, plan->key.gmax);
+  plan->key.unit_rows = unit_rows_for(kv_dtype, block_size);
   if (!pa::decode_geometry(plan->key, num_seqs, &plan->geo)) return PA_ERR_UNSUPPORTED;
   const int ur = plan->geo.unit_rows;
   const int max_units = static_cast<int>((static_cast<int64_t>(max_blocks_per_seq) * block_size + ur - 1) / ur);

@@ -12,7 +12,7 @@
 // recurrence runs in base 2 with log2(e) folded into the scale.
 //
 // How it is laid out on GB300 (this is not the pages' A100 kernel design):
-//  * Work unit = UR (16 or 32) consecutive rows of one (sequence, KV head).
+//  * Work unit = UR (16, 32; 64 for FP8) consecutive rows of one (sequence, KV head).
 //    A unit is filled by 3-D TMA boxes of min(UR, B) whole rows: part of one
 //    block when B >= UR, one box per block when a unit spans several blocks;
 //    one TMA instruction per box for K and one for V.  A box lands as
@@ -66,6 +66,7 @@ namespace pa {
 constexpr int kMinUnitsPerWarp = 2;            // smallest balanced share (small batches spread wide)
 constexpr int kStageBytesPerWarp = 24 * 1024;  // default K/V pipeline bytes per consumer warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kTablePrefetch = 3;              // units whose table entries the producer fetches ahead
 
 // Integer tuning override from the environment (read once per name), or -1.
 int tuning_override(const char* name);
@@ -81,8 +82,9 @@ struct DecodeTraits {
   static constexpr int KVB = elem<KVT>::bytes;
   static constexpr int ROW = D * KVB;  // bytes of one cache row
   static_assert(ROW == 128 || ROW == 256, "cache rows must be 128 or 256 bytes");
-  static constexpr int UR = UR_;                 // rows per work unit (16 or 32)
-  static_assert(UR == 16 || UR == 32, "unit rows");
+  static constexpr int UR = UR_;                 // rows per work unit (16, 32; 64 for FP8)
+  static_assert(UR == 16 || UR == 32 || (UR == 64 && KVB == 1), "unit rows");
+  static constexpr int UR_SHIFT = UR == 64 ? 6 : (UR == 32 ? 5 : 4);
   static constexpr int NSUB = ROW / 128;         // 128-byte halves per row
   static constexpr int TILE = UR * ROW;          // bytes of one unit of K (or V)
   static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
@@ -158,7 +160,7 @@ __device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, c
   it.jend = it.j0 + static_cast<int>(fend - it.u);
   const bool whole = (it.u == seg_start) && (fend == seg_end);
   it.slot = whole ? -1 : it.gw * 2 + (it.frag_idx == 0 ? 0 : 1);
-  it.T = clamped_len(p, s, false);
+  it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
   it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
 }
 
@@ -170,7 +172,7 @@ __device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, cons
   it.s = s;
   it.kvh = rr / parts;
   const int part = rr % parts;
-  it.T = clamped_len(p, s, false);
+  it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
   it.nu = (it.T + UR - 1) / UR;
   it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
   it.j0 = part * p.partition_units;
@@ -211,23 +213,38 @@ struct MergeSlots {
 
 // Merges the nfr partial (m, l, acc) records of one segment with the
 // online-softmax recurrence and writes out[orow .. orow+G-1].  Run by the
-// warp that arrived last.  Lane f first holds record f's weights e^(m_f - M);
-// the warp then walks the records RB at a time with all their loads in
-// flight, lane i owning head_dim columns [i*D/32, (i+1)*D/32) of every head.
+// warp that arrived last.  Lane f holds record f's (m, l) and weights
+// e^(m_f - M); the warp then walks the records RB at a time with all their
+// loads in flight, lane i owning head_dim columns [i*D/32, (i+1)*D/32) of
+// every head.
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int G,
                                               float vs, void* out, int out_dtype, int64_t orow) {
   constexpr int EPL = D / 32;       // columns per lane
   constexpr int NF = EPL * GM;      // floats per lane per record (contiguous)
-  constexpr int RB = NF >= 32 ? 2 : (NF >= 16 ? 4 : 8);
+  constexpr int RB = NF >= 32 ? 2 : (NF >= 16 ? 4 : 8);  // 64 floats in flight per lane (registers)
   const int e0 = lane * EPL;
-  float M[GM], L[GM];
+  // records 0..31: slot, m and l on lane f (kept for the second pass)
+  int slot0 = 0;
+  float m0[GM], l0[GM], M[GM], L[GM];
 #pragma unroll
   for (int g = 0; g < GM; ++g) {
-    M[g] = -INFINITY;
+    m0[g] = -INFINITY;
+    l0[g] = 0.f;
     L[g] = 0.f;
   }
-  for (int f0 = 0; f0 < nfr; f0 += 32) {
+  if (lane < nfr) {
+    slot0 = ms.slot(lane);
+    const float* rf = records + static_cast<int64_t>(slot0) * REC + GM * D;
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+      m0[g] = __ldcg(rf + g);
+      l0[g] = __ldcg(rf + GM + g);
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < GM; ++g) M[g] = m0[g];
+  for (int f0 = 32; f0 < nfr; f0 += 32) {
     if (f0 + lane < nfr) {
       const float* rf = records + static_cast<int64_t>(ms.slot(f0 + lane)) * REC + GM * D;
 #pragma unroll
@@ -244,19 +261,27 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
   for (int f0 = 0; f0 < nfr; f0 += 32) {
     const int nb = min(32, nfr - f0);
     float wf[GM];
-    int my_slot = 0;
-    if (lane < nb) {
+    int my_slot = slot0;
+    float mf[GM], lf[GM];
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+      mf[g] = m0[g];
+      lf[g] = l0[g];
+    }
+    if (f0 > 0 && lane < nb) {
       my_slot = ms.slot(f0 + lane);
       const float* rf = records + static_cast<int64_t>(my_slot) * REC + GM * D;
 #pragma unroll
       for (int g = 0; g < GM; ++g) {
-        // M is finite: every record covers at least one valid row
-        wf[g] = exp2f(__ldcg(rf + g) - M[g]);
-        L[g] += wf[g] * __ldcg(rf + GM + g);
+        mf[g] = __ldcg(rf + g);
+        lf[g] = __ldcg(rf + GM + g);
       }
-    } else {
+    }
 #pragma unroll
-      for (int g = 0; g < GM; ++g) wf[g] = 0.f;
+    for (int g = 0; g < GM; ++g) {
+      // M is finite: every record covers at least one valid row
+      wf[g] = lane < nb ? exp2f(mf[g] - M[g]) : 0.f;
+      L[g] += wf[g] * (lane < nb ? lf[g] : 0.f);
     }
     for (int k = 0; k < nb; k += RB) {
       float v[RB][NF];
@@ -334,14 +359,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // one TMA box per block it touches, BOX rows high.  B is a power of two.
   const bool unit_in_block = B >= UR;
   const int BOX = unit_in_block ? UR : B;
-  const int upb_shift = unit_in_block ? p.block_shift - (UR == 32 ? 5 : 4) : 0;  // log2(units per block)
-  const int bpu_shift = unit_in_block ? 0 : (UR == 32 ? 5 : 4) - p.block_shift;  // log2(blocks per unit)
+  const int upb_shift = unit_in_block ? p.block_shift - Tr::UR_SHIFT : 0;  // log2(units per block)
+  const int bpu_shift = unit_in_block ? 0 : Tr::UR_SHIFT - p.block_shift;  // log2(blocks per unit)
   const bool fixed = p.partition_units > 0;
 
   const int NS = p.stages;  // pipeline depth per consumer
   const int wsm = Tr::warp_smem(NS);
+  // shared: prefix[S+1] (units before sequence s), lens[S] (clamped seq_lens),
+  // scan scratch, then the producer's block-table ring (16 ints per consumer)
   int* prefix = reinterpret_cast<int*>(base + W * wsm);
-  int* scan_tmp = prefix + (S + 1);
+  int* lens = prefix + (S + 1);
+  int* scan_tmp = lens + S;
+  const uint32_t table_ring_u32 = base_u32 + W * wsm + align_up_c((2 * S + 1 + NWARP) * 4, 16);
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);
@@ -356,6 +385,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       int units = 0;
       if (s < S) {
         const int T = clamped_len(p, s, blockIdx.x == 0);
+        lens[s] = T;
         const int nu = (T + UR - 1) / UR;
         units = (fixed ? (nu + p.partition_units - 1) / p.partition_units : nu) * Hkv;
       }
@@ -382,7 +412,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
   // ---- 2. empty sequences attend to nothing: their outputs are zero
   for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
-    if (clamped_len(p, s, false) == 0) {
+    if (lens[s] == 0) {
       const int64_t n = static_cast<int64_t>(p.num_heads) * D;
       for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
     }
@@ -425,15 +455,32 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
   if (warp == 0) {
     // =================================================================== producer
-    // Lane c feeds consumer c: one unit per free stage of its ring.
-    WorkIter it;
+    // Lane c feeds consumer c: one unit per free stage of its ring.  The
+    // block-table entries of a unit are copied into shared memory
+    // (cp.async, no register dependency) kTablePrefetch units before the
+    // unit is issued, so that a table read never stalls the warp.
+    WorkIter it, ah;  // next unit to issue; next unit whose table entries to fetch
     it.valid = false;
     if (lane < W) start_iter(it, blockIdx.x * W + lane);
+    ah = it;
     const uint32_t cbase = base_u32 + (lane < W ? lane : 0) * wsm;
+    const uint32_t ring = table_ring_u32 + (lane < W ? lane : 0) * 64;  // 4 units x 4 entries
     int pst = 0, pph = 1, issued = 0;
+    int pf = 0, rs_use = 0, rs_pf = 0;  // units fetched ahead; ring slots to read / fill
     uint64_t wait_since = 0;
-    int nx_s = -1, nx_bj = -1;  // table entries of the next unit, loaded ahead
-    int nx_phys[4] = {0, 0, 0, 0};
+    auto fetch_tables = [&]() {
+      const int bj = unit_in_block ? (ah.j >> upb_shift) : (ah.j << bpu_shift);
+      const int nb = unit_in_block ? 1 : min(1 << bpu_shift, ah.nblk - bj);
+      const int32_t* src = p.block_tables + static_cast<int64_t>(ah.s) * p.max_blocks_per_seq + bj;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i < nb) cp_async4(ring + (rs_pf * 4 + i) * 4, src + i);
+      cp_async_commit();
+      rs_pf = (rs_pf + 1) & 3;
+      ++pf;
+      if (++ah.j == ah.jend) iter_next_fragment(ah, prefix, p, fixed, UR);
+    };
+    while (ah.valid && pf < kTablePrefetch) fetch_tables();
     while (__any_sync(0xffffffffu, it.valid)) {
       bool did = false;
       if (it.valid) {
@@ -456,15 +503,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
           const int row_in_block = unit_in_block ? (it.j - (bj0 << upb_shift)) * UR : 0;
           const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
-          int phys[4];
-          if (nx_s == it.s && nx_bj == bj0) {  // entries loaded while issuing the previous unit
-#pragma unroll
-            for (int i = 0; i < 4; ++i) phys[i] = nx_phys[i];
+          // this unit's entries were fetched pf - 1 units before the newest fetch
+          if (pf >= 3) {
+            cp_async_wait<2>();
+          } else if (pf == 2) {
+            cp_async_wait<1>();
           } else {
-            const int32_t* trow = p.block_tables + static_cast<int64_t>(it.s) * p.max_blocks_per_seq + bj0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) phys[i] = (i < nbox) ? __ldg(trow + i) : 0;
+            cp_async_wait<0>();
           }
+          int phys[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) phys[i] = (i < nbox) ? static_cast<int>(lds32(ring + (rs_use * 4 + i) * 4)) : 0;
+          rs_use = (rs_use + 1) & 3;
+          --pf;
           mbar_arrive_expect_tx(bar, 2u * nbox * BOX * Tr::ROW + qbytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -489,29 +540,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             pst = 0;
             pph ^= 1;
           }
-          // load the next unit's table entries now; they are used one refill later
-          nx_s = -1;
-          if (it.j + 1 < it.jend) {
-            const int nj = it.j + 1;
-            const int nbj0 = unit_in_block ? (nj >> upb_shift) : (nj << bpu_shift);
-            if (nbj0 != bj0) {
-              const int nnbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - nbj0);
-              const int32_t* trow = p.block_tables + static_cast<int64_t>(it.s) * p.max_blocks_per_seq + nbj0;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) nx_phys[i] = (i < nnbox) ? __ldg(trow + i) : 0;
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) nx_phys[i] = phys[i];
-            }
-            nx_s = it.s;
-            nx_bj = nbj0;
-          }
+          if (ah.valid) fetch_tables();
           if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, UR);
           did = true;
         }
       }
       if (!__any_sync(0xffffffffu, did)) __nanosleep(64);
     }
+    cp_async_wait<0>();  // nothing of ours may still land in shared memory after exit
     return;
   }
 
@@ -530,7 +566,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // Byte offset of 16-byte chunk ch of row t in a K or V tile: a box of BOX
   // rows per block is stored as NSUB half-planes [BOX rows][128 B], each
   // swizzled by row (chunk ^ row % 8).
-  const int bshift = unit_in_block ? (UR == 32 ? 5 : 4) : p.block_shift;  // log2(BOX)
+  const int bshift = unit_in_block ? Tr::UR_SHIFT : p.block_shift;  // log2(BOX)
   const int plane = BOX * 128;
   auto chunk_off = [&](int t, int ch) -> uint32_t {
     return static_cast<uint32_t>(((t >> bshift) * Tr::NSUB + (ch >> 3)) * plane + (t & (BOX - 1)) * 128 +
@@ -852,7 +888,7 @@ struct DecodeVariant {
 
   static size_t smem_bytes(int num_seqs, int warps, int stages) {
     return 1024 + static_cast<size_t>(warps) * Tr::warp_smem(stages) +
-           static_cast<size_t>(align_up_c((num_seqs + 1 + warps + 1) * 4, 16));
+           static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1) * 4, 16)) + static_cast<size_t>(warps) * 64;
   }
 
   // Launch geometry: pipeline depth (stages per consumer) and consumer warps
