@@ -26,6 +26,11 @@ Readings where the pages are silent (each also listed in the design doc):
   * FP8 KV ([P2] §"KV量子化"): value = float64(e4m3 code) * float64(scale[h])
     with one float32 scale per KV head, separately for K and V.
   * a sequence of length 0 attends to nothing; its output is defined as 0.
+  * sliding window (named as a limitation of the paged kernel in the
+    "局限性与未来工作" list of the dihengye.cn notes, no definition given):
+    with a window W > 0 the single query of a sequence of length T, which sits
+    at position T-1, attends to positions max(0, T-W) .. T-1 only; W = 0
+    means the whole sequence.
 
 Pins: brute-force triple loop, textbook numpy attention for MHA, T=1 -> v_0,
 constant keys -> mean(V), one dominant logit -> that V row, block-layout
@@ -79,9 +84,14 @@ def _scale64(scale: float) -> float:
     return float(np.float32(scale))
 
 
+def window_start(seq_len: int, window: int) -> int:
+    """First attended position of the query at position seq_len-1 (window 0 = all)."""
+    return max(0, int(seq_len) - int(window)) if window and window > 0 else 0
+
+
 def paged_decode_attention_one(q, k_cache, v_cache, block_tables, seq_lens, scale,
                                block_size, s, h, *, q_fmt="f16", kv_fmt="f16",
-                               k_scale=None, v_scale=None, num_kv_heads=None):
+                               k_scale=None, v_scale=None, num_kv_heads=None, window=0):
     """Output vector out[s, h, :] only (for sampled checks on large inputs).
 
     ``k_cache``/``v_cache`` may be the full pool or any array indexable by the
@@ -98,15 +108,16 @@ def paged_decode_attention_one(q, k_cache, v_cache, block_tables, seq_lens, scal
     vb = v_cache[phys, kvh]
     ks = None if k_scale is None else np.asarray(k_scale)[kvh:kvh + 1]
     vs = None if v_scale is None else np.asarray(v_scale)[kvh:kvh + 1]
-    Kf = dequantize_kv(kb[:, None], kv_fmt, ks)[:, 0].reshape(-1, kb.shape[-1])[:T]
-    Vf = dequantize_kv(vb[:, None], kv_fmt, vs)[:, 0].reshape(-1, vb.shape[-1])[:T]
+    lo = window_start(T, window)
+    Kf = dequantize_kv(kb[:, None], kv_fmt, ks)[:, 0].reshape(-1, kb.shape[-1])[lo:T]
+    Vf = dequantize_kv(vb[:, None], kv_fmt, vs)[:, 0].reshape(-1, vb.shape[-1])[lo:T]
     qv = storage_to_f64(q[s, h], q_fmt)
     return dense_decode_attention(qv, Kf, Vf, _scale64(scale))
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size,
-                           *, q_fmt="f16", kv_fmt="f16", k_scale=None, v_scale=None):
-    """out[S, H_q, d] float64 for every sequence and query head."""
+                           *, q_fmt="f16", kv_fmt="f16", k_scale=None, v_scale=None, window=0):
+    """out[S, H_q, d] float64 for every sequence and query head (window: see module notes)."""
     S, Hq, d = q.shape
     Hkv = k_cache.shape[1]
     if Hq % Hkv != 0:
@@ -119,9 +130,10 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, b
     out = np.zeros((S, Hq, d), dtype=np.float64)
     for s in range(S):
         T = int(seq_lens[s])
+        lo = window_start(T, window)
         for kvh in range(Hkv):
-            K = gather_sequence(Kc, block_tables[s], T, block_size, kvh)
-            V = gather_sequence(Vc, block_tables[s], T, block_size, kvh)
+            K = gather_sequence(Kc, block_tables[s], T, block_size, kvh)[lo:]
+            V = gather_sequence(Vc, block_tables[s], T, block_size, kvh)[lo:]
             for g in range(G):
                 h = kvh * G + g
                 out[s, h] = dense_decode_attention(qf[s, h], K, V, sc)

@@ -539,3 +539,96 @@ def test_pins_catch_planted_mistakes():
     assert check_brute_force(_paged_transposed_block) > 1e-3
     assert check_gqa_reduces_to_mha(_paged_wrong_group) > 1e-3
     assert check_e4m3_ties(_e4m3_ties_away) > 0
+
+
+# ----------------------------------------------------------------------------- sliding window
+
+def check_window_brute_force(paged_fn, seed=21):
+    """Hand loop over positions max(0, T-W) .. T-1 for every (sequence, head)."""
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for B in [1, 4, 16]:
+        for W in [1, 3, 17, 64]:
+            q, kc, vc, tables, lens = _tiny_paged(rng, 3, 4, 2, 4, B, 40)
+            out = paged_fn(q, kc, vc, tables, lens, 0.6, B, window=W)
+            for s in range(3):
+                T = int(lens[s])
+                for h in range(4):
+                    kvh = h // 2
+                    rows_k, rows_v = [], []
+                    for p in range(max(0, T - W), T):
+                        blk = int(tables[s][p // B])
+                        rows_k.append([float(x) for x in kc[blk, kvh, p % B]])
+                        rows_v.append([float(x) for x in vc[blk, kvh, p % B]])
+                    ref = _brute_force_one([float(x) for x in q[s, h]], rows_k, rows_v, float(np.float32(0.6)))
+                    worst = max(worst, float(np.max(np.abs(np.array(ref) - out[s, h]))))
+    return worst
+
+
+def test_window_brute_force():
+    assert check_window_brute_force(oracle.paged_decode_attention) <= 1e-12
+
+
+def test_window_covering_sequence_is_full_attention():
+    rng = np.random.default_rng(22)
+    q, kc, vc, tables, lens = _tiny_paged(rng, 4, 4, 4, 8, 16, 60)
+    full = oracle.paged_decode_attention(q, kc, vc, tables, lens, 0.4, 16)
+    for W in (60, 61, 1000):
+        assert np.array_equal(oracle.paged_decode_attention(q, kc, vc, tables, lens, 0.4, 16, window=W), full)
+
+
+def test_window_one_returns_newest_row():
+    rng = np.random.default_rng(23)
+    q, kc, vc, tables, lens = _tiny_paged(rng, 3, 2, 2, 8, 4, 30)
+    out = oracle.paged_decode_attention(q, kc, vc, tables, lens, 0.4, 4, window=1)
+    for s in range(3):
+        p = int(lens[s]) - 1
+        blk = int(tables[s][p // 4])
+        for h in range(2):
+            assert np.array_equal(out[s, h], vc[blk, h, p % 4].astype(np.float64))
+
+
+def test_window_ignores_rows_before_it():
+    """Rows before the window may hold anything (NaN here) without changing the result."""
+    rng = np.random.default_rng(24)
+    q, kc, vc, tables, lens = _tiny_paged(rng, 3, 4, 2, 8, 4, 40)
+    lens = np.maximum(lens, 12).astype(np.int32)
+    nbs = -(-lens // 4)
+    NB = kc.shape[0]
+    need = int(nbs.sum()) + 3
+    if need > NB:
+        kc = np.concatenate([kc, rng.standard_normal((need - NB,) + kc.shape[1:]).astype(np.float16)])
+        vc = np.concatenate([vc, rng.standard_normal((need - NB,) + vc.shape[1:]).astype(np.float16)])
+    tables = np.full((3, int(nbs.max())), -1, dtype=np.int32)
+    perm = rng.permutation(kc.shape[0])
+    c = 0
+    for s in range(3):
+        tables[s, :nbs[s]] = perm[c:c + nbs[s]]
+        c += nbs[s]
+    W = 7
+    ref = oracle.paged_decode_attention(q, kc, vc, tables, lens, 0.5, 4, window=W)
+    kc2, vc2 = kc.copy(), vc.copy()
+    for s in range(3):
+        for p in range(int(lens[s]) - W):
+            kc2[tables[s][p // 4], :, p % 4] = np.nan
+            vc2[tables[s][p // 4], :, p % 4] = np.nan
+    assert np.array_equal(oracle.paged_decode_attention(q, kc2, vc2, tables, lens, 0.5, 4, window=W), ref)
+
+
+def test_window_one_query_helper_matches_full():
+    rng = np.random.default_rng(25)
+    q, kc, vc, tables, lens = _tiny_paged(rng, 3, 4, 2, 8, 4, 40)
+    full = oracle.paged_decode_attention(q, kc, vc, tables, lens, 0.5, 4, window=9)
+    for s in range(3):
+        for h in range(4):
+            one = oracle.paged_decode_attention_one(q, kc, vc, tables, lens, 0.5, 4, s, h, window=9)
+            assert np.array_equal(one, full[s, h])
+
+
+def _paged_window_off_by_one(q, kc, vc, tables, lens, scale, B, window=0, **kw):
+    # planted: the window keeps one row too many
+    return oracle.paged_decode_attention(q, kc, vc, tables, lens, scale, B, window=window + 1 if window else 0)
+
+
+def test_window_pins_catch_planted_mistake():
+    assert check_window_brute_force(_paged_window_off_by_one) > 1e-3
