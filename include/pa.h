@@ -133,6 +133,39 @@ int pa_decode(void* out, pa_dtype out_dtype,
               void* stream);
 
 /*
+ * pa_decode_ex - pa_decode with options: variants of the decode step that a
+ * serving system adds on top of the plain one.
+ *
+ * Same arguments and semantics as pa_decode, plus `opt` (NULL = all options
+ * off, i.e. exactly pa_decode).  The caller sets opt->struct_size to
+ * sizeof(pa_decode_options) as it was compiled; fields beyond that size are
+ * taken as 0, so older callers keep working when fields are added.
+ *
+ *   window   > 0: sliding-window decode.  The query of sequence s, at
+ *            position seq_lens[s]-1, attends to positions
+ *            max(0, seq_lens[s]-window) .. seq_lens[s]-1 only, and only the
+ *            blocks holding them are read (the "局限性与未来工作" list of the
+ *            dihengye.cn notes names sliding-window attention as a limitation
+ *            of the paged kernel; this is its plainest reading).  0 = the
+ *            whole sequence.  Negative values are rejected (PA_ERR_SHAPE).
+ */
+typedef struct pa_decode_options {
+  size_t struct_size;
+  int32_t window;
+} pa_decode_options;
+
+int pa_decode_ex(void* out, pa_dtype out_dtype,
+                 const void* q, pa_dtype q_dtype, int64_t q_stride,
+                 const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                 const float* k_scale, const float* v_scale,
+                 const int32_t* block_tables, int max_blocks_per_seq,
+                 const int32_t* seq_lens,
+                 int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                 float scale, int block_size, int partition_size,
+                 void* workspace, size_t workspace_bytes,
+                 const pa_decode_options* opt, void* stream);
+
+/*
  * pa_decode_launch_config - the launch geometry pa_decode uses for these
  * sizes on the current device (introspection; nothing is launched).
  * Outputs (host pointers): resident CTAs over the device, warps per CTA,

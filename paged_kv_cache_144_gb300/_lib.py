@@ -23,10 +23,20 @@ SIZE_MAX = ctypes.c_size_t(-1).value
 
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 
+class DecodeOptions(ctypes.Structure):
+    """pa_decode_options (include/pa.h); struct_size is filled in by the constructor."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("window", ctypes.c_int32)]
+
+    def __init__(self, **kw):
+        super().__init__(struct_size=ctypes.sizeof(DecodeOptions), **kw)
+
+
 _SIGNATURES = {
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_decode": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
                          _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp]),
+    "pa_decode_ex": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
+                            _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, ctypes.POINTER(DecodeOptions), _vp]),
     "pa_reshape_and_cache": (_i32, [_vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32, _i64, _vp, _i32, _i32, _i32,
                                     _i32, _vp, _vp, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _i64, _sz, _vp, _i32, _vp]),
@@ -100,6 +110,10 @@ def pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block
 
 def pa_decode(*args) -> int:
     return int(load().pa_decode(*args))
+
+
+def pa_decode_ex(*args) -> int:
+    return int(load().pa_decode_ex(*args))
 
 
 def pa_decode_noalloc(*args) -> int:
@@ -191,8 +205,11 @@ def new_workspace(nbytes: int, device):
 
 
 def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale, block_size, *,
-           k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None):
-    """out[s,h] = softmax(scale * K_s q[s,h]) V_s through the block tables (pa_decode)."""
+           k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None, window=0):
+    """out[s,h] = softmax(scale * K_s q[s,h]) V_s through the block tables (pa_decode).
+
+    window > 0: sliding-window decode over the last `window` positions (pa_decode_ex).
+    """
     for n, t in (("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
                  ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale)):
         _require_cuda(n, t)
@@ -202,12 +219,18 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
     S, Hq, D = q.shape
     NB = k_cache.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = pa_decode(_ptr(out), dtype_code(out), _ptr(q), dtype_code(q), q.stride(0),
-                   _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), NB,
-                   _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
-                   S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
-                   _ptr(workspace), ws_bytes, _stream(stream))
-    _check("pa_decode", st)
+    args = (_ptr(out), dtype_code(out), _ptr(q), dtype_code(q), q.stride(0),
+            _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), NB,
+            _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+            S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
+            _ptr(workspace), ws_bytes)
+    if window:
+        opt = DecodeOptions(window=int(window))
+        st = pa_decode_ex(*args, ctypes.byref(opt), _stream(stream))
+        _check("pa_decode_ex", st)
+    else:
+        st = pa_decode(*args, _stream(stream))
+        _check("pa_decode", st)
     return out
 
 

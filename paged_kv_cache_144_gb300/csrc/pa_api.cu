@@ -225,12 +225,20 @@ PA_EXPORT int pa_decode_launch_config(int num_seqs, int num_heads, int num_kv_he
   return PA_OK;
 }
 
-PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
-                        const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
-                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                        int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
-                        int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
+                           const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                           const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
+                           void* workspace, size_t workspace_bytes, const pa_decode_options* opt, void* stream) {
+  // options: fields beyond the caller's struct_size read as 0
+  pa_decode_options o;
+  memset(&o, 0, sizeof(o));
+  if (opt) {
+    if (opt->struct_size < sizeof(size_t)) return PA_ERR_SHAPE;
+    memcpy(&o, opt, opt->struct_size < sizeof(o) ? opt->struct_size : sizeof(o));
+  }
+  if (o.window < 0) return PA_ERR_SHAPE;
   const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                     partition_size, kv_dtype);
   if (sh != PA_OK) return sh;
@@ -280,6 +288,7 @@ PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q
   p.block_size = block_size;
   p.block_shift = __builtin_ctz(static_cast<unsigned>(block_size));
   p.partition_units = plan.partition_units;
+  p.window = o.window;
   p.stages = plan.geo.stages;
   p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)
@@ -291,6 +300,17 @@ PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q
     snprintf(g_last_error + n, sizeof(g_last_error) - n, "; %s", pa::launch_failure_note());
   }
   return st;
+}
+
+PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
+                        const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return pa_decode_ex(out, out_dtype, q, q_dtype, q_stride, k_cache, v_cache, kv_dtype, num_blocks, k_scale, v_scale,
+                      block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads, num_kv_heads, head_dim, scale,
+                      block_size, partition_size, workspace, workspace_bytes, nullptr, stream);
 }
 
 PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype, int64_t k_stride,

@@ -122,7 +122,10 @@ __device__ __forceinline__ int clamped_len(const DecodeParams& p, int s, bool re
 // warp processes.  Walks either the warp's balanced unit range or its fixed
 // partitions.
 struct WorkIter {
-  int s, kvh, j, jend, j0, nu, T;
+  int s, kvh, j, jend, j0, T;
+  int nu;         // units of the segment that are attended (from unit ulo on)
+  int ulo;        // first attended unit of the sequence
+  int lo;         // first attended position (sliding window), 0 without one
   int nblk;       // blocks that hold rows of sequence s
   int frag_idx;   // ordinal of the current fragment within this warp
   int slot;       // partial-record slot, -1 when the fragment is a whole segment
@@ -144,15 +147,23 @@ __device__ __forceinline__ int find_seq(const int* prefix, int S, long long u) {
   return lo;
 }
 
-__device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p) {
+// First attended position of a sequence of length T (sliding window).
+__device__ __forceinline__ int window_lo(const DecodeParams& p, int T) {
+  return (p.window > 0 && T > p.window) ? T - p.window : 0;
+}
+
+__device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
   const int Hkv = p.num_kv_heads;
   const int s = find_seq(prefix, p.num_seqs, it.u);
   const int nu = (prefix[s + 1] - prefix[s]) / Hkv;
   const long long r = it.u - prefix[s];
   it.s = s;
   it.nu = nu;
+  it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
+  it.lo = window_lo(p, it.T);
+  it.ulo = it.lo >> ur_shift;
   it.kvh = static_cast<int>(r / nu);
-  it.j0 = static_cast<int>(r % nu);
+  it.j0 = it.ulo + static_cast<int>(r % nu);
   it.j = it.j0;
   const long long seg_start = prefix[s] + static_cast<long long>(it.kvh) * nu;
   const long long seg_end = seg_start + nu;
@@ -160,11 +171,10 @@ __device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, c
   it.jend = it.j0 + static_cast<int>(fend - it.u);
   const bool whole = (it.u == seg_start) && (fend == seg_end);
   it.slot = whole ? -1 : it.gw * 2 + (it.frag_idx == 0 ? 0 : 1);
-  it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
   it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
 }
 
-__device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, const DecodeParams& p, int UR) {
+__device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
   const int Hkv = p.num_kv_heads;
   const int s = find_seq(prefix, p.num_seqs, it.r);
   const int parts = (prefix[s + 1] - prefix[s]) / Hkv;
@@ -173,25 +183,28 @@ __device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, cons
   it.kvh = rr / parts;
   const int part = rr % parts;
   it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
-  it.nu = (it.T + UR - 1) / UR;
+  it.lo = window_lo(p, it.T);
+  it.ulo = it.lo >> ur_shift;
+  const int nu_all = (it.T + (1 << ur_shift) - 1) >> ur_shift;
+  it.nu = nu_all - it.ulo;
   it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
-  it.j0 = part * p.partition_units;
+  it.j0 = it.ulo + part * p.partition_units;
   it.j = it.j0;
-  it.jend = min(it.nu, it.j0 + p.partition_units);
+  it.jend = min(nu_all, it.j0 + p.partition_units);
   it.slot = (parts == 1) ? -1 : it.r;
 }
 
 __device__ __forceinline__ void iter_next_fragment(WorkIter& it, const int* prefix, const DecodeParams& p,
-                                                   bool fixed, int UR) {
+                                                   bool fixed, int ur_shift) {
   it.frag_idx++;
   if (fixed) {
     it.r += it.rstride;
     if (it.r >= it.R) { it.valid = false; return; }
-    frag_fixed(it, prefix, p, UR);
+    frag_fixed(it, prefix, p, ur_shift);
   } else {
     it.u += it.jend - it.j0;
     if (it.u >= it.u1) { it.valid = false; return; }
-    frag_balanced(it, prefix, p);
+    frag_balanced(it, prefix, p, ur_shift);
   }
 }
 
@@ -386,7 +399,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       if (s < S) {
         const int T = clamped_len(p, s, blockIdx.x == 0);
         lens[s] = T;
-        const int nu = (T + UR - 1) / UR;
+        const int nu = ((T + UR - 1) >> Tr::UR_SHIFT) - (window_lo(p, T) >> Tr::UR_SHIFT);
         units = (fixed ? (nu + p.partition_units - 1) / p.partition_units : nu) * Hkv;
       }
       int x = units;
@@ -445,11 +458,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       w.R = static_cast<int>(U);
       w.rstride = nw_total;
       w.r = gc;
-      if (w.r < w.R) { w.valid = true; frag_fixed(w, prefix, p, UR); }
+      if (w.r < w.R) { w.valid = true; frag_fixed(w, prefix, p, Tr::UR_SHIFT); }
     } else if (U > 0 && gc < nw_eff) {
       w.u = gc * U / nw_eff;
       w.u1 = (gc + 1) * U / nw_eff;
-      if (w.u < w.u1) { w.valid = true; frag_balanced(w, prefix, p); }
+      if (w.u < w.u1) { w.valid = true; frag_balanced(w, prefix, p, Tr::UR_SHIFT); }
     }
   };
 
@@ -468,17 +481,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     int pst = 0, pph = 1, issued = 0;
     int pf = 0, rs_use = 0, rs_pf = 0;  // units fetched ahead; ring slots to read / fill
     uint64_t wait_since = 0;
+    // boxes [first_box, nbox) of a unit hold attended rows: blocks wholly
+    // before a sliding window are neither looked up nor loaded
+    auto first_box = [&](const WorkIter& w, int bj) {
+      return unit_in_block ? 0 : max(0, (w.lo >> p.block_shift) - bj);
+    };
     auto fetch_tables = [&]() {
       const int bj = unit_in_block ? (ah.j >> upb_shift) : (ah.j << bpu_shift);
       const int nb = unit_in_block ? 1 : min(1 << bpu_shift, ah.nblk - bj);
+      const int i0 = first_box(ah, bj);
       const int32_t* src = p.block_tables + static_cast<int64_t>(ah.s) * p.max_blocks_per_seq + bj;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (i < nb) cp_async4(ring + (rs_pf * 4 + i) * 4, src + i);
+        if (i >= i0 && i < nb) cp_async4(ring + (rs_pf * 4 + i) * 4, src + i);
       cp_async_commit();
       rs_pf = (rs_pf + 1) & 3;
       ++pf;
-      if (++ah.j == ah.jend) iter_next_fragment(ah, prefix, p, fixed, UR);
+      if (++ah.j == ah.jend) iter_next_fragment(ah, prefix, p, fixed, Tr::UR_SHIFT);
     };
     while (ah.valid && pf < kTablePrefetch) fetch_tables();
     while (__any_sync(0xffffffffu, it.valid)) {
@@ -501,6 +520,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const uint32_t vdst = kdst + Tr::TILE;
           const int bj0 = unit_in_block ? (it.j >> upb_shift) : (it.j << bpu_shift);
           const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
+          const int box0 = first_box(it, bj0);
           const int row_in_block = unit_in_block ? (it.j - (bj0 << upb_shift)) * UR : 0;
           const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
           // this unit's entries were fetched pf - 1 units before the newest fetch
@@ -513,13 +533,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           }
           int phys[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) phys[i] = (i < nbox) ? static_cast<int>(lds32(ring + (rs_use * 4 + i) * 4)) : 0;
+          for (int i = 0; i < 4; ++i)
+            phys[i] = (i >= box0 && i < nbox) ? static_cast<int>(lds32(ring + (rs_use * 4 + i) * 4)) : 0;
           rs_use = (rs_use + 1) & 3;
           --pf;
-          mbar_arrive_expect_tx(bar, 2u * nbox * BOX * Tr::ROW + qbytes);
+          mbar_arrive_expect_tx(bar, 2u * (nbox - box0) * BOX * Tr::ROW + qbytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            if (i < nbox) {
+            if (i >= box0 && i < nbox) {
               int pb = phys[i];
               if (pb < 0 || pb >= p.num_blocks) {
                 raise_error(p.err, PA_DEVERR_BLOCK_ID);
@@ -541,7 +562,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             pph ^= 1;
           }
           if (ah.valid) fetch_tables();
-          if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, UR);
+          if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
           did = true;
         }
       }
@@ -615,7 +636,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
   // One unit: S^T = Q K^T, online-softmax update, O^T += V^T P^T.
   // FULL: all UR rows valid.
-  auto unit_step = [&](auto full_tag, uint32_t kt, int n_valid) {
+  auto unit_step = [&](auto full_tag, uint32_t kt, int n_valid, int lo_rel) {
     constexpr bool FULL = decltype(full_tag)::value;
     const uint32_t vt = kt + Tr::TILE;
     float sc[Tr::NT][4];
@@ -658,7 +679,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         float x = sc[nt][e] * score_scale;
         if constexpr (!FULL) {
           const int tok = nt * 8 + (kFp8 ? sigma(2 * tig + e) : 2 * tig + e);
-          x = tok < n_valid ? x : -INFINITY;
+          x = (tok < n_valid && tok >= lo_rel) ? x : -INFINITY;
         }
         sc[nt][e] = x;
         mx = fmaxf(mx, x);
@@ -693,11 +714,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       ph[nt >> 1][nt & 1] = h;
       pl[nt >> 1][nt & 1] = pack2<MB>(p0 - hf.x, p1 - hf.y);
     }
-    // rows past the end of the sequence may hold anything: zero them in V
+    // rows past the end of the sequence, and rows before a sliding window,
+    // may hold anything (or were not loaded): zero them in V
     if constexpr (!FULL) {
-      const int nz = (UR - n_valid) * Tr::NSUB * 8;
+      const int nlo = max(lo_rel, 0);
+      const int nz = (UR - n_valid + nlo) * Tr::NSUB * 8;
       for (int k = lane; k < nz; k += 32) {
-        const int r = n_valid + k / (Tr::NSUB * 8);
+        const int rr = k / (Tr::NSUB * 8);
+        const int r = rr < nlo ? rr : n_valid + (rr - nlo);
         const int ch = k % (Tr::NSUB * 8);
         sts128_zero(vt + chunk_off(r, ch));
       }
@@ -780,10 +804,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     for (;;) {
       const uint32_t stage_u32 = wbase_u32 + Tr::OFF_STAGES + cst * Tr::STAGE;
       const int n_valid = min(UR, it.T - it.j * UR);
-      if (n_valid == UR) {
-        unit_step(std::true_type{}, stage_u32, UR);
+      const int lo_rel = it.lo - it.j * UR;  // positions before the window (> 0 only in its first unit)
+      if (n_valid == UR && lo_rel <= 0) {
+        unit_step(std::true_type{}, stage_u32, UR, 0);
       } else {
-        unit_step(std::false_type{}, stage_u32, n_valid);
+        unit_step(std::false_type{}, stage_u32, n_valid, lo_rel);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(wbase_u32 + Tr::OFF_EMPTY + 8 * cst);  // the stage may be refilled
@@ -875,7 +900,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
     }
     ++it.j;
-    iter_next_fragment(it, prefix, p, fixed, UR);
+    iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
   }
 }
 
@@ -899,9 +924,13 @@ struct DecodeVariant {
   static bool geometry(int num_seqs, DecodeGeometry* g) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    int sms = 0;
+    int sms = 0, optin = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
     auto kern = paged_decode_kernel<QT, KVT, D, GM, UR>;
+    // allow every size the device allows, once: geometries of other batch
+    // sizes are cached and launched later without touching the attribute
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess) return false;
     int ns = kStageBytesPerWarp / Tr::STAGE;
     ns = ns < 2 ? 2 : (ns > Tr::MAX_NS ? Tr::MAX_NS : ns);
     const int env_ns = tuning_override("PA_DECODE_STAGES");
@@ -911,10 +940,7 @@ struct DecodeVariant {
     for (int w = 1; w <= Tr::MAX_W; ++w) {
       if (env_w > 0 && w != env_w) continue;
       const size_t smem = smem_bytes(num_seqs, w, ns);
-      if (smem > 227 * 1024) break;
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-          cudaSuccess)
-        return false;
+      if (smem > static_cast<size_t>(optin)) break;
       int occ = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (w + 1) * 32, smem) != cudaSuccess) return false;
       if (occ * w >= best_warps && occ > 0) {
@@ -925,8 +951,6 @@ struct DecodeVariant {
     }
     if (best_w == 0) return false;
     const size_t smem = smem_bytes(num_seqs, best_w, ns);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-      return false;
     g->warps_per_cta = best_w;
     g->stages = ns;
     g->ctas = sms * best_occ;

@@ -45,12 +45,42 @@ template <> constexpr int dtype_code<e4m3_t>() { return PA_FP8_E4M3; }
   (key.q_dtype == dtype_code<QT>() && key.kv_dtype == dtype_code<KVT>() && key.head_dim == D && key.gmax == GM && \
    key.unit_rows == UR)
 
-bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
+namespace {
+bool compute_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
 #define PA_GEO(QT, KVT, D, GM, UR) \
   if (PA_MATCH(QT, KVT, D, GM, UR)) return decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(num_seqs, geo);
   PA_DECODE_VARIANTS(PA_GEO)
 #undef PA_GEO
   return false;
+}
+}  // namespace
+
+// The geometry depends only on the device, the variant and the batch size
+// (the prologue's per-sequence arrays live in shared memory), so it is
+// computed once per combination: the occupancy queries cost far more host
+// time than a small decode launch.
+bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t k = (static_cast<uint64_t>(dev & 0xff) << 56) | (static_cast<uint64_t>(key.q_dtype & 0xf) << 52) |
+                     (static_cast<uint64_t>(key.kv_dtype & 0xf) << 48) |
+                     (static_cast<uint64_t>(key.head_dim & 0xfff) << 36) |
+                     (static_cast<uint64_t>(key.gmax & 0xf) << 32) | (static_cast<uint64_t>(key.unit_rows & 0xff) << 24) |
+                     static_cast<uint64_t>(num_seqs & 0xffffff);
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, DecodeGeometry> cache;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(k);
+    if (it != cache.end()) {
+      *geo = it->second;
+      return true;
+    }
+  }
+  if (!compute_geometry(key, num_seqs, geo)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache.emplace(k, *geo);
+  return true;
 }
 
 cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,

@@ -59,7 +59,8 @@ struct DecodeParams {
   float qk_scale_log2;          // softmax scale * log2(e)
   int block_size;               // tokens per cache block (a power of two >= 8)
   int block_shift;              // log2(block_size)
-  int partition_units;          // 0: balanced split; >0: fixed partitions of this many 8-row units
+  int partition_units;          // 0: balanced split; >0: fixed partitions of this many units
+  int window;                   // > 0: attend to the last `window` positions only; 0: all
   float* part_records;          // split-K partial records (workspace)
   int* seg_counters;            // [num_seqs * num_kv_heads] arrival counters (workspace)
   unsigned int* err;            // per-device error word
@@ -71,8 +72,8 @@ struct DecodeKey {
   int q_dtype;    // PA_F16 / PA_BF16
   int kv_dtype;   // PA_F16 / PA_BF16 / PA_FP8_E4M3
   int head_dim;   // 64 / 128
-  int gmax;
-  int unit_rows;  // 16 / 32 rows per work unit       // 1 / 4 / 8 (query heads per KV head, rounded up)
+  int gmax;       // 1 / 4 / 8 (query heads per KV head, rounded up)
+  int unit_rows;  // 16 / 32 / 64 rows per work unit
 };
 
 // Launch geometry of one variant on the current device.

@@ -41,7 +41,7 @@ def out_tolerance(ref: np.ndarray, out_fmt: str) -> np.ndarray:
     return PA_TOL + 0.5 * spacing
 
 
-def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda"):
+def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda", window=0):
     """Fill the cache (FP8: quantising writes), append the new token, decode.
 
     Returns (out float64 numpy, k_cache numpy, v_cache numpy, device error bits).
@@ -77,12 +77,12 @@ def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", d
                                       batch.max_blocks_per_seq, partition_size, pa.dtype_code(kc))
         ws = pa.new_workspace(n, device) if n else None
     pa.decode(out, q, kc, vc, tables, lens, batch.num_kv_heads, batch.scale, B, k_scale=ks, v_scale=vs,
-              partition_size=partition_size, workspace=ws)
+              partition_size=partition_size, workspace=ws, window=window)
     err = pa.get_device_error()
     return (out.float().cpu().numpy().astype(np.float64), to_numpy(kc, kv), to_numpy(vc, kv), err)
 
 
-def run_oracle(batch, vals):
+def run_oracle(batch, vals, window=0):
     """Oracle caches after the same writes, and the oracle attention output."""
     kv = batch.kv_fmt
     B = batch.block_size
@@ -97,7 +97,7 @@ def run_oracle(batch, vals):
                                       src_fmt=src_fmt, kv_fmt=kv, k_inv_scale=kis, v_inv_scale=vis)
     ref = oracle.paged_decode_attention(vals["q"], kc, vc, batch.block_tables, batch.seq_lens, batch.scale, B,
                                         q_fmt=batch.q_fmt, kv_fmt=kv, k_scale=vals.get("k_scale"),
-                                        v_scale=vals.get("v_scale"))
+                                        v_scale=vals.get("v_scale"), window=window)
     return ref, kc, vc
 
 

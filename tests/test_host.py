@@ -72,6 +72,31 @@ def test_decode_validation(lib):
     assert _decode(S=20000) == pa.PA_ERR_UNSUPPORTED
 
 
+def _decode_ex(opt, **kw):
+    args = dict(out=A, out_dtype=pa.PA_F32, q=A, q_dtype=pa.PA_BF16, q_stride=32 * 128, k=A, v=A2,
+                kv_dtype=pa.PA_BF16, nb=100, ks=None, vs=None, bt=A, mb=16, sl=A, S=4, Hq=32, Hkv=8, D=128,
+                scale=0.1, B=16, P=0, ws=None, wsb=0, stream=None)
+    args.update(kw)
+    a = args
+    return pa.pa_decode_ex(a["out"], a["out_dtype"], a["q"], a["q_dtype"], a["q_stride"], a["k"], a["v"],
+                           a["kv_dtype"], a["nb"], a["ks"], a["vs"], a["bt"], a["mb"], a["sl"], a["S"], a["Hq"],
+                           a["Hkv"], a["D"], a["scale"], a["B"], a["P"], a["ws"], a["wsb"],
+                           None if opt is None else ctypes.byref(opt), a["stream"])
+
+
+def test_decode_ex_options_validation(lib):
+    assert _decode_ex(None, S=0) == pa.PA_OK
+    assert _decode_ex(pa.DecodeOptions(window=5), S=0) == pa.PA_OK
+    assert _decode_ex(pa.DecodeOptions(window=-1)) == pa.PA_ERR_SHAPE
+    bad = pa.DecodeOptions(window=5)
+    bad.struct_size = 0
+    assert _decode_ex(bad) == pa.PA_ERR_SHAPE
+    # option checks come before the shape checks that pa_decode shares
+    assert _decode_ex(pa.DecodeOptions(window=3), Hq=30) == pa.PA_ERR_SHAPE
+    assert _decode_ex(pa.DecodeOptions(window=3), B=12) == pa.PA_ERR_UNSUPPORTED
+    assert ctypes.sizeof(pa.DecodeOptions) >= 12
+
+
 def _rc(**kw):
     a = dict(k=A, v=A2, src=pa.PA_F16, ks=8 * 128, vs=8 * 128, kc=A, vc=A2, kv=pa.PA_F16, nb=10, sm=A, N=3,
              Hkv=8, D=128, B=16, ki=None, vi=None, stream=None)
