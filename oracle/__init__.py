@@ -23,6 +23,8 @@ from .codecs import (
     f16_to_f64,
     e4m3_decode,
     e4m3_encode_f32,
+    int8_decode,
+    int8_encode_f32,
     E4M3_MAX,
 )
 from .attention import (

@@ -25,6 +25,9 @@ Readings where the pages are silent (each also listed in the design doc):
   * scale: the float32 value passed to the kernel, widened to float64.
   * FP8 KV ([P2] §"KV量子化"): value = float64(e4m3 code) * float64(scale[h])
     with one float32 scale per KV head, separately for K and V.
+  * INT8 KV (same section: "scale / zero point"): value = (code - zp[h]) *
+    float64(scale[h]), one float32 scale and one integer zero point per KV
+    head, separately for K and V (codec in ``codecs``).
   * a sequence of length 0 attends to nothing; its output is defined as 0.
   * sliding window (named as a limitation of the paged kernel in the
     "局限性与未来工作" list of the dihengye.cn notes, no definition given):
@@ -42,11 +45,18 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codecs import storage_to_f64
+from .codecs import int8_decode, storage_to_f64
 
 
-def dequantize_kv(cache: np.ndarray, fmt: str, scale: np.ndarray | None = None) -> np.ndarray:
-    """Storage cache [NB, H_kv, B, d] -> float64, applying per-KV-head scale for e4m3."""
+def dequantize_kv(cache: np.ndarray, fmt: str, scale: np.ndarray | None = None,
+                  zero_point: np.ndarray | None = None) -> np.ndarray:
+    """Storage cache [NB, H_kv, B, d] -> float64, applying per-KV-head scale (and zero point for i8)."""
+    if fmt == "i8":
+        if scale is None or zero_point is None:
+            raise ValueError("i8 cache needs a per-KV-head scale and zero point")
+        zp = np.asarray(zero_point, dtype=np.int64)[None, :, None, None]
+        sc = np.asarray(scale, dtype=np.float32).astype(np.float64)[None, :, None, None]
+        return int8_decode(cache, zp) * sc
     out = storage_to_f64(cache, fmt)
     if fmt == "e4m3":
         if scale is None:
@@ -91,7 +101,8 @@ def window_start(seq_len: int, window: int) -> int:
 
 def paged_decode_attention_one(q, k_cache, v_cache, block_tables, seq_lens, scale,
                                block_size, s, h, *, q_fmt="f16", kv_fmt="f16",
-                               k_scale=None, v_scale=None, num_kv_heads=None, window=0):
+                               k_scale=None, v_scale=None, num_kv_heads=None, window=0,
+                               k_zero_point=None, v_zero_point=None):
     """Output vector out[s, h, :] only (for sampled checks on large inputs).
 
     ``k_cache``/``v_cache`` may be the full pool or any array indexable by the
@@ -108,23 +119,26 @@ def paged_decode_attention_one(q, k_cache, v_cache, block_tables, seq_lens, scal
     vb = v_cache[phys, kvh]
     ks = None if k_scale is None else np.asarray(k_scale)[kvh:kvh + 1]
     vs = None if v_scale is None else np.asarray(v_scale)[kvh:kvh + 1]
+    kz = None if k_zero_point is None else np.asarray(k_zero_point)[kvh:kvh + 1]
+    vz = None if v_zero_point is None else np.asarray(v_zero_point)[kvh:kvh + 1]
     lo = window_start(T, window)
-    Kf = dequantize_kv(kb[:, None], kv_fmt, ks)[:, 0].reshape(-1, kb.shape[-1])[lo:T]
-    Vf = dequantize_kv(vb[:, None], kv_fmt, vs)[:, 0].reshape(-1, vb.shape[-1])[lo:T]
+    Kf = dequantize_kv(kb[:, None], kv_fmt, ks, kz)[:, 0].reshape(-1, kb.shape[-1])[lo:T]
+    Vf = dequantize_kv(vb[:, None], kv_fmt, vs, vz)[:, 0].reshape(-1, vb.shape[-1])[lo:T]
     qv = storage_to_f64(q[s, h], q_fmt)
     return dense_decode_attention(qv, Kf, Vf, _scale64(scale))
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size,
-                           *, q_fmt="f16", kv_fmt="f16", k_scale=None, v_scale=None, window=0):
+                           *, q_fmt="f16", kv_fmt="f16", k_scale=None, v_scale=None, window=0,
+                           k_zero_point=None, v_zero_point=None):
     """out[S, H_q, d] float64 for every sequence and query head (window: see module notes)."""
     S, Hq, d = q.shape
     Hkv = k_cache.shape[1]
     if Hq % Hkv != 0:
         raise ValueError("H_q must be a multiple of H_kv")
     G = Hq // Hkv
-    Kc = dequantize_kv(k_cache, kv_fmt, k_scale)
-    Vc = dequantize_kv(v_cache, kv_fmt, v_scale)
+    Kc = dequantize_kv(k_cache, kv_fmt, k_scale, k_zero_point)
+    Vc = dequantize_kv(v_cache, kv_fmt, v_scale, v_zero_point)
     qf = storage_to_f64(q, q_fmt)
     sc = _scale64(scale)
     out = np.zeros((S, Hq, d), dtype=np.float64)

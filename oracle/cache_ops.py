@@ -13,6 +13,8 @@ reshape_and_cache
     16-bit caches receive the source bits unchanged.  FP8-e4m3 caches receive
     e4m3_rne_satfinite(float32(x) * inv_scale[h]), the product rounded in
     IEEE float32 ([P2] §"KV量子化" for FP8 storage; codec in ``codecs``).
+    INT8 caches receive clamp(rne(float32(x) * inv_scale[h]) + zero_point[h],
+    -128, 127) (same section, "scale / zero point"; codec in ``codecs``).
 
 copy_blocks
     [P1] §"Copy-on-Write（CoW）によるメモリ共有": when a sequence must write into a
@@ -30,11 +32,12 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codecs import e4m3_encode_f32, storage_to_f32
+from .codecs import e4m3_encode_f32, int8_encode_f32, storage_to_f32
 
 
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *,
-                      src_fmt="f16", kv_fmt="f16", k_inv_scale=None, v_inv_scale=None):
+                      src_fmt="f16", kv_fmt="f16", k_inv_scale=None, v_inv_scale=None,
+                      k_zero_point=None, v_zero_point=None):
     """Return new (k_cache, v_cache) with tokens' rows written to their slots.
 
     k, v: [N, H_kv, d] in the source storage format (float16 or bf16 bits).
@@ -49,13 +52,16 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *,
         if slot < 0:
             continue
         blk, off = slot // block_size, slot % block_size
-        for src, dst, inv in ((k, k_out, k_inv_scale), (v, v_out, v_inv_scale)):
+        for src, dst, inv, zp in ((k, k_out, k_inv_scale, k_zero_point), (v, v_out, v_inv_scale, v_zero_point)):
             row = np.asarray(src[n])
-            if kv_fmt == "e4m3":
+            if kv_fmt in ("e4m3", "i8"):
                 x = storage_to_f32(row, src_fmt)                 # [H_kv, d] float32
                 inv32 = np.asarray(inv, dtype=np.float32)[:Hkv, None]
                 prod = (x * inv32).astype(np.float32)            # IEEE float32 product
-                dst[blk, :, off, :] = e4m3_encode_f32(prod)
+                if kv_fmt == "e4m3":
+                    dst[blk, :, off, :] = e4m3_encode_f32(prod)
+                else:
+                    dst[blk, :, off, :] = int8_encode_f32(prod, np.asarray(zp, dtype=np.int64)[:Hkv, None])
             else:
                 if kv_fmt != src_fmt:
                     raise ValueError("16-bit caches take source bits unchanged")

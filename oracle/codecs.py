@@ -15,9 +15,20 @@ definition alone: the finite non-negative E4M3 values are enumerated, the
 nearest one is chosen, ties go to the code whose mantissa LSB is 0, and any
 magnitude at or above 448 (including +-inf) saturates to 448.
 
+INT8 with a scale and a zero point (the same section lists INT8 KV at one
+byte per element that "needs a scale / zero point", without a formula): the
+plainest affine reading is value = (code - zero_point) * scale with a signed
+8-bit code in [-128, 127] and an integer zero point, one (scale, zero_point)
+pair per KV head for K and one for V.  Quantisation of a float32 product
+y = x * inv_scale (formed in float32 by the caller): code = clamp(rne(y) +
+zero_point, -128, 127), where rne rounds to the nearest integer with ties to
+even; +-inf saturate, and NaN is taken to saturate to +127.
+
 Pins: ``tests/test_oracle_pins.py::test_e4m3_*`` (known OCP values, all 256
-codes against torch.float8_e4m3fn, round trips, tie midpoints, saturation)
-and ``test_bf16_*`` (against torch.bfloat16).
+codes against torch.float8_e4m3fn, round trips, tie midpoints, saturation),
+``test_bf16_*`` (against torch.bfloat16) and ``test_int8_*`` (round trips of
+all codes for several zero points, ties to even, saturation, torch's
+quantize_per_tensor with scale 1).
 """
 
 from __future__ import annotations
@@ -85,6 +96,23 @@ def e4m3_encode_f32(x: np.ndarray) -> np.ndarray:
     return code
 
 
+def int8_decode(codes: np.ndarray, zero_point) -> np.ndarray:
+    """int8 codes -> float64 (code - zero_point), exact; zero_point broadcasts."""
+    c = np.asarray(codes, dtype=np.int8).astype(np.float64)
+    return c - np.asarray(zero_point, dtype=np.int64).astype(np.float64)
+
+
+def int8_encode_f32(y: np.ndarray, zero_point) -> np.ndarray:
+    """float32 values (already x * inv_scale) -> int8 codes: clamp(rne(y) + zp, -128, 127)."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    zp = np.asarray(zero_point, dtype=np.int64).astype(np.float64)
+    nan = np.isnan(y)
+    r = np.rint(np.where(nan, 0.0, y)) + zp        # numpy rint: nearest, ties to even
+    r = np.clip(r, -128.0, 127.0)
+    r = np.where(nan, 127.0, r)
+    return r.astype(np.int8)
+
+
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """bfloat16 bit patterns (uint16/int16) -> float64 (exact).
 
@@ -107,6 +135,8 @@ def storage_to_f64(x: np.ndarray, fmt: str) -> np.ndarray:
         return bf16_bits_to_f64(x)
     if fmt == "e4m3":
         return e4m3_decode(x)
+    if fmt == "i8":
+        return np.asarray(x, dtype=np.int8).astype(np.float64)   # raw codes (no zero point)
     if fmt == "f32":
         return np.asarray(x, dtype=np.float32).astype(np.float64)
     raise ValueError(f"unknown storage format {fmt!r}")

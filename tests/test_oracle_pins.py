@@ -632,3 +632,89 @@ def _paged_window_off_by_one(q, kc, vc, tables, lens, scale, B, window=0, **kw):
 
 def test_window_pins_catch_planted_mistake():
     assert check_window_brute_force(_paged_window_off_by_one) > 1e-3
+
+
+# ----------------------------------------------------------------------------- INT8 KV (scale + zero point)
+
+def test_int8_known_values():
+    enc = oracle.int8_encode_f32
+    assert enc(np.array([2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5], np.float32), 0).tolist() == [2, 4, -2, -4, 0, 0, 2]
+    assert enc(np.array([1000.0, -1000.0, np.inf, -np.inf, np.nan], np.float32), 0).tolist() == \
+        [127, -128, 127, -128, 127]
+    assert enc(np.array([120.0, -140.0, 117.0, -138.0], np.float32), 10).tolist() == [127, -128, 127, -128]
+    assert enc(np.array([0.0, 1.0, -1.0], np.float32), -7).tolist() == [-7, -6, -8]
+
+
+def test_int8_roundtrip_all_codes():
+    codes = np.arange(-128, 128).astype(np.int8)
+    for zp in (-128, -37, 0, 5, 127):
+        vals = oracle.int8_decode(codes, zp)
+        assert np.array_equal(vals, codes.astype(np.float64) - zp)
+        assert np.array_equal(oracle.int8_encode_f32(vals.astype(np.float32), zp), codes)
+
+
+def check_int8_vs_torch(encode, n=50000, seed=31):
+    """torch.quantize_per_tensor with scale 1: clamp(nearbyint(x) + zp)."""
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal(n) * 60).astype(np.float32)
+    x[: n // 10] = np.round(x[: n // 10]) + 0.5          # exact ties
+    bad = 0
+    for zp in (-20, 0, 33):
+        ref = torch.quantize_per_tensor(torch.from_numpy(x), 1.0, zp, torch.qint8).int_repr().numpy()
+        bad += int(np.sum(encode(x, zp) != ref))
+    return bad
+
+
+def test_int8_encode_vs_torch():
+    assert check_int8_vs_torch(oracle.int8_encode_f32) == 0
+
+
+def test_int8_dequant_applies_per_head_scale_and_zero_point():
+    codes = np.full((2, 3, 4, 2), 10, dtype=np.int8)
+    scale = np.array([0.5, 2.0, 0.125], dtype=np.float32)
+    zp = np.array([0, 12, -6], dtype=np.int32)
+    deq = oracle.dequantize_kv(codes, "i8", scale, zp)
+    for h, want in enumerate([5.0, -4.0, 2.0]):
+        assert np.all(deq[:, h] == want)
+
+
+def test_reshape_and_cache_int8_quantises_product():
+    rng = np.random.default_rng(16)
+    B, NB, H, d = 4, 3, 2, 8
+    src = rng.standard_normal((3, H, d)).astype(np.float16)
+    inv = np.array([31.0, 7.5], dtype=np.float32)
+    zp = np.array([-3, 9], dtype=np.int32)
+    kc = np.zeros((NB, H, B, d), dtype=np.int8)
+    k2, _ = oracle.reshape_and_cache(src, src, kc, kc, [1, 5, 10], B, src_fmt="f16", kv_fmt="i8",
+                                     k_inv_scale=inv, v_inv_scale=inv, k_zero_point=zp, v_zero_point=zp)
+    for n, sl in enumerate([1, 5, 10]):
+        for h in range(H):
+            y = torch.from_numpy(src[n, h].astype(np.float32)) * float(inv[h])      # float32 product
+            ref = torch.quantize_per_tensor(y, 1.0, int(zp[h]), torch.qint8).int_repr().numpy()
+            assert np.array_equal(k2[sl // B, h, sl % B], ref)
+
+
+def _int8_ties_away(y, zp):
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    r = np.sign(y) * np.floor(np.abs(y) + 0.5) + np.asarray(zp, dtype=np.float64)
+    return np.clip(r, -128, 127).astype(np.int8)
+
+
+def test_int8_pins_catch_planted_mistake():
+    assert check_int8_vs_torch(_int8_ties_away) > 0
+
+
+def test_int8_attention_equals_float_cache_of_same_values():
+    """An i8 cache (scale s, zero point z) attends exactly like an f16 cache holding (code - z) * s."""
+    rng = np.random.default_rng(32)
+    q, kc16, vc16, tables, lens = _tiny_paged(rng, 3, 4, 2, 8, 4, 30)
+    kcode = rng.integers(-128, 128, size=kc16.shape).astype(np.int8)
+    vcode = rng.integers(-128, 128, size=vc16.shape).astype(np.int8)
+    ks, vs = np.array([0.25, 0.5], np.float32), np.array([0.125, 1.0], np.float32)
+    kz, vz = np.array([3, -5], np.int32), np.array([0, 7], np.int32)
+    kf = ((kcode.astype(np.float64) - kz[None, :, None, None]) * ks[None, :, None, None]).astype(np.float16)
+    vf = ((vcode.astype(np.float64) - vz[None, :, None, None]) * vs[None, :, None, None]).astype(np.float16)
+    a = oracle.paged_decode_attention(q, kcode, vcode, tables, lens, 0.5, 4, kv_fmt="i8", k_scale=ks,
+                                      v_scale=vs, k_zero_point=kz, v_zero_point=vz)
+    b = oracle.paged_decode_attention(q, kf, vf, tables, lens, 0.5, 4)
+    assert np.array_equal(a, b)
