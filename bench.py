@@ -40,15 +40,18 @@ import workloads  # noqa: E402
 
 METRIC = "paged-decode KV-read HBM GB/s & % of GB300 peak; decode attn tokens/s"
 UNIT = "GB/s"
-FMT_BYTES = {"f16": 2, "bf16": 2, "e4m3": 1, "f32": 4}
+FMT_BYTES = {"f16": 2, "bf16": 2, "e4m3": 1, "i8": 1, "f32": 4}
 KERNEL_SOURCES = ["pa_common.cuh", "pa_decode.cuh", "pa_decode_variants.h", "pa_decode_dispatch.cu",
-                  "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_fp8.cu", "pa_api.cu", "pa_kernels.h"]
+                  "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_fp8.cu", "pa_decode_int8.cu", "pa_api.cu",
+                  "pa_kernels.h"]
 WORKLOAD_TEXT = {
     "tiny": "4 seqs, cached len ~U{1..128} + 1, 4 heads MHA, d 64, B 16, fp16",
     "gqa_32x4k": "32 seqs, len ~U{1..4096}, 32 q heads / 8 KV heads, d 128, B 16, bf16",
     "long_32k": "8 seqs x 32768 tokens, 64 q heads / 8 KV heads, d 128, B 16, bf16",
     "fp8_mix": "256 seqs, len=clip(round(lognormal(7,1)),16,8192), 32 q / 8 KV heads, d 128, B 16, "
                "K/V fp8-e4m3 per-head scales, bf16 q",
+    "int8_mix": "256 seqs, len=clip(round(lognormal(7,1)),16,8192), 32 q / 8 KV heads, d 128, B 16, "
+                "K/V INT8 per-head scale + zero point, bf16 q",
     "beam_cow": "6 beams sharing a 1000-token prompt (63 blocks, refcount 6, partial block copied on write), "
                 "private tails ~U{1..256}, 40 heads MHA, d 128, B 16, fp16",
 }
@@ -62,15 +65,21 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def algorithmic_bytes(batch) -> dict:
-    """Bytes a step must move at minimum (valid tokens only; tails, workspace and scales excluded)."""
+def algorithmic_bytes(batch, window: int = 0) -> dict:
+    """Bytes a step must move at minimum (attended tokens only; tails, workspace and scales excluded).
+
+    With a sliding window only the last `window` positions of each sequence and the
+    block-table entries of the blocks holding them count.
+    """
     S, Hq, Hkv, D, B = batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
     b_kv = FMT_BYTES[batch.kv_fmt]
     b_q = FMT_BYTES[batch.q_fmt]
     T = batch.seq_lens.astype(np.int64)
-    kv = int(T.sum()) * Hkv * D * b_kv * 2
-    decode = kv + S * Hq * D * b_q + S * Hq * D * b_q + int(((T + B - 1) // B).sum()) * 4 + 4 * S
-    src_b = b_q if batch.kv_fmt == "e4m3" else b_kv
+    lo = np.maximum(T - window, 0) if window > 0 else np.zeros_like(T)
+    kv = int((T - lo).sum()) * Hkv * D * b_kv * 2
+    blocks = int(((T + B - 1) // B - lo // B).sum())
+    decode = kv + S * Hq * D * b_q + S * Hq * D * b_q + blocks * 4 + 4 * S
+    src_b = b_q if batch.kv_fmt in ("e4m3", "i8") else b_kv
     append = S * Hkv * D * (src_b + b_kv) * 2 + 8 * S
     return {"kv": kv, "decode": decode, "append": append, "step": decode + append}
 
@@ -158,11 +167,12 @@ def _oracle_segment(args):
     """Worker: oracle attention for one (sequence, KV head) segment; returns seconds."""
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     import oracle
-    q, kc, vc, T, scale, B, q_fmt, kv_fmt, ks, vs = args
+    q, kc, vc, T, scale, B, q_fmt, kv_fmt, ks, vs, kz, vz = args
     nb = kc.shape[0]
     t0 = time.perf_counter()
     oracle.paged_decode_attention(q, kc, vc, np.arange(nb, dtype=np.int32)[None, :], np.array([T]), scale, B,
-                                  q_fmt=q_fmt, kv_fmt=kv_fmt, k_scale=ks, v_scale=vs)
+                                  q_fmt=q_fmt, kv_fmt=kv_fmt, k_scale=ks, v_scale=vs, k_zero_point=kz,
+                                  v_zero_point=vz)
     return time.perf_counter() - t0
 
 
@@ -185,11 +195,14 @@ def host_segments(batch, dev_vals, seg_ids):
         kc = host(dev_vals["k_cache"].index_select(0, blocks)[:, kvh:kvh + 1], batch.kv_fmt)
         vc = host(dev_vals["v_cache"].index_select(0, blocks)[:, kvh:kvh + 1], batch.kv_fmt)
         q = host(q_all[s:s + 1, kvh * G:(kvh + 1) * G], batch.q_fmt)
-        ks = vs = None
-        if batch.kv_fmt == "e4m3":
+        ks = vs = kz = vz = None
+        if batch.kv_fmt in ("e4m3", "i8"):
             ks = dev_vals["k_scale"][kvh:kvh + 1].cpu().numpy()
             vs = dev_vals["v_scale"][kvh:kvh + 1].cpu().numpy()
-        out.append((q, kc, vc, T, batch.scale, B, batch.q_fmt, batch.kv_fmt, ks, vs))
+        if batch.kv_fmt == "i8":
+            kz = dev_vals["k_zero_point"][kvh:kvh + 1].cpu().numpy()
+            vz = dev_vals["v_zero_point"][kvh:kvh + 1].cpu().numpy()
+        out.append((q, kc, vc, T, batch.scale, B, batch.q_fmt, batch.kv_fmt, ks, vs, kz, vz))
     return out
 
 
@@ -298,10 +311,11 @@ def run_ours(args):
     batch = workloads.make_batch(args.workload, seed=args.seed + 1000 * rank)
     vals = workloads.device_values(batch, args.seed + 1000 * rank, dev)
     B, Hkv, D, S, Hq = batch.block_size, batch.num_kv_heads, batch.head_dim, batch.num_seqs, batch.num_heads
-    fp8 = batch.kv_fmt == "e4m3"
-    if fp8:
+    kz, vz = vals.get("k_zero_point"), vals.get("v_zero_point")
+    if batch.kv_fmt in ("e4m3", "i8"):
         pa.reshape_and_cache(vals["k_src"], vals["v_src"], vals["k_cache"], vals["v_cache"], vals["src_slots"], B,
-                             k_inv_scale=vals["k_inv_scale"], v_inv_scale=vals["v_inv_scale"])
+                             k_inv_scale=vals["k_inv_scale"], v_inv_scale=vals["v_inv_scale"], k_zero_point=kz,
+                             v_zero_point=vz)
         del vals["k_src"], vals["v_src"]
     pool_bytes = 2 * vals["k_cache"].numel() * vals["k_cache"].element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -325,12 +339,14 @@ def run_ours(args):
 
     def step(i, ev=None):
         kc, vc = caches[i % replicas]
-        pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, stream=stream)
+        pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
+                             v_zero_point=vz, stream=stream)
         pa.copy_blocks(kc, vc, no_pairs, stream=stream)          # no shared block is written: no launch
         if ev is not None:
             ev[0].record(stream)
         pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                  partition_size=args.partition_size, workspace=ws, stream=stream)
+                  partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
+                  k_zero_point=kz, v_zero_point=vz)
         if ev is not None:
             ev[1].record(stream)
 
@@ -381,9 +397,11 @@ def run_ours(args):
             for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_tables, h_tables),
                          (d_lens, h_lens)):
                 d.copy_(h, non_blocking=True)
-            pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis, stream=stream)
+            pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
+                                 v_zero_point=vz, stream=stream)
             pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                      partition_size=args.partition_size, workspace=ws, stream=stream)
+                      partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
+                      k_zero_point=kz, v_zero_point=vz)
             h_out.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -398,7 +416,7 @@ def run_ours(args):
         e2e_s = max_over_ranks(e2e_s, world)
         e2e = (e2e_s, h2d, d2h)
 
-    ab = algorithmic_bytes(batch)
+    ab = algorithmic_bytes(batch, args.window)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     total_step_bytes = sum_over_ranks(float(ab["step"]), world)
     total_kv = sum_over_ranks(float(ab["kv"]), world)
@@ -424,6 +442,7 @@ def run_ours(args):
             "num_seqs": S, "num_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": B,
             "context_tokens": int(batch.seq_lens.sum()), "kv_dtype": batch.kv_fmt, "q_dtype": batch.q_fmt,
             "split": "balanced" if args.partition_size == 0 else f"fixed {args.partition_size} tokens",
+            "window": args.window or None,
             "step": "reshape_and_cache(1 new token/seq) + pa_decode",
             "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
             "seed": args.seed,
@@ -609,6 +628,10 @@ def run_reference(args):
             kc = vrng.integers(0, 0x7E, size=(nb, 1, B, D)).astype(np.uint8)
             vc = vrng.integers(0, 0x7E, size=(nb, 1, B, D)).astype(np.uint8)
             sc = np.array([0.01], dtype=np.float32)
+        elif batch.kv_fmt == "i8":
+            kc = vrng.integers(-128, 128, size=(nb, 1, B, D)).astype(np.int8)
+            vc = vrng.integers(-128, 128, size=(nb, 1, B, D)).astype(np.int8)
+            sc = np.array([0.01], dtype=np.float32)
         else:
             kc = workloads.configs._normal_storage(vrng, (nb, 1, B, D), batch.kv_fmt)
             vc = workloads.configs._normal_storage(vrng, (nb, 1, B, D), batch.kv_fmt)
@@ -618,8 +641,9 @@ def run_reference(args):
 
     q, kc, vc, tb, ln, sc = make(min(T_full, 256))
     t0 = time.perf_counter()
+    zp = np.zeros(1, dtype=np.int32) if batch.kv_fmt == "i8" else None
     oracle.paged_decode_attention(q, kc, vc, tb, ln, batch.scale, B, q_fmt=batch.q_fmt, kv_fmt=batch.kv_fmt,
-                                  k_scale=sc, v_scale=sc)
+                                  k_scale=sc, v_scale=sc, k_zero_point=zp, v_zero_point=zp)
     per_tok = (time.perf_counter() - t0) / int(ln[0])
     T = int(max(1, min(T_full, per_step_budget / max(per_tok, 1e-9))))
     q, kc, vc, tb, ln, sc = make(T)
@@ -628,7 +652,7 @@ def run_reference(args):
 
     def one():
         oracle.paged_decode_attention(q, kc, vc, tb, ln, batch.scale, B, q_fmt=batch.q_fmt, kv_fmt=batch.kv_fmt,
-                                      k_scale=sc, v_scale=sc)
+                                      k_scale=sc, v_scale=sc, k_zero_point=zp, v_zero_point=zp)
 
     for _ in range(args.warmup):
         one()
@@ -654,7 +678,10 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_32x4k", choices=["tiny", "gqa_32x4k", "long_32k", "fp8_mix", "beam_cow"])
+    ap.add_argument("--workload", default="gqa_32x4k",
+                    choices=["tiny", "gqa_32x4k", "long_32k", "fp8_mix", "int8_mix", "beam_cow"])
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window decode over the last W positions (bytes counted over the window)")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--replicas", type=int, default=0, help="KV pool replicas to rotate (0 = enough for > 4x L2)")
     ap.add_argument("--seed", type=int, default=0)

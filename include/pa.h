@@ -50,7 +50,9 @@ typedef enum {
   PA_F32 = 0,
   PA_F16 = 1,
   PA_BF16 = 2,
-  PA_FP8_E4M3 = 3 /* OCP E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa; max 448 */
+  PA_FP8_E4M3 = 3, /* OCP E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa; max 448 */
+  PA_INT8 = 4      /* signed 8-bit code with a per-KV-head scale and zero point:
+                      value = (code - zero_point) * scale */
 } pa_dtype;
 
 typedef enum {
@@ -148,10 +150,17 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            dihengye.cn notes names sliding-window attention as a limitation
  *            of the paged kernel; this is its plainest reading).  0 = the
  *            whole sequence.  Negative values are rejected (PA_ERR_SHAPE).
+ *   k_zero_point / v_zero_point
+ *            int32 [num_kv_heads] device arrays, values in [-128, 127];
+ *            required for kv_dtype PA_INT8 (k_scale / v_scale are then the
+ *            INT8 scales), ignored otherwise ([P2] "KV量子化: FP8とINT8":
+ *            INT8 KV needs a scale and a zero point).
  */
 typedef struct pa_decode_options {
   size_t struct_size;
   int32_t window;
+  const int32_t* k_zero_point;
+  const int32_t* v_zero_point;
 } pa_decode_options;
 
 int pa_decode_ex(void* out, pa_dtype out_dtype,
@@ -203,6 +212,32 @@ int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype,
                          int num_kv_heads, int head_dim, int block_size,
                          const float* k_inv_scale, const float* v_inv_scale,
                          void* stream);
+
+/*
+ * pa_reshape_and_cache_ex - pa_reshape_and_cache with options (NULL = none).
+ * opt->struct_size = sizeof(pa_cache_write_options) as compiled by the
+ * caller; later fields read as 0.
+ *
+ *   k_zero_point / v_zero_point  int32 [num_kv_heads] device arrays in
+ *            [-128, 127]; required for kv_dtype PA_INT8 ([P2] "KV量子化"),
+ *            whose rows receive clamp(rne(float32(x) * inv_scale[h]) +
+ *            zero_point[h], -128, 127): the product rounded in float32, then
+ *            to the nearest integer with ties to even; +-inf saturate and NaN
+ *            becomes +127.
+ */
+typedef struct pa_cache_write_options {
+  size_t struct_size;
+  const int32_t* k_zero_point;
+  const int32_t* v_zero_point;
+} pa_cache_write_options;
+
+int pa_reshape_and_cache_ex(const void* k, const void* v, pa_dtype src_dtype,
+                            int64_t k_stride, int64_t v_stride,
+                            void* k_cache, void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                            const int64_t* slot_mapping, int num_tokens,
+                            int num_kv_heads, int head_dim, int block_size,
+                            const float* k_inv_scale, const float* v_inv_scale,
+                            const pa_cache_write_options* opt, void* stream);
 
 /*
  * pa_copy_blocks - the device half of copy-on-write.

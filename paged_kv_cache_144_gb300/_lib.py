@@ -14,7 +14,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libpagedattn.so")
 HEADER = os.path.join(os.path.dirname(PKG_DIR), "include", "pa.h")
 
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_INT8 = 0, 1, 2, 3, 4
 PA_OK = 0
 PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_DTYPE, PA_ERR_UNSUPPORTED = -1, -2, -3, -4
 PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_ALIGN = -5, -6, -7
@@ -25,10 +25,20 @@ _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctyp
 
 class DecodeOptions(ctypes.Structure):
     """pa_decode_options (include/pa.h); struct_size is filled in by the constructor."""
-    _fields_ = [("struct_size", ctypes.c_size_t), ("window", ctypes.c_int32)]
+    _fields_ = [("struct_size", ctypes.c_size_t), ("window", ctypes.c_int32),
+                ("k_zero_point", ctypes.c_void_p), ("v_zero_point", ctypes.c_void_p)]
 
     def __init__(self, **kw):
         super().__init__(struct_size=ctypes.sizeof(DecodeOptions), **kw)
+
+
+class CacheWriteOptions(ctypes.Structure):
+    """pa_cache_write_options (include/pa.h)."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("k_zero_point", ctypes.c_void_p),
+                ("v_zero_point", ctypes.c_void_p)]
+
+    def __init__(self, **kw):
+        super().__init__(struct_size=ctypes.sizeof(CacheWriteOptions), **kw)
 
 
 _SIGNATURES = {
@@ -39,6 +49,8 @@ _SIGNATURES = {
                             _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, ctypes.POINTER(DecodeOptions), _vp]),
     "pa_reshape_and_cache": (_i32, [_vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32, _i64, _vp, _i32, _i32, _i32,
                                     _i32, _vp, _vp, _vp]),
+    "pa_reshape_and_cache_ex": (_i32, [_vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32, _i64, _vp, _i32, _i32, _i32,
+                                       _i32, _vp, _vp, ctypes.POINTER(CacheWriteOptions), _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _i64, _sz, _vp, _i32, _vp]),
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_get_device_error": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint)]),
@@ -128,6 +140,10 @@ def pa_reshape_and_cache(*args) -> int:
     return int(load().pa_reshape_and_cache(*args))
 
 
+def pa_reshape_and_cache_ex(*args) -> int:
+    return int(load().pa_reshape_and_cache_ex(*args))
+
+
 def pa_copy_blocks(*args) -> int:
     return int(load().pa_copy_blocks(*args))
 
@@ -160,7 +176,8 @@ def _torch():
 
 def dtype_code(t) -> int:
     torch = _torch()
-    m = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3}
+    m = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3,
+         torch.int8: PA_INT8}
     f8 = getattr(torch, "float8_e4m3fn", None)
     if f8 is not None:
         m[f8] = PA_FP8_E4M3
@@ -205,13 +222,16 @@ def new_workspace(nbytes: int, device):
 
 
 def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale, block_size, *,
-           k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None, window=0):
+           k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None, window=0,
+           k_zero_point=None, v_zero_point=None):
     """out[s,h] = softmax(scale * K_s q[s,h]) V_s through the block tables (pa_decode).
 
     window > 0: sliding-window decode over the last `window` positions (pa_decode_ex).
+    INT8 caches (torch.int8) take k/v scales and int32 per-KV-head zero points (pa_decode_ex).
     """
     for n, t in (("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
-                 ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale)):
+                 ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale), ("k_zero_point", k_zero_point),
+                 ("v_zero_point", v_zero_point)):
         _require_cuda(n, t)
     _require_cuda("q", q, contiguous=False)
     if q.stride(2) != 1 or q.stride(1) != q.shape[2]:
@@ -224,8 +244,8 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
             _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
             S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
             _ptr(workspace), ws_bytes)
-    if window:
-        opt = DecodeOptions(window=int(window))
+    if window or k_zero_point is not None or v_zero_point is not None:
+        opt = DecodeOptions(window=int(window), k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point))
         st = pa_decode_ex(*args, ctypes.byref(opt), _stream(stream))
         _check("pa_decode_ex", st)
     else:
@@ -254,10 +274,14 @@ def decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_head
 
 
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *, k_inv_scale=None, v_inv_scale=None,
-                      stream=None):
-    """Write rows k[n], v[n] ([N, H_kv, d]) to cache slots slot_mapping[n] (pa_reshape_and_cache)."""
+                      k_zero_point=None, v_zero_point=None, stream=None):
+    """Write rows k[n], v[n] ([N, H_kv, d]) to cache slots slot_mapping[n] (pa_reshape_and_cache).
+
+    INT8 caches (torch.int8) also take int32 per-KV-head zero points (pa_reshape_and_cache_ex).
+    """
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("slot_mapping", slot_mapping),
-                 ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale)):
+                 ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale), ("k_zero_point", k_zero_point),
+                 ("v_zero_point", v_zero_point)):
         _require_cuda(n, t)
     _require_cuda("k", k, contiguous=False)
     _require_cuda("v", v, contiguous=False)
@@ -265,11 +289,16 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *, k_inv
     for t in (k, v):
         if t.stride(2) != 1 or t.stride(1) != D:
             raise ValueError("k/v rows must be contiguous per token")
-    st = pa_reshape_and_cache(_ptr(k), _ptr(v), dtype_code(k), k.stride(0), v.stride(0),
-                              _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), k_cache.shape[0],
-                              _ptr(slot_mapping), N, Hkv, D, int(block_size),
-                              _ptr(k_inv_scale), _ptr(v_inv_scale), _stream(stream))
-    _check("pa_reshape_and_cache", st)
+    args = (_ptr(k), _ptr(v), dtype_code(k), k.stride(0), v.stride(0),
+            _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), k_cache.shape[0],
+            _ptr(slot_mapping), N, Hkv, D, int(block_size), _ptr(k_inv_scale), _ptr(v_inv_scale))
+    if k_zero_point is not None or v_zero_point is not None:
+        opt = CacheWriteOptions(k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point))
+        st = pa_reshape_and_cache_ex(*args, ctypes.byref(opt), _stream(stream))
+        _check("pa_reshape_and_cache_ex", st)
+    else:
+        st = pa_reshape_and_cache(*args, _stream(stream))
+        _check("pa_reshape_and_cache", st)
 
 
 def copy_blocks(k_cache, v_cache, src_dst_pairs, *, stream=None):

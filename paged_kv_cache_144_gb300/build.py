@@ -30,6 +30,7 @@ SOURCES = [
     "pa_decode_f16.cu",
     "pa_decode_bf16.cu",
     "pa_decode_fp8.cu",
+    "pa_decode_int8.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -53,6 +53,7 @@ int dtype_bytes(int dt) {
     case PA_F16: return 2;
     case PA_BF16: return 2;
     case PA_FP8_E4M3: return 1;
+    case PA_INT8: return 1;
     default: return 0;
   }
 }
@@ -103,7 +104,7 @@ int gmax_for_group(int g) { return g <= 1 ? 1 : (g <= 4 ? 4 : 8); }
 // 64-row units need B >= 16.  PA_DECODE_UNIT_ROWS (16, 32; 64 for FP8)
 // overrides it (tuning).
 int unit_rows_for(int kv_dtype, int block_size) {
-  const bool fp8 = kv_dtype == PA_FP8_E4M3;
+  const bool fp8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8;  // 8-bit cache
   const int env = pa::tuning_override("PA_DECODE_UNIT_ROWS");
   if (env == 16 || env == 32) return env;
   if (env == 64 && fp8 && block_size >= 16) return 64;
@@ -117,7 +118,7 @@ int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_d
   if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
   if (num_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (kv_dtype == PA_FP8_E4M3 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if ((kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8) && head_dim != 128) return PA_ERR_UNSUPPORTED;
   // a power of two from 8 to 1024: a work unit (16, 32 or 64 rows) then covers
   // whole blocks or a whole fraction of one
   if (block_size < 8 || block_size > 1024 || (block_size & (block_size - 1)) != 0) return PA_ERR_UNSUPPORTED;
@@ -195,7 +196,7 @@ PA_EXPORT size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_
   if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                          partition_size, kv_dtype) != PA_OK)
     return static_cast<size_t>(-1);
-  const int q_dtype = (kv_dtype == PA_FP8_E4M3) ? PA_BF16 : kv_dtype;
+  const int q_dtype = (kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8) ? PA_BF16 : kv_dtype;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return static_cast<size_t>(-1);
   DecodePlan plan;
   if (make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, partition_size, q_dtype,
@@ -213,7 +214,7 @@ PA_EXPORT int pa_decode_launch_config(int num_seqs, int num_heads, int num_kv_he
   if (sh != PA_OK) return sh;
   if (!ctas || !warps_per_cta || !stages || !smem_bytes) return PA_ERR_NULL;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_DTYPE;
-  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
+  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3 && kv_dtype != PA_INT8) return PA_ERR_DTYPE;
   DecodePlan plan;
   const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                            partition_size, q_dtype, kv_dtype, true, &plan);
@@ -246,8 +247,9 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_NULL;
   if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_DTYPE;
-  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
-  if (kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_NULL;
+  if (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3 && kv_dtype != PA_INT8) return PA_ERR_DTYPE;
+  if ((kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8) && (!k_scale || !v_scale)) return PA_ERR_NULL;
+  if (kv_dtype == PA_INT8 && (!o.k_zero_point || !o.v_zero_point)) return PA_ERR_NULL;
   if (num_blocks <= 0 || num_blocks * num_kv_heads * block_size >= (int64_t{1} << 31)) return PA_ERR_SHAPE;
   if (q_stride < static_cast<int64_t>(num_heads) * head_dim) return PA_ERR_SHAPE;
   if (!aligned16(q) || (q_stride * 2) % 16 != 0 || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
@@ -276,6 +278,8 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.q_stride = q_stride;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.k_zero_point = o.k_zero_point;
+  p.v_zero_point = o.v_zero_point;
   p.block_tables = block_tables;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.seq_lens = seq_lens;
@@ -313,18 +317,26 @@ PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q
                       block_size, partition_size, workspace, workspace_bytes, nullptr, stream);
 }
 
-PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype, int64_t k_stride,
-                                   int64_t v_stride, void* k_cache, void* v_cache, pa_dtype kv_dtype,
-                                   int64_t num_blocks, const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
-                                   int head_dim, int block_size, const float* k_inv_scale,
-                                   const float* v_inv_scale, void* stream) {
+PA_EXPORT int pa_reshape_and_cache_ex(const void* k, const void* v, pa_dtype src_dtype, int64_t k_stride,
+                                      int64_t v_stride, void* k_cache, void* v_cache, pa_dtype kv_dtype,
+                                      int64_t num_blocks, const int64_t* slot_mapping, int num_tokens,
+                                      int num_kv_heads, int head_dim, int block_size, const float* k_inv_scale,
+                                      const float* v_inv_scale, const pa_cache_write_options* opt, void* stream) {
+  pa_cache_write_options o;
+  memset(&o, 0, sizeof(o));
+  if (opt) {
+    if (opt->struct_size < sizeof(size_t)) return PA_ERR_SHAPE;
+    memcpy(&o, opt, opt->struct_size < sizeof(o) ? opt->struct_size : sizeof(o));
+  }
   if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
   if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
   if (src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_DTYPE;
-  if (kv_dtype != src_dtype && kv_dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
-  if (kv_dtype == PA_FP8_E4M3 && (!k_inv_scale || !v_inv_scale)) return PA_ERR_NULL;
+  const bool quant = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8;
+  if (kv_dtype != src_dtype && !quant) return PA_ERR_DTYPE;
+  if (quant && (!k_inv_scale || !v_inv_scale)) return PA_ERR_NULL;
+  if (kv_dtype == PA_INT8 && (!o.k_zero_point || !o.v_zero_point)) return PA_ERR_NULL;
   const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
   if (k_stride < row || v_stride < row) return PA_ERR_SHAPE;
   if (!aligned16(k) || !aligned16(v) || (k_stride * 2) % 16 != 0 || (v_stride * 2) % 16 != 0 ||
@@ -351,8 +363,20 @@ PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dt
   a.block_size = block_size;
   a.k_inv_scale = k_inv_scale;
   a.v_inv_scale = v_inv_scale;
+  a.k_zero_point = o.k_zero_point;
+  a.v_zero_point = o.v_zero_point;
   return cuda_status(pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream)),
                      "pa_reshape_and_cache launch");
+}
+
+PA_EXPORT int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype, int64_t k_stride,
+                                   int64_t v_stride, void* k_cache, void* v_cache, pa_dtype kv_dtype,
+                                   int64_t num_blocks, const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_dim, int block_size, const float* k_inv_scale,
+                                   const float* v_inv_scale, void* stream) {
+  return pa_reshape_and_cache_ex(k, v, src_dtype, k_stride, v_stride, k_cache, v_cache, kv_dtype, num_blocks,
+                                 slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, k_inv_scale,
+                                 v_inv_scale, nullptr, stream);
 }
 
 PA_EXPORT int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, size_t block_bytes,
@@ -438,7 +462,8 @@ PA_EXPORT int pa_decode_noalloc(void* out, pa_dtype out_dtype, const void* q, pa
                                     partition_size, kv_dtype);
   if (sh != PA_OK) return sh;
   if (num_seqs == 0) return PA_OK;
-  if ((q_dtype != PA_F16 && q_dtype != PA_BF16) || (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3))
+  if ((q_dtype != PA_F16 && q_dtype != PA_BF16) ||
+      (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3 && kv_dtype != PA_INT8))
     return PA_ERR_DTYPE;
   DecodePlan plan;
   const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,

@@ -7,7 +7,8 @@
 // One warp writes one (token, head, K|V) row: a single coalesced load of the
 // source row and a single coalesced store into the cache row.  FP8 caches
 // (§"KV量子化: FP8とINT8") quantise float32(x) * inv_scale[h] with
-// round-to-nearest-even and saturation to +-448.
+// round-to-nearest-even and saturation to +-448; INT8 caches store
+// clamp(rne(float32(x) * inv_scale[h]) + zero_point[h], -128, 127).
 //
 // copy_blocks follows the PagedAttention explainer (0h-n0.github.io),
 // §"Copy-on-Write（CoW）によるメモリ共有": the contents of a shared block are
@@ -21,12 +22,24 @@ namespace pa {
 
 namespace {
 
-template <typename SRC, bool TO_FP8, int D>
+enum CacheMode { kCopy = 0, kToFp8 = 1, kToInt8 = 2 };
+
+// float32 y (= x * inv_scale, already rounded to float32) -> INT8 code:
+// nearest integer (ties to even) plus the zero point, saturated to the int8
+// range; NaN saturates upward.
+__device__ __forceinline__ int int8_code(float y, int zp) {
+  if (y != y) return 127;
+  const float r = rintf(y) + static_cast<float>(zp);
+  return static_cast<int>(fminf(fmaxf(r, -128.f), 127.f));
+}
+
+template <typename SRC, int MODE, int D>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const void* __restrict__ k, const void* __restrict__ v, int64_t k_stride, int64_t v_stride,
     void* __restrict__ k_cache, void* __restrict__ v_cache, int64_t num_blocks,
     const int64_t* __restrict__ slot_mapping, int num_tokens, int num_kv_heads, int block_size,
-    const float* __restrict__ k_inv_scale, const float* __restrict__ v_inv_scale, unsigned int* err) {
+    const float* __restrict__ k_inv_scale, const float* __restrict__ v_inv_scale,
+    const int32_t* __restrict__ k_zero_point, const int32_t* __restrict__ v_zero_point, unsigned int* err) {
   constexpr int EPL = D / 32;  // elements per lane: 2 or 4
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -50,13 +63,28 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
   const int64_t src_elem = n * (which ? v_stride : k_stride) + static_cast<int64_t>(h) * D + lane * EPL;
   void* cache = which ? v_cache : k_cache;
 
-  if constexpr (!TO_FP8) {
+  if constexpr (MODE == kCopy) {
     if constexpr (EPL == 4) {
       const uint2 x = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + src_elem);
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(cache) + dst_elem) = x;
     } else {
       const uint32_t x = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(src) + src_elem);
       *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(cache) + dst_elem) = x;
+    }
+  } else if constexpr (MODE == kToInt8) {
+    const float inv = (which ? v_inv_scale : k_inv_scale)[h];
+    const int zp = (which ? v_zero_point : k_zero_point)[h];
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int c = int8_code(__fmul_rn(load_scalar<SRC>(src, src_elem + i), inv), zp);
+      packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * i);
+    }
+    uint8_t* dst = static_cast<uint8_t*>(cache) + dst_elem;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
     }
   } else {
     const float inv = (which ? v_inv_scale : k_inv_scale)[h];
@@ -115,19 +143,23 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
   if (rows == 0) return cudaSuccess;
   const int warps_per_cta = 8;
   const int64_t grid = (rows + warps_per_cta - 1) / warps_per_cta;
-#define PA_RC_LAUNCH(SRC, FP8, D)                                                               \
-  reshape_and_cache_kernel<SRC, FP8, D><<<static_cast<unsigned>(grid), 256, 0, stream>>>(      \
+#define PA_RC_LAUNCH(SRC, MODE, D)                                                              \
+  reshape_and_cache_kernel<SRC, MODE, D><<<static_cast<unsigned>(grid), 256, 0, stream>>>(     \
       a.k, a.v, a.k_stride, a.v_stride, a.k_cache, a.v_cache, a.num_blocks, a.slot_mapping,     \
-      a.num_tokens, a.num_kv_heads, a.block_size, a.k_inv_scale, a.v_inv_scale, a.err)
-  const bool fp8 = a.kv_dtype == PA_FP8_E4M3;
+      a.num_tokens, a.num_kv_heads, a.block_size, a.k_inv_scale, a.v_inv_scale, a.k_zero_point, \
+      a.v_zero_point, a.err)
+#define PA_RC_D(SRC, MODE) \
+  if (a.head_dim == 128) PA_RC_LAUNCH(SRC, MODE, 128); else PA_RC_LAUNCH(SRC, MODE, 64);
+  const int mode = a.kv_dtype == PA_FP8_E4M3 ? kToFp8 : (a.kv_dtype == PA_INT8 ? kToInt8 : kCopy);
   (void)cudaGetLastError();
   if (a.src_dtype == PA_F16) {
-    if (fp8) { if (a.head_dim == 128) PA_RC_LAUNCH(f16_t, true, 128); else PA_RC_LAUNCH(f16_t, true, 64); }
-    else { if (a.head_dim == 128) PA_RC_LAUNCH(f16_t, false, 128); else PA_RC_LAUNCH(f16_t, false, 64); }
+    if (mode == kToFp8) { PA_RC_D(f16_t, kToFp8) } else if (mode == kToInt8) { PA_RC_D(f16_t, kToInt8) }
+    else { PA_RC_D(f16_t, kCopy) }
   } else {
-    if (fp8) { if (a.head_dim == 128) PA_RC_LAUNCH(bf16_t, true, 128); else PA_RC_LAUNCH(bf16_t, true, 64); }
-    else { if (a.head_dim == 128) PA_RC_LAUNCH(bf16_t, false, 128); else PA_RC_LAUNCH(bf16_t, false, 64); }
+    if (mode == kToFp8) { PA_RC_D(bf16_t, kToFp8) } else if (mode == kToInt8) { PA_RC_D(bf16_t, kToInt8) }
+    else { PA_RC_D(bf16_t, kCopy) }
   }
+#undef PA_RC_D
 #undef PA_RC_LAUNCH
   return cudaGetLastError();
 }

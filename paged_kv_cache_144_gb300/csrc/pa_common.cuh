@@ -161,11 +161,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 struct f16_t {};
 struct bf16_t {};
 struct e4m3_t {};
+struct i8_t {};  // INT8 code with a per-KV-head scale and zero point
 
 template <typename T> struct elem;
 template <> struct elem<f16_t> { static constexpr int bytes = 2; using storage = uint16_t; };
 template <> struct elem<bf16_t> { static constexpr int bytes = 2; using storage = uint16_t; };
 template <> struct elem<e4m3_t> { static constexpr int bytes = 1; using storage = uint8_t; };
+template <> struct elem<i8_t> { static constexpr int bytes = 1; using storage = int8_t; };
 
 // Widen two packed 16-bit values (one 32-bit word) to a float2 (x = low half).
 template <typename T> __device__ __forceinline__ float2 widen2(uint32_t w);
@@ -273,6 +275,29 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
   uint32_t d;
   asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(w16));
   return d;
+}
+
+// Four 8-bit cache codes w (byte i = element i) -> two f16x2 words: elements
+// (0, 1) in lo and (2, 3) in hi, low index in the low half, exact.
+//  * e4m3: hardware conversion.
+//  * int8 (value = code - zero point): each code c is placed as the low byte
+//    of the f16 pattern 0x64xx after flipping its sign bit, which reads as
+//    1024 + (c + 128); subtracting zp2 = f16x2(1152 + zero point) leaves
+//    c - zero point.  Every step is exact (integers below 2048).
+template <typename T>
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t zp2, uint32_t& lo, uint32_t& hi);
+template <>
+__device__ __forceinline__ void widen4<e4m3_t>(uint32_t w, uint32_t /*zp2*/, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_to_f16x2(w & 0xffffu);
+  hi = e4m3x2_to_f16x2(w >> 16);
+}
+template <>
+__device__ __forceinline__ void widen4<i8_t>(uint32_t w, uint32_t zp2, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = prmt(u, 0x64646464u, 0x5140u);
+  const uint32_t b = prmt(u, 0x64646464u, 0x7362u);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(zp2));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(zp2));
 }
 
 // (lo, hi) fp32 -> packed 16-bit pair, round to nearest even; lo in the low half.

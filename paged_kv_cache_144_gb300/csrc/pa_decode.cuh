@@ -12,7 +12,7 @@
 // recurrence runs in base 2 with log2(e) folded into the scale.
 //
 // How it is laid out on GB300 (this is not the pages' A100 kernel design):
-//  * Work unit = UR (16, 32; 64 for FP8) consecutive rows of one (sequence, KV head).
+//  * Work unit = UR (16, 32; 64 for 8-bit caches) consecutive rows of one (sequence, KV head).
 //    A unit is filled by 3-D TMA boxes of min(UR, B) whole rows: part of one
 //    block when B >= UR, one box per block when a unit spans several blocks;
 //    one TMA instruction per box for K and one for V.  A box lands as
@@ -41,11 +41,12 @@
 //    a hi + lo pair of 16-bit values (two MMAs), which keeps their rounding
 //    error near 2^-16 relative.
 //  * 16-bit caches feed the MMAs with ldmatrix (K) and ldmatrix.trans (V)
-//    straight from the swizzled tiles.  FP8 caches are widened in registers
-//    (e4m3 -> f16x2, exact) with the head_dim order of QK permuted so that a
-//    lane reads 16 contiguous bytes of a K row, and V transposed in registers
-//    with byte permutes; the per-head K scale multiplies the scores, the V
-//    scale the final divide, and q is rounded to f16 for the product.
+//    straight from the swizzled tiles.  8-bit caches are widened in registers
+//    (e4m3 -> f16x2, or INT8 code - zero point -> f16x2, both exact) with the
+//    head_dim order of QK permuted so that a lane reads 16 contiguous bytes
+//    of a K row, and V transposed in registers with byte permutes; the
+//    per-head K scale multiplies the scores, the V scale the final divide,
+//    and q is rounded to f16 for the product.
 //  * Split segments: a warp whose range covers only part of a segment writes
 //    its (m, l, acc) record to the workspace and bumps the segment's arrival
 //    counter; the warp that arrives last merges all records with the same
@@ -82,7 +83,7 @@ struct DecodeTraits {
   static constexpr int KVB = elem<KVT>::bytes;
   static constexpr int ROW = D * KVB;  // bytes of one cache row
   static_assert(ROW == 128 || ROW == 256, "cache rows must be 128 or 256 bytes");
-  static constexpr int UR = UR_;                 // rows per work unit (16, 32; 64 for FP8)
+  static constexpr int UR = UR_;                 // rows per work unit (16, 32; 64 for 8-bit caches)
   static_assert(UR == 16 || UR == 32 || (UR == 64 && KVB == 1), "unit rows");
   static constexpr int UR_SHIFT = UR == 64 ? 6 : (UR == 32 ? 5 : 4);
   static constexpr int NSUB = ROW / 128;         // 128-byte halves per row
@@ -94,9 +95,9 @@ struct DecodeTraits {
   static constexpr int KS = D / 16;              // k-steps of S^T = Q K^T, m-tiles of O^T
   static constexpr int NT = UR / 8;              // 8-token n-tiles of a unit
   static constexpr int NSB = UR / 16;            // 16-token sub-tiles (one PV k-step each)
-  static constexpr bool FP8 = KVB == 1;
-  static constexpr bool MMA_BF16 = !FP8 && std::is_same<KVT, bf16_t>::value;  // else f16
-  static_assert(!FP8 || D == 128, "FP8 caches: head_dim 128");
+  static constexpr bool B8 = KVB == 1;          // FP8-e4m3 or INT8 cache
+  static constexpr bool MMA_BF16 = !B8 && std::is_same<KVT, bf16_t>::value;  // else f16
+  static_assert(!B8 || D == 128, "8-bit caches: head_dim 128");
   // per-consumer shared memory: [full[MAX_NS] | empty[MAX_NS] | NS stages]
   static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + MAX_NS * 8;
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__((DecodeTraits<QT, KVT, D, GM, UR_>::MAX_W + 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const DecodeParams p) {
   using Tr = DecodeTraits<QT, KVT, D, GM, UR_>;
-  constexpr bool kFp8 = elem<KVT>::bytes == 1;
+  constexpr bool k8bit = elem<KVT>::bytes == 1;
   constexpr int UR = Tr::UR;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -600,11 +601,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // (K) or m-tile s (V).  Matrices 0..3 = (rows 0-7, cols lo), (rows 0-7,
   // cols hi), (rows 8-15, cols lo), (rows 8-15, cols hi) of a 16x16 block.
   uint32_t moff[Tr::KS];
-  // FP8 tiles: n-position j of an 8-token n-tile holds token j ^ 4(j & 1),
+  // 8-bit tiles: n-position j of an 8-token n-tile holds token j ^ 4(j & 1),
   // which keeps both the K and the V loads below free of bank conflicts.
   auto sigma = [](int j) { return j ^ ((j & 1) << 2); };
   uint32_t kb8[2], vb8[2][Tr::KS / 2];
-  if constexpr (!kFp8) {
+  if constexpr (!k8bit) {
     const int lt = (lane & 7) + ((lane >> 4) << 3);
     const int lhi = (lane >> 3) & 1;
 #pragma unroll
@@ -625,7 +626,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   }
   // head_dim column of accumulator row (m-tile i, half hf) of O^T
   auto dim_of = [&](int i, int hf) -> int {
-    if constexpr (!kFp8) return 16 * i + gid + 8 * hf;
+    if constexpr (!k8bit) return 16 * i + gid + 8 * hf;
     return 32 * (i >> 1) + 4 * gid + 2 * (i & 1) + hf;
   };
 
@@ -633,6 +634,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   float m = -INFINITY, l = 0.f;       // running max / sum of head gid (log2 domain)
   float acc[Tr::KS][4];               // O^T: rows = head_dim columns, cols = heads 2t, 2t+1
   float score_scale = p.qk_scale_log2;
+  uint32_t zpk2 = 0u, zpv2 = 0u;  // INT8: f16x2(1152 + zero point) of this KV head
 
   // One unit: S^T = Q K^T, online-softmax update, O^T += V^T P^T.
   // FULL: all UR rows valid.
@@ -643,7 +645,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
     for (int nt = 0; nt < Tr::NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
     // ---- scores
-    if constexpr (!kFp8) {
+    if constexpr (!k8bit) {
 #pragma unroll
       for (int sb = 0; sb < Tr::NSB; ++sb) {
 #pragma unroll
@@ -664,8 +666,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int s = 4 * g + r;
-            mma16816<false>(sc[nt], qa0[s], 0u, qa1[s], 0u, e4m3x2_to_f16x2(ws[r] & 0xffffu),
-                            e4m3x2_to_f16x2(ws[r] >> 16));
+            uint32_t b0, b1;
+            widen4<KVT>(ws[r], zpk2, b0, b1);
+            mma16816<false>(sc[nt], qa0[s], 0u, qa1[s], 0u, b0, b1);
           }
         }
       }
@@ -678,7 +681,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       for (int e = 0; e < 2; ++e) {
         float x = sc[nt][e] * score_scale;
         if constexpr (!FULL) {
-          const int tok = nt * 8 + (kFp8 ? sigma(2 * tig + e) : 2 * tig + e);
+          const int tok = nt * 8 + (k8bit ? sigma(2 * tig + e) : 2 * tig + e);
           x = (tok < n_valid && tok >= lo_rel) ? x : -INFINITY;
         }
         sc[nt][e] = x;
@@ -729,7 +732,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       __syncwarp();
     }
     // ---- O^T += V^T P^T
-    if constexpr (!kFp8) {
+    if constexpr (!k8bit) {
 #pragma unroll
       for (int sb = 0; sb < Tr::NSB; ++sb) {
 #pragma unroll
@@ -752,10 +755,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const uint32_t y1 = lds32(vt + (2 * sb + 1) * 1024 + vb8[1][jj]);
           const uint32_t lo01 = prmt(x0, x1, 0x5140u), lo23 = prmt(x0, x1, 0x7362u);
           const uint32_t hi01 = prmt(y0, y1, 0x5140u), hi23 = prmt(y0, y1, 0x7362u);
-          const uint32_t d0l = e4m3x2_to_f16x2(lo01 & 0xffffu), d1l = e4m3x2_to_f16x2(lo01 >> 16);
-          const uint32_t d2l = e4m3x2_to_f16x2(lo23 & 0xffffu), d3l = e4m3x2_to_f16x2(lo23 >> 16);
-          const uint32_t d0h = e4m3x2_to_f16x2(hi01 & 0xffffu), d1h = e4m3x2_to_f16x2(hi01 >> 16);
-          const uint32_t d2h = e4m3x2_to_f16x2(hi23 & 0xffffu), d3h = e4m3x2_to_f16x2(hi23 >> 16);
+          uint32_t d0l, d1l, d2l, d3l, d0h, d1h, d2h, d3h;
+          widen4<KVT>(lo01, zpv2, d0l, d1l);
+          widen4<KVT>(lo23, zpv2, d2l, d3l);
+          widen4<KVT>(hi01, zpv2, d0h, d1h);
+          widen4<KVT>(hi23, zpv2, d2h, d3h);
           mma16816<false>(acc[2 * jj], d0l, d1l, d0h, d1h, ph[sb][0], ph[sb][1]);
           mma16816<false>(acc[2 * jj], d0l, d1l, d0h, d1h, pl[sb][0], pl[sb][1]);
           mma16816<false>(acc[2 * jj + 1], d2l, d3l, d2h, d3h, ph[sb][0], ph[sb][1]);
@@ -778,14 +782,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
       for (int s = 0; s < Tr::KS; ++s) {
         // columns of k-step s held by this lane: (d, d+1) for a0, (d2, d2+1) for a2
-        const int d = kFp8 ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 16 * s + 2 * tig;
-        const int d2 = kFp8 ? d + 2 : d + 8;
+        const int d = k8bit ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 16 * s + 2 * tig;
+        const int d2 = k8bit ? d + 2 : d + 8;
         uint32_t w0 = 0u, w1 = 0u;
         if (row_ok) {
           w0 = *reinterpret_cast<const uint32_t*>(qr + (gid * D + d) * 2);
           w1 = *reinterpret_cast<const uint32_t*>(qr + (gid * D + d2) * 2);
         }
-        if constexpr (kFp8 && std::is_same<QT, bf16_t>::value) {
+        if constexpr (k8bit && std::is_same<QT, bf16_t>::value) {
           const float2 f0 = widen2<bf16_t>(w0), f1 = widen2<bf16_t>(w1);
           w0 = pack2<false>(f0.x, f0.y);
           w1 = pack2<false>(f1.x, f1.y);
@@ -795,7 +799,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
     }
     score_scale = p.qk_scale_log2;
-    if constexpr (kFp8) score_scale *= __ldg(p.k_scale + it.kvh);
+    if constexpr (k8bit) score_scale *= __ldg(p.k_scale + it.kvh);
+    if constexpr (std::is_same<KVT, i8_t>::value) {
+      const uint32_t zk = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.k_zero_point + it.kvh))));
+      const uint32_t zv = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.v_zero_point + it.kvh))));
+      zpk2 = zk | (zk << 16);
+      zpv2 = zv | (zv << 16);
+    }
     m = -INFINITY;
     l = 0.f;
 #pragma unroll
@@ -834,7 +844,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       const float l1 = __shfl_sync(0xffffffffu, lt, 8 * tig + 4);  // head 2t+1
       const int h0 = 2 * tig, h1 = 2 * tig + 1;
       float vs = 1.f;
-      if constexpr (kFp8) vs = __ldg(p.v_scale + it.kvh);
+      if constexpr (k8bit) vs = __ldg(p.v_scale + it.kvh);
       const int64_t orow = static_cast<int64_t>(it.s) * p.num_heads + static_cast<int64_t>(it.kvh) * G;
       if (it.slot < 0) {
         const float i0 = vs / l0, i1 = vs / l1;

@@ -40,6 +40,7 @@ template <typename T> constexpr int dtype_code();
 template <> constexpr int dtype_code<f16_t>() { return PA_F16; }
 template <> constexpr int dtype_code<bf16_t>() { return PA_BF16; }
 template <> constexpr int dtype_code<e4m3_t>() { return PA_FP8_E4M3; }
+template <> constexpr int dtype_code<i8_t>() { return PA_INT8; }
 
 #define PA_MATCH(QT, KVT, D, GM, UR)                                                        \
   (key.q_dtype == dtype_code<QT>() && key.kv_dtype == dtype_code<KVT>() && key.head_dim == D && key.gmax == GM && \

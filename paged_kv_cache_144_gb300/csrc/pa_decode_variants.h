@@ -1,6 +1,6 @@
 // pa_decode_variants.h - the compiled (q dtype, kv dtype, head_dim, max group,
 // unit rows) variants of the decode kernel (the block size is a runtime
-// parameter; 64-row units are compiled for FP8 caches only).  A group G is served by the
+// parameter; 64-row units are compiled for 8-bit caches only).  A group G is served by the
 // smallest compiled maximum >= G (1, 4 or 8).
 #pragma once
 
@@ -27,7 +27,16 @@
   X(bf16_t, e4m3_t, 128, 1, 64) X(bf16_t, e4m3_t, 128, 4, 64) X(bf16_t, e4m3_t, 128, 8, 64) \
   X(f16_t, e4m3_t, 128, 1, 64) X(f16_t, e4m3_t, 128, 4, 64) X(f16_t, e4m3_t, 128, 8, 64)
 
-#define PA_DECODE_VARIANTS(X) PA_DECODE_VARIANTS_F16(X) PA_DECODE_VARIANTS_BF16(X) PA_DECODE_VARIANTS_FP8(X)
+#define PA_DECODE_VARIANTS_INT8(X) \
+  X(bf16_t, i8_t, 128, 1, 16) X(bf16_t, i8_t, 128, 1, 32) X(bf16_t, i8_t, 128, 1, 64) \
+  X(bf16_t, i8_t, 128, 4, 16) X(bf16_t, i8_t, 128, 4, 32) X(bf16_t, i8_t, 128, 4, 64) \
+  X(bf16_t, i8_t, 128, 8, 16) X(bf16_t, i8_t, 128, 8, 32) X(bf16_t, i8_t, 128, 8, 64) \
+  X(f16_t, i8_t, 128, 1, 16) X(f16_t, i8_t, 128, 1, 32) X(f16_t, i8_t, 128, 1, 64) \
+  X(f16_t, i8_t, 128, 4, 16) X(f16_t, i8_t, 128, 4, 32) X(f16_t, i8_t, 128, 4, 64) \
+  X(f16_t, i8_t, 128, 8, 16) X(f16_t, i8_t, 128, 8, 32) X(f16_t, i8_t, 128, 8, 64)
+
+#define PA_DECODE_VARIANTS(X) \
+  PA_DECODE_VARIANTS_F16(X) PA_DECODE_VARIANTS_BF16(X) PA_DECODE_VARIANTS_FP8(X) PA_DECODE_VARIANTS_INT8(X)
 
 // Each variant translation unit defines these two plain functions; the
 // dispatcher sees only the declarations, so every kernel is instantiated and

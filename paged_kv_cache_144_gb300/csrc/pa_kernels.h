@@ -33,6 +33,8 @@ struct ReshapeArgs {
   int block_size;
   const float* k_inv_scale;
   const float* v_inv_scale;
+  const int32_t* k_zero_point;  // INT8 only
+  const int32_t* v_zero_point;  // INT8 only
   unsigned int* err;
 };
 
@@ -46,8 +48,10 @@ struct DecodeParams {
   int out_dtype;
   const void* q;
   int64_t q_stride;             // elements between consecutive sequences of q
-  const float* k_scale;         // FP8 only
-  const float* v_scale;         // FP8 only
+  const float* k_scale;         // 8-bit caches only
+  const float* v_scale;         // 8-bit caches only
+  const int32_t* k_zero_point;  // INT8 only
+  const int32_t* v_zero_point;  // INT8 only
   const int32_t* block_tables;
   int max_blocks_per_seq;
   const int32_t* seq_lens;
@@ -70,7 +74,7 @@ struct DecodeParams {
 // Compile-time variant of the decode kernel.
 struct DecodeKey {
   int q_dtype;    // PA_F16 / PA_BF16
-  int kv_dtype;   // PA_F16 / PA_BF16 / PA_FP8_E4M3
+  int kv_dtype;   // PA_F16 / PA_BF16 / PA_FP8_E4M3 / PA_INT8
   int head_dim;   // 64 / 128
   int gmax;       // 1 / 4 / 8 (query heads per KV head, rounded up)
   int unit_rows;  // 16 / 32 / 64 rows per work unit

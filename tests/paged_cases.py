@@ -8,7 +8,7 @@ import numpy as np
 import oracle
 import workloads
 
-TORCH_DT = {"f16": "float16", "bf16": "bfloat16", "e4m3": "uint8", "f32": "float32"}
+TORCH_DT = {"f16": "float16", "bf16": "bfloat16", "e4m3": "uint8", "i8": "int8", "f32": "float32"}
 PA_TOL = 2e-3          # max-abs error bound for attention outputs (fp32 out)
 
 
@@ -18,6 +18,8 @@ def to_torch(x: np.ndarray, fmt: str, device):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
     if fmt == "e4m3":
         return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint8)).to(device)
+    if fmt == "i8":
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int8)).to(device)
     return torch.from_numpy(np.ascontiguousarray(x)).to(device)
 
 
@@ -54,19 +56,23 @@ def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", d
     q = to_torch(vals["q"], batch.q_fmt, device)
     kc = to_torch(vals["k_cache"], kv, device)
     vc = to_torch(vals["v_cache"], kv, device)
-    src_fmt = "bf16" if kv == "e4m3" else kv   # FP8 sources are bf16 rows
-    ks = vs = kis = vis = None
-    if kv == "e4m3":
+    quant = kv in ("e4m3", "i8")
+    src_fmt = "bf16" if quant else kv   # 8-bit caches are written from bf16 rows
+    ks = vs = kis = vis = kz = vz = None
+    if quant:
         ks = torch.from_numpy(vals["k_scale"]).to(device)
         vs = torch.from_numpy(vals["v_scale"]).to(device)
         kis = torch.from_numpy(vals["k_inv_scale"]).to(device)
         vis = torch.from_numpy(vals["v_inv_scale"]).to(device)
+        if kv == "i8":
+            kz = torch.from_numpy(vals["k_zero_point"]).to(device)
+            vz = torch.from_numpy(vals["v_zero_point"]).to(device)
         slots = torch.from_numpy(vals["src_slots"]).to(device)
         pa.reshape_and_cache(to_torch(vals["k_src"], "bf16", device), to_torch(vals["v_src"], "bf16", device),
-                             kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis)
+                             kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz, v_zero_point=vz)
     new_slots = torch.from_numpy(batch.new_slots).to(device)
     pa.reshape_and_cache(to_torch(vals["k_new"], src_fmt, device), to_torch(vals["v_new"], src_fmt, device),
-                         kc, vc, new_slots, B, k_inv_scale=kis, v_inv_scale=vis)
+                         kc, vc, new_slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz, v_zero_point=vz)
     tables = torch.from_numpy(batch.block_tables).to(device)
     lens = torch.from_numpy(batch.seq_lens).to(device)
     out = torch.empty((batch.num_seqs, batch.num_heads, batch.head_dim), dtype=getattr(torch, TORCH_DT[out_fmt]),
@@ -77,7 +83,7 @@ def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", d
                                       batch.max_blocks_per_seq, partition_size, pa.dtype_code(kc))
         ws = pa.new_workspace(n, device) if n else None
     pa.decode(out, q, kc, vc, tables, lens, batch.num_kv_heads, batch.scale, B, k_scale=ks, v_scale=vs,
-              partition_size=partition_size, workspace=ws, window=window)
+              partition_size=partition_size, workspace=ws, window=window, k_zero_point=kz, v_zero_point=vz)
     err = pa.get_device_error()
     return (out.float().cpu().numpy().astype(np.float64), to_numpy(kc, kv), to_numpy(vc, kv), err)
 
@@ -87,17 +93,22 @@ def run_oracle(batch, vals, window=0):
     kv = batch.kv_fmt
     B = batch.block_size
     kc, vc = vals["k_cache"], vals["v_cache"]
-    src_fmt = "bf16" if kv == "e4m3" else kv
+    quant = kv in ("e4m3", "i8")
+    src_fmt = "bf16" if quant else kv
     kis = vals.get("k_inv_scale")
     vis = vals.get("v_inv_scale")
-    if kv == "e4m3":
+    kz, vz = vals.get("k_zero_point"), vals.get("v_zero_point")
+    if quant:
         kc, vc = oracle.reshape_and_cache(vals["k_src"], vals["v_src"], kc, vc, vals["src_slots"], B,
-                                          src_fmt="bf16", kv_fmt="e4m3", k_inv_scale=kis, v_inv_scale=vis)
+                                          src_fmt="bf16", kv_fmt=kv, k_inv_scale=kis, v_inv_scale=vis,
+                                          k_zero_point=kz, v_zero_point=vz)
     kc, vc = oracle.reshape_and_cache(vals["k_new"], vals["v_new"], kc, vc, batch.new_slots, B,
-                                      src_fmt=src_fmt, kv_fmt=kv, k_inv_scale=kis, v_inv_scale=vis)
+                                      src_fmt=src_fmt, kv_fmt=kv, k_inv_scale=kis, v_inv_scale=vis,
+                                      k_zero_point=kz, v_zero_point=vz)
     ref = oracle.paged_decode_attention(vals["q"], kc, vc, batch.block_tables, batch.seq_lens, batch.scale, B,
                                         q_fmt=batch.q_fmt, kv_fmt=kv, k_scale=vals.get("k_scale"),
-                                        v_scale=vals.get("v_scale"), window=window)
+                                        v_scale=vals.get("v_scale"), window=window, k_zero_point=kz,
+                                        v_zero_point=vz)
     return ref, kc, vc
 
 

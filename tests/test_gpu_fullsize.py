@@ -31,21 +31,23 @@ def _run_full(name, seed, *, q_mult=1.0, n_samples=12, **overrides):
     vals = workloads.device_values(b, seed, dev, q_mult=q_mult)
     B, Hkv, D = b.block_size, b.num_kv_heads, b.head_dim
     kc, vc = vals["k_cache"], vals["v_cache"]
-    fp8 = b.kv_fmt == "e4m3"
+    quant = b.kv_fmt in ("e4m3", "i8")
     ks = vs = kis = vis = None
-    if fp8:
+    kz, vz = vals.get("k_zero_point"), vals.get("v_zero_point")
+    if quant:
         ks, vs, kis, vis = vals["k_scale"], vals["v_scale"], vals["k_inv_scale"], vals["v_inv_scale"]
         pa.reshape_and_cache(vals["k_src"], vals["v_src"], kc, vc, vals["src_slots"], B,
-                             k_inv_scale=kis, v_inv_scale=vis)
+                             k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz, v_zero_point=vz)
     pa.reshape_and_cache(vals["k_new"], vals["v_new"], kc, vc, torch.from_numpy(b.new_slots).to(dev), B,
-                         k_inv_scale=kis, v_inv_scale=vis)
+                         k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz, v_zero_point=vz)
     tables = torch.from_numpy(b.block_tables).to(dev)
     lens = torch.from_numpy(b.seq_lens).to(dev)
     out = torch.empty((b.num_seqs, b.num_heads, D), dtype=torch.float32, device=dev)
     n = pa.decode_workspace_bytes(b.num_seqs, b.num_heads, Hkv, D, B, b.max_blocks_per_seq, 0,
                                   pa.dtype_code(kc))
     ws = pa.new_workspace(n, dev)
-    pa.decode(out, vals["q"], kc, vc, tables, lens, Hkv, b.scale, B, k_scale=ks, v_scale=vs, workspace=ws)
+    pa.decode(out, vals["q"], kc, vc, tables, lens, Hkv, b.scale, B, k_scale=ks, v_scale=vs, workspace=ws,
+              k_zero_point=kz, v_zero_point=vz)
     assert pa.get_device_error() == 0
     out_h = out.cpu().numpy().astype(np.float64)
     assert np.all(np.isfinite(out_h))
@@ -60,18 +62,21 @@ def _run_full(name, seed, *, q_mult=1.0, n_samples=12, **overrides):
         gk = to_numpy(kc.index_select(0, blocks), b.kv_fmt)
         gv = to_numpy(vc.index_select(0, blocks), b.kv_fmt)
         local_tables = np.arange(nb, dtype=np.int32)[None, :]
-        if fp8:
+        if quant:
             # the sequence's bytes must equal the oracle's quantisation of its bf16 rows
+            zkw = {}
+            if b.kv_fmt == "i8":
+                zkw = dict(k_zero_point=kz.cpu().numpy(), v_zero_point=vz.cpu().numpy())
             rows = slice(int(src_off[s]), int(src_off[s + 1]))
             kr = np.concatenate([to_numpy(vals["k_src"][rows], "bf16"), to_numpy(vals["k_new"][s:s + 1], "bf16")])
             vr = np.concatenate([to_numpy(vals["v_src"][rows], "bf16"), to_numpy(vals["v_new"][s:s + 1], "bf16")])
             zero = np.zeros_like(gk)
-            ok, ov = oracle.reshape_and_cache(kr, vr, zero, zero, np.arange(T), B, src_fmt="bf16", kv_fmt="e4m3",
-                                              k_inv_scale=kis.cpu().numpy(), v_inv_scale=vis.cpu().numpy())
-            assert bits_equal(gk, ok) and bits_equal(gv, ov), f"fp8 cache bytes of sequence {s}"
+            ok, ov = oracle.reshape_and_cache(kr, vr, zero, zero, np.arange(T), B, src_fmt="bf16", kv_fmt=b.kv_fmt,
+                                              k_inv_scale=kis.cpu().numpy(), v_inv_scale=vis.cpu().numpy(), **zkw)
+            assert bits_equal(gk, ok) and bits_equal(gv, ov), f"{b.kv_fmt} cache bytes of sequence {s}"
             ref = oracle.paged_decode_attention_one(q_h[s:s + 1], ok, ov, local_tables, np.array([T]), b.scale, B,
-                                                    0, h, q_fmt=b.q_fmt, kv_fmt="e4m3", k_scale=ks.cpu().numpy(),
-                                                    v_scale=vs.cpu().numpy(), num_kv_heads=Hkv)
+                                                    0, h, q_fmt=b.q_fmt, kv_fmt=b.kv_fmt, k_scale=ks.cpu().numpy(),
+                                                    v_scale=vs.cpu().numpy(), num_kv_heads=Hkv, **zkw)
         else:
             # the appended row landed in its slot
             kvh = h // b.group
@@ -98,3 +103,7 @@ def test_long_32k_full(q_mult):
 @pytest.mark.parametrize("B", [16, 32])
 def test_fp8_mix_full(B):
     _run_full("fp8_mix", 0, block_size=B, n_samples=10)
+
+
+def test_int8_mix_full():
+    _run_full("int8_mix", 0, n_samples=10)

@@ -75,6 +75,24 @@ def test_fp8_cache(B, qfmt):
     _check(b, workloads.host_values(b, seed=5))
 
 
+@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("qfmt", ["bf16", "f16"])
+def test_int8_cache(B, qfmt):
+    """INT8 cache (per-head scale + zero point): cache bytes bit-exact, attention within 2e-3."""
+    b = workloads.make_batch("int8_mix", seed=6, num_seqs=8, block_size=B, q_fmt=qfmt,
+                             lengths=("lognormal", 6.0, 1.0, 16, 1500))
+    _check(b, workloads.host_values(b, seed=6))
+
+
+def test_int8_split_modes_and_extreme_zero_points():
+    b = workloads.make_batch("int8_mix", seed=7, num_seqs=6, lengths=("lognormal", 6.0, 1.0, 16, 2000))
+    v = workloads.host_values(b, seed=7)
+    v["k_zero_point"] = np.array([-128, 127, 0, 5, -5, 100, -100, 1][: b.num_kv_heads], dtype=np.int32)
+    v["v_zero_point"] = np.array([127, -128, 3, -3, 64, -64, 0, 2][: b.num_kv_heads], dtype=np.int32)
+    for mode in (0, 256):
+        _check(b, v, partition_size=mode)
+
+
 def test_many_short_sequences_cross_warp_ranges():
     b = workloads.make_batch("gqa_32x4k", seed=6, num_seqs=300, lengths=("uniform", 1, 60))
     _check(b, workloads.host_values(b, seed=6))

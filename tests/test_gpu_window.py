@@ -55,6 +55,12 @@ def test_window_fp8(B, W):
     _check(b, workloads.host_values(b, seed=42), W)
 
 
+@pytest.mark.parametrize("W", [9, 200])
+def test_window_int8(W):
+    b = workloads.make_batch("int8_mix", seed=46, num_seqs=10)
+    _check(b, workloads.host_values(b, seed=46), W)
+
+
 def test_window_long_extreme_logits():
     b = workloads.make_batch("long_32k", seed=43, num_seqs=2, lengths=("const", 5000))
     _check(b, workloads.host_values(b, seed=43, q_mult=30.0), 777)

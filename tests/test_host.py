@@ -95,6 +95,28 @@ def test_decode_ex_options_validation(lib):
     assert _decode_ex(pa.DecodeOptions(window=3), Hq=30) == pa.PA_ERR_SHAPE
     assert _decode_ex(pa.DecodeOptions(window=3), B=12) == pa.PA_ERR_UNSUPPORTED
     assert ctypes.sizeof(pa.DecodeOptions) >= 12
+    # INT8 caches need scales and zero points
+    assert _decode_ex(None, kv_dtype=pa.PA_INT8, ks=A, vs=A) == pa.PA_ERR_NULL
+    assert _decode_ex(pa.DecodeOptions(k_zero_point=0x10000, v_zero_point=0x20000), kv_dtype=pa.PA_INT8) == \
+        pa.PA_ERR_NULL
+    assert _decode_ex(pa.DecodeOptions(k_zero_point=0x10000, v_zero_point=0x20000), kv_dtype=pa.PA_INT8, ks=A,
+                      vs=A, D=64, q_stride=32 * 64) == pa.PA_ERR_UNSUPPORTED
+
+
+def test_cache_write_int8_validation(lib):
+    def rc(opt, **kw):
+        a = dict(k=A, v=A2, src=pa.PA_BF16, ks=8 * 128, vs=8 * 128, kc=A, vc=A2, kv=pa.PA_INT8, nb=10, sm=A, N=3,
+                 Hkv=8, D=128, B=16, ki=A, vi=A)
+        a.update(kw)
+        return pa.pa_reshape_and_cache_ex(a["k"], a["v"], a["src"], a["ks"], a["vs"], a["kc"], a["vc"], a["kv"],
+                                          a["nb"], a["sm"], a["N"], a["Hkv"], a["D"], a["B"], a["ki"], a["vi"],
+                                          None if opt is None else ctypes.byref(opt), None)
+    assert rc(None) == pa.PA_ERR_NULL                      # zero points required
+    assert rc(pa.CacheWriteOptions(k_zero_point=0x10000, v_zero_point=0x20000), ki=None) == pa.PA_ERR_NULL
+    bad = pa.CacheWriteOptions(k_zero_point=0x10000, v_zero_point=0x20000)
+    bad.struct_size = 0
+    assert rc(bad) == pa.PA_ERR_SHAPE
+    assert rc(pa.CacheWriteOptions(k_zero_point=0x10000, v_zero_point=0x20000), N=0) == pa.PA_OK
 
 
 def _rc(**kw):

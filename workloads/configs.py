@@ -23,6 +23,10 @@ WORKLOADS = {
     "fp8_mix": dict(num_seqs=256, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                     q_fmt="bf16", kv_fmt="e4m3", scale=1.0 / math.sqrt(128.0),
                     lengths=("lognormal", 7.0, 1.0, 16, 8192), pool=("slack", 0.10)),
+    # the fp8_mix batch with an INT8 cache (per-head scale and zero point)
+    "int8_mix": dict(num_seqs=256, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                     q_fmt="bf16", kv_fmt="i8", scale=1.0 / math.sqrt(128.0),
+                     lengths=("lognormal", 7.0, 1.0, 16, 8192), pool=("slack", 0.10)),
 }
 
 
@@ -182,6 +186,30 @@ def fp8_scales_from_amax(amax: np.ndarray):
     return scale, inv
 
 
+def int8_params_from_range(mn: np.ndarray, mx: np.ndarray):
+    """Per-head INT8 calibration from the value range: scale = (max - min) / 255 (float32),
+    zero point = clamp(round(-128 - min / scale), -128, 127) (int32), inv = 1 / scale (float32)."""
+    mn = np.asarray(mn, dtype=np.float32)
+    mx = np.asarray(mx, dtype=np.float32)
+    scale = ((mx - mn) / np.float32(255.0)).astype(np.float32)
+    scale = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    zp = np.clip(np.round(-128.0 - mn.astype(np.float64) / scale.astype(np.float64)), -128, 127).astype(np.int32)
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    return scale, zp, inv
+
+
+def _bf16_range_per_head(*arrays):
+    """(min, max) per KV head (axis 1) over bf16-bit arrays [N, H_kv, d], via torch."""
+    import torch
+    lo = hi = None
+    for a in arrays:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).float()
+        a_lo, a_hi = t.amin(dim=(0, 2)), t.amax(dim=(0, 2))
+        lo = a_lo if lo is None else torch.minimum(lo, a_lo)
+        hi = a_hi if hi is None else torch.maximum(hi, a_hi)
+    return lo.numpy().astype(np.float32), hi.numpy().astype(np.float32)
+
+
 def _bf16_amax_per_head(*arrays) -> np.ndarray:
     """max |x| per KV head (axis 1) over bf16-bit arrays [N, H_kv, d], via torch."""
     import torch
@@ -224,7 +252,7 @@ def host_values(batch: DecodeBatch, seed: int = 0, *, q_mult: float = 1.0, nan_t
         out["k_cache"], out["v_cache"] = k, v
         out["k_new"] = _normal_storage(rng, (S, Hkv, d), batch.kv_fmt)
         out["v_new"] = _normal_storage(rng, (S, Hkv, d), batch.kv_fmt)
-    elif batch.kv_fmt == "e4m3":
+    elif batch.kv_fmt in ("e4m3", "i8"):
         slots = batch.cached_slots()
         n = len(slots)
         ks32 = rng.standard_normal(size=(n, Hkv, d), dtype=np.float32)
@@ -235,10 +263,15 @@ def host_values(batch: DecodeBatch, seed: int = 0, *, q_mult: float = 1.0, nan_t
         knb, vnb = bf16_bits_from_f32(kn32), bf16_bits_from_f32(vn32)
         out["k_src"], out["v_src"], out["src_slots"] = kb, vb, slots
         out["k_new"], out["v_new"] = knb, vnb
-        out["k_scale"], out["k_inv_scale"] = fp8_scales_from_amax(_bf16_amax_per_head(kb, knb))
-        out["v_scale"], out["v_inv_scale"] = fp8_scales_from_amax(_bf16_amax_per_head(vb, vnb))
-        out["k_cache"] = np.zeros((NB, Hkv, B, d), dtype=np.uint8)
-        out["v_cache"] = np.zeros((NB, Hkv, B, d), dtype=np.uint8)
+        if batch.kv_fmt == "e4m3":
+            out["k_scale"], out["k_inv_scale"] = fp8_scales_from_amax(_bf16_amax_per_head(kb, knb))
+            out["v_scale"], out["v_inv_scale"] = fp8_scales_from_amax(_bf16_amax_per_head(vb, vnb))
+        else:
+            out["k_scale"], out["k_zero_point"], out["k_inv_scale"] = int8_params_from_range(*_bf16_range_per_head(kb, knb))
+            out["v_scale"], out["v_zero_point"], out["v_inv_scale"] = int8_params_from_range(*_bf16_range_per_head(vb, vnb))
+        cdt = np.uint8 if batch.kv_fmt == "e4m3" else np.int8
+        out["k_cache"] = np.zeros((NB, Hkv, B, d), dtype=cdt)
+        out["v_cache"] = np.zeros((NB, Hkv, B, d), dtype=cdt)
     else:
         raise ValueError(batch.kv_fmt)
     return out
@@ -279,13 +312,20 @@ def device_values(batch: DecodeBatch, seed: int, device, *, q_mult: float = 1.0)
         out["v_new"] = randn((S, Hkv, d), "bf16")
         out["src_slots"] = torch.from_numpy(slots).to(device)
         for kv in ("k", "v"):
-            a = torch.maximum(out[f"{kv}_src"].float().abs().amax(dim=(0, 2)),
-                              out[f"{kv}_new"].float().abs().amax(dim=(0, 2)))
-            sc, inv = fp8_scales_from_amax(a.cpu().numpy())
+            src, new = out[f"{kv}_src"].float(), out[f"{kv}_new"].float()
+            if batch.kv_fmt == "e4m3":
+                a = torch.maximum(src.abs().amax(dim=(0, 2)), new.abs().amax(dim=(0, 2)))
+                sc, inv = fp8_scales_from_amax(a.cpu().numpy())
+            else:
+                lo = torch.minimum(src.amin(dim=(0, 2)), new.amin(dim=(0, 2)))
+                hi = torch.maximum(src.amax(dim=(0, 2)), new.amax(dim=(0, 2)))
+                sc, zp, inv = int8_params_from_range(lo.cpu().numpy(), hi.cpu().numpy())
+                out[f"{kv}_zero_point"] = torch.from_numpy(zp).to(device)
             out[f"{kv}_scale"] = torch.from_numpy(sc).to(device)
             out[f"{kv}_inv_scale"] = torch.from_numpy(inv).to(device)
-        out["k_cache"] = torch.zeros((NB, Hkv, B, d), dtype=torch.uint8, device=device)
-        out["v_cache"] = torch.zeros((NB, Hkv, B, d), dtype=torch.uint8, device=device)
+        cdt = torch.uint8 if batch.kv_fmt == "e4m3" else torch.int8
+        out["k_cache"] = torch.zeros((NB, Hkv, B, d), dtype=cdt, device=device)
+        out["v_cache"] = torch.zeros((NB, Hkv, B, d), dtype=cdt, device=device)
     return out
 
 
