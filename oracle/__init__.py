@@ -32,6 +32,7 @@ from .attention import (
     dense_decode_attention,
     paged_decode_attention,
     paged_decode_attention_one,
+    paged_append_decode,
     dequantize_kv,
 )
 from .online_softmax import online_softmax_attention, merge_partials, partial_state

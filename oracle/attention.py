@@ -152,3 +152,32 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, b
                 h = kvh * G + g
                 out[s, h] = dense_decode_attention(qf[s, h], K, V, sc)
     return out
+
+
+def paged_append_decode(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, scale, block_size, *,
+                        q_fmt="f16", src_fmt="f16", kv_fmt="f16", k_scale=None, v_scale=None,
+                        k_inv_scale=None, v_inv_scale=None, k_zero_point=None, v_zero_point=None, window=0):
+    """Append + decode in one step: the rows k_new[s], v_new[s] of position seq_lens[s]-1 are written to
+    the slot that position maps to through the block table (the cache write of ``cache_ops``), then every
+    sequence attends over its seq_lens[s] rows (including the new one).
+
+    [P2] §"PagedAttention: OS仮想メモリ式の管理": a new token's K and V go into the slot of its position;
+    [P1] §"Attention計算": the query then attends over all cached rows.  Returns (out, k_cache, v_cache).
+    """
+    from .cache_ops import reshape_and_cache
+    S = q.shape[0]
+    slots = []
+    for s in range(S):
+        T = int(seq_lens[s])
+        if T <= 0:
+            slots.append(-1)
+            continue
+        p = T - 1
+        slots.append(int(block_tables[s][p // block_size]) * block_size + p % block_size)
+    kc, vc = reshape_and_cache(k_new, v_new, k_cache, v_cache, slots, block_size, src_fmt=src_fmt, kv_fmt=kv_fmt,
+                               k_inv_scale=k_inv_scale, v_inv_scale=v_inv_scale, k_zero_point=k_zero_point,
+                               v_zero_point=v_zero_point)
+    out = paged_decode_attention(q, kc, vc, block_tables, seq_lens, scale, block_size, q_fmt=q_fmt, kv_fmt=kv_fmt,
+                                 k_scale=k_scale, v_scale=v_scale, window=window, k_zero_point=k_zero_point,
+                                 v_zero_point=v_zero_point)
+    return out, kc, vc

@@ -718,3 +718,32 @@ def test_int8_attention_equals_float_cache_of_same_values():
                                       v_scale=vs, k_zero_point=kz, v_zero_point=vz)
     b = oracle.paged_decode_attention(q, kf, vf, tables, lens, 0.5, 4)
     assert np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------- fused append + decode
+
+def test_append_decode_single_token_returns_new_row():
+    """T = 1: the only row attended is the appended one, so out = v_new exactly (whatever the cache held)."""
+    rng = np.random.default_rng(33)
+    q, kc, vc, tables, _ = _tiny_paged(rng, 3, 4, 2, 8, 4, 12)
+    kc[:] = np.nan
+    vc[:] = np.nan
+    lens = np.ones(3, dtype=np.int32)
+    kn = rng.standard_normal((3, 2, 8)).astype(np.float16)
+    vn = rng.standard_normal((3, 2, 8)).astype(np.float16)
+    out, k2, v2 = oracle.paged_append_decode(q, kn, vn, kc, vc, tables, lens, 0.5, 4)
+    for s in range(3):
+        for h in range(4):
+            assert np.array_equal(out[s, h], vn[s, h // 2].astype(np.float64))
+        assert np.array_equal(k2[tables[s][0], :, 0], kn[s]) and np.array_equal(v2[tables[s][0], :, 0], vn[s])
+
+
+def test_append_decode_writes_only_the_newest_slot():
+    rng = np.random.default_rng(34)
+    q, kc, vc, tables, lens = _tiny_paged(rng, 4, 4, 2, 8, 4, 30)
+    kn = rng.standard_normal((4, 2, 8)).astype(np.float16)
+    vn = rng.standard_normal((4, 2, 8)).astype(np.float16)
+    _, k2, v2 = oracle.paged_append_decode(q, kn, vn, kc, vc, tables, lens, 0.5, 4)
+    changed = np.argwhere(np.any(k2 != kc, axis=(1, 3)) | np.any(v2 != vc, axis=(1, 3)))
+    want = {(int(tables[s][(int(lens[s]) - 1) // 4]), (int(lens[s]) - 1) % 4) for s in range(4)}
+    assert {(int(b), int(r)) for b, r in changed} <= want
