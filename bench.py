@@ -339,6 +339,17 @@ def run_ours(args):
 
     def step(i, ev=None):
         kc, vc = caches[i % replicas]
+        if args.fused:
+            # one launch: the cache write of the new rows fused into the decode
+            if ev is not None:
+                ev[0].record(stream)
+            pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
+                      partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
+                      k_zero_point=kz, v_zero_point=vz, k_new=k_new, v_new=v_new, k_inv_scale=kis,
+                      v_inv_scale=vis)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
                              v_zero_point=vz, stream=stream)
         pa.copy_blocks(kc, vc, no_pairs, stream=stream)          # no shared block is written: no launch
@@ -397,11 +408,17 @@ def run_ours(args):
             for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_tables, h_tables),
                          (d_lens, h_lens)):
                 d.copy_(h, non_blocking=True)
-            pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
-                                 v_zero_point=vz, stream=stream)
-            pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                      partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                      k_zero_point=kz, v_zero_point=vz)
+            if args.fused:
+                pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
+                          partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
+                          k_zero_point=kz, v_zero_point=vz, k_new=d_k, v_new=d_v, k_inv_scale=kis,
+                          v_inv_scale=vis)
+            else:
+                pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis,
+                                     k_zero_point=kz, v_zero_point=vz, stream=stream)
+                pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
+                          partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
+                          k_zero_point=kz, v_zero_point=vz)
             h_out.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -425,7 +442,8 @@ def run_ours(args):
     ms_step = elapsed_ms / K
     peaks = load_peaks()
     value = total_step_bytes / (ms_step * 1e-3) / 1e9
-    achieved = ab["decode"] / (dec_ms * 1e-3) / 1e9
+    kernel_bytes = ab["step"] if args.fused else ab["decode"]   # fused: the launch also moves the new rows
+    achieved = kernel_bytes / (dec_ms * 1e-3) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_rate(batch, {"q": q, "k_cache": caches[0][0], "v_cache": caches[0][1], "k_scale": ks,
@@ -443,7 +461,8 @@ def run_ours(args):
             "context_tokens": int(batch.seq_lens.sum()), "kv_dtype": batch.kv_fmt, "q_dtype": batch.q_fmt,
             "split": "balanced" if args.partition_size == 0 else f"fixed {args.partition_size} tokens",
             "window": args.window or None,
-            "step": "reshape_and_cache(1 new token/seq) + pa_decode",
+            "step": ("pa_decode_ex with the new token's cache write fused (one launch)" if args.fused
+                     else "reshape_and_cache(1 new token/seq) + pa_decode"),
             "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
             "seed": args.seed,
             "launch": geometry,
@@ -455,10 +474,10 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (pa_decode, one launch)",
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                     "algorithmic_bytes_per_launch": ab["decode"], "avg_launch_ms": round(dec_ms, 6),
+                     "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 6),
                      "traffic": traffic},
         "cpu_baseline": cpu,
-        "gpu_launches": 2 * K,
+        "gpu_launches": (1 if args.fused else 2) * K,
         "clocks": clocks,
     }
     if e2e is not None:
@@ -680,6 +699,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_32x4k",
                     choices=["tiny", "gqa_32x4k", "long_32k", "fp8_mix", "int8_mix", "beam_cow"])
+    ap.add_argument("--fused", action="store_true",
+                    help="one launch per step: the new token's cache write fused into pa_decode_ex")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window decode over the last W positions (bytes counted over the window)")
     ap.add_argument("--partition-size", type=int, default=0)

@@ -155,12 +155,31 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            required for kv_dtype PA_INT8 (k_scale / v_scale are then the
  *            INT8 scales), ignored otherwise ([P2] "KV量子化: FP8とINT8":
  *            INT8 KV needs a scale and a zero point).
+ *   k_new / v_new  (fused append; NULL = off)
+ *            rows [num_seqs][num_kv_heads][head_dim] of every sequence's
+ *            newest position seq_lens[s]-1, new_stride elements apart per
+ *            sequence, new_dtype F16/BF16 (== kv_dtype for 16-bit caches).
+ *            The call first stores them into the slot that position maps to
+ *            through block_tables (quantised with k_inv_scale / v_inv_scale,
+ *            and the zero points for INT8, exactly as pa_reshape_and_cache
+ *            does) and attends over all seq_lens[s] rows including them: one
+ *            launch for the cache write and the decode of a step ([P2]
+ *            "PagedAttention: OS仮想メモリ式の管理": a new token's rows go into
+ *            the slot of its position).  16-byte aligned bases,
+ *            new_stride*2 % 16 == 0.  Sequences with seq_lens[s] == 0 write
+ *            nothing.
  */
 typedef struct pa_decode_options {
   size_t struct_size;
   int32_t window;
   const int32_t* k_zero_point;
   const int32_t* v_zero_point;
+  const void* k_new;
+  const void* v_new;
+  int32_t new_dtype;
+  int64_t new_stride;
+  const float* k_inv_scale;
+  const float* v_inv_scale;
 } pa_decode_options;
 
 int pa_decode_ex(void* out, pa_dtype out_dtype,

@@ -26,7 +26,9 @@ _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctyp
 class DecodeOptions(ctypes.Structure):
     """pa_decode_options (include/pa.h); struct_size is filled in by the constructor."""
     _fields_ = [("struct_size", ctypes.c_size_t), ("window", ctypes.c_int32),
-                ("k_zero_point", ctypes.c_void_p), ("v_zero_point", ctypes.c_void_p)]
+                ("k_zero_point", ctypes.c_void_p), ("v_zero_point", ctypes.c_void_p),
+                ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("new_dtype", ctypes.c_int32),
+                ("new_stride", ctypes.c_int64), ("k_inv_scale", ctypes.c_void_p), ("v_inv_scale", ctypes.c_void_p)]
 
     def __init__(self, **kw):
         super().__init__(struct_size=ctypes.sizeof(DecodeOptions), **kw)
@@ -223,17 +225,28 @@ def new_workspace(nbytes: int, device):
 
 def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale, block_size, *,
            k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None, window=0,
-           k_zero_point=None, v_zero_point=None):
+           k_zero_point=None, v_zero_point=None, k_new=None, v_new=None, k_inv_scale=None, v_inv_scale=None):
     """out[s,h] = softmax(scale * K_s q[s,h]) V_s through the block tables (pa_decode).
 
     window > 0: sliding-window decode over the last `window` positions (pa_decode_ex).
     INT8 caches (torch.int8) take k/v scales and int32 per-KV-head zero points (pa_decode_ex).
+    k_new / v_new ([S, H_kv, d], F16/BF16): fused append -- the rows of position seq_lens[s]-1 are
+    written into their cache slots (quantised with k_inv_scale / v_inv_scale for 8-bit caches) and
+    attended in the same launch (pa_decode_ex).
     """
     for n, t in (("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
                  ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale), ("k_zero_point", k_zero_point),
-                 ("v_zero_point", v_zero_point)):
+                 ("v_zero_point", v_zero_point), ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale)):
         _require_cuda(n, t)
     _require_cuda("q", q, contiguous=False)
+    new_stride, new_dtype = 0, PA_F16
+    if k_new is not None or v_new is not None:
+        _require_cuda("k_new", k_new, contiguous=False)
+        _require_cuda("v_new", v_new, contiguous=False)
+        for t in (k_new, v_new):
+            if t.stride(2) != 1 or t.stride(1) != t.shape[2] or t.stride(0) != k_new.stride(0):
+                raise ValueError("k_new/v_new rows must be contiguous per sequence with equal strides")
+        new_stride, new_dtype = k_new.stride(0), dtype_code(k_new)
     if q.stride(2) != 1 or q.stride(1) != q.shape[2]:
         raise ValueError("q rows must be contiguous per sequence")
     S, Hq, D = q.shape
@@ -244,8 +257,10 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
             _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
             S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
             _ptr(workspace), ws_bytes)
-    if window or k_zero_point is not None or v_zero_point is not None:
-        opt = DecodeOptions(window=int(window), k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point))
+    if window or k_zero_point is not None or v_zero_point is not None or k_new is not None:
+        opt = DecodeOptions(window=int(window), k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point),
+                            k_new=_ptr(k_new), v_new=_ptr(v_new), new_dtype=new_dtype, new_stride=new_stride,
+                            k_inv_scale=_ptr(k_inv_scale), v_inv_scale=_ptr(v_inv_scale))
         st = pa_decode_ex(*args, ctypes.byref(opt), _stream(stream))
         _check("pa_decode_ex", st)
     else:

@@ -141,7 +141,8 @@ struct DecodePlan {
 // Resolves the variant, launch geometry and workspace need.  `have_ws` tells
 // whether the caller supplied a workspace (balanced mode needs one).
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
-              int partition_size, int q_dtype, int kv_dtype, bool have_ws, DecodePlan* plan) {
+              int partition_size, int q_dtype, int kv_dtype, bool have_ws, DecodePlan* plan, bool append = false) {
+  plan->key.append = append ? 1 : 0;
   plan->key.q_dtype = q_dtype;
   plan->key.kv_dtype = kv_dtype;
   plan->key.head_dim = head_dim;
@@ -240,6 +241,16 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
     memcpy(&o, opt, opt->struct_size < sizeof(o) ? opt->struct_size : sizeof(o));
   }
   if (o.window < 0) return PA_ERR_SHAPE;
+  const bool append = o.k_new != nullptr || o.v_new != nullptr;
+  if (append) {
+    if (!o.k_new || !o.v_new) return PA_ERR_NULL;
+    if (o.new_dtype != PA_F16 && o.new_dtype != PA_BF16) return PA_ERR_DTYPE;
+    const bool q8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8;
+    if (!q8 && o.new_dtype != kv_dtype) return PA_ERR_DTYPE;
+    if (q8 && (!o.k_inv_scale || !o.v_inv_scale)) return PA_ERR_NULL;
+    if (o.new_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return PA_ERR_SHAPE;
+    if (!aligned16(o.k_new) || !aligned16(o.v_new) || (o.new_stride * 2) % 16 != 0) return PA_ERR_ALIGN;
+  }
   const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                     partition_size, kv_dtype);
   if (sh != PA_OK) return sh;
@@ -257,7 +268,7 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   DecodePlan plan;
   const bool have_ws = workspace != nullptr && workspace_bytes > 0;
   const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                           partition_size, q_dtype, kv_dtype, have_ws, &plan);
+                           partition_size, q_dtype, kv_dtype, have_ws, &plan, append);
   if (pr != PA_OK) return pr;
   if (plan.bytes > 0 && (!have_ws || workspace_bytes < plan.bytes || !aligned16(workspace))) return PA_ERR_WORKSPACE;
 
@@ -293,6 +304,15 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.block_shift = __builtin_ctz(static_cast<unsigned>(block_size));
   p.partition_units = plan.partition_units;
   p.window = o.window;
+  p.k_new = append ? o.k_new : nullptr;
+  p.v_new = append ? o.v_new : nullptr;
+  p.new_stride = o.new_stride;
+  p.new_dtype = o.new_dtype;
+  p.k_inv_scale = o.k_inv_scale;
+  p.v_inv_scale = o.v_inv_scale;
+  p.k_cache = const_cast<void*>(k_cache);
+  p.v_cache = const_cast<void*>(v_cache);
+  p.stage_bytes = plan.geo.stage_bytes;
   p.stages = plan.geo.stages;
   p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)

@@ -24,15 +24,6 @@ namespace {
 
 enum CacheMode { kCopy = 0, kToFp8 = 1, kToInt8 = 2 };
 
-// float32 y (= x * inv_scale, already rounded to float32) -> INT8 code:
-// nearest integer (ties to even) plus the zero point, saturated to the int8
-// range; NaN saturates upward.
-__device__ __forceinline__ int int8_code(float y, int zp) {
-  if (y != y) return 127;
-  const float r = rintf(y) + static_cast<float>(zp);
-  return static_cast<int>(fminf(fmaxf(r, -128.f), 127.f));
-}
-
 template <typename SRC, int MODE, int D>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const void* __restrict__ k, const void* __restrict__ v, int64_t k_stride, int64_t v_stride,

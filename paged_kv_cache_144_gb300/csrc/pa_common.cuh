@@ -259,6 +259,10 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return r;
 }
 
+__device__ __forceinline__ void st_shared_s32(uint32_t addr, int v) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void sts128_zero(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
@@ -298,6 +302,20 @@ __device__ __forceinline__ void widen4<i8_t>(uint32_t w, uint32_t zp2, uint32_t&
   const uint32_t b = prmt(u, 0x64646464u, 0x7362u);
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(zp2));
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(zp2));
+}
+
+// float32 y (= x * inv_scale, already rounded to float32) -> INT8 code:
+// nearest integer (ties to even) plus the zero point, saturated to the int8
+// range; NaN saturates upward.
+__device__ __forceinline__ int int8_code(float y, int zp) {
+  if (y != y) return 127;
+  const float r = rintf(y) + static_cast<float>(zp);
+  return static_cast<int>(fminf(fmaxf(r, -128.f), 127.f));
+}
+
+// Two float32 products -> two e4m3 codes (low byte = first), RNE, saturating.
+__device__ __forceinline__ uint32_t e4m3x2_code(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
 // (lo, hi) fp32 -> packed 16-bit pair, round to nearest even; lo in the low half.

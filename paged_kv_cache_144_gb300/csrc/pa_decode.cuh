@@ -90,6 +90,11 @@ struct DecodeTraits {
   static constexpr int TILE = UR * ROW;          // bytes of one unit of K (or V)
   static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
   static constexpr int STAGE = align_up_c(2 * TILE + QRAW, 1024);  // K tile + V tile + raw q
+  // fused append: each stage can also stage the new K and V rows (16-bit
+  // source format) and the physical block that receives them
+  static constexpr int OFF_NEW = 2 * TILE + QRAW;
+  static constexpr int NEWB = 2 * D * 2 + 16;
+  static constexpr int STAGE_APPEND = align_up_c(2 * TILE + QRAW + NEWB, 1024);
   static constexpr int MAX_NS = 8;               // stages per consumer (chosen at launch, 2..MAX_NS)
   static constexpr int MAX_W = 7;                // consumer warps per CTA (with the producer: 8 warps, up to 255 registers)
   static constexpr int KS = D / 16;              // k-steps of S^T = Q K^T, m-tiles of O^T
@@ -103,7 +108,7 @@ struct DecodeTraits {
   static constexpr int OFF_EMPTY = OFF_FULL + MAX_NS * 8;
   static constexpr int OFF_STAGES = 1024;
   static_assert(OFF_EMPTY + MAX_NS * 8 <= OFF_STAGES, "barriers");
-  __host__ __device__ static constexpr int warp_smem(int ns) { return OFF_STAGES + ns * STAGE; }
+  __host__ __device__ static constexpr int warp_smem(int ns, int stage) { return OFF_STAGES + ns * stage; }
   // partial record: acc as [D][GM] (head fastest), then m[GM], l[GM]
   static constexpr int REC = align_up_c(GM * (D + 2), 4);
 };
@@ -378,7 +383,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   const bool fixed = p.partition_units > 0;
 
   const int NS = p.stages;  // pipeline depth per consumer
-  const int wsm = Tr::warp_smem(NS);
+  const int STG = p.stage_bytes;
+  const int wsm = Tr::warp_smem(NS, STG);
+  const bool append = p.k_new != nullptr;
   // shared: prefix[S+1] (units before sequence s), lens[S] (clamped seq_lens),
   // scan scratch, then the producer's block-table ring (16 ints per consumer)
   int* prefix = reinterpret_cast<int*>(base + W * wsm);
@@ -517,7 +524,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           wait_since = 0;
           const bool new_frag = (it.j == it.j0);
           const uint32_t bar = cbase + Tr::OFF_FULL + 8 * pst;
-          const uint32_t kdst = cbase + Tr::OFF_STAGES + pst * Tr::STAGE;
+          const uint32_t kdst = cbase + Tr::OFF_STAGES + pst * STG;
           const uint32_t vdst = kdst + Tr::TILE;
           const int bj0 = unit_in_block ? (it.j >> upb_shift) : (it.j << bpu_shift);
           const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
@@ -538,7 +545,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             phys[i] = (i >= box0 && i < nbox) ? static_cast<int>(lds32(ring + (rs_use * 4 + i) * 4)) : 0;
           rs_use = (rs_use + 1) & 3;
           --pf;
-          mbar_arrive_expect_tx(bar, 2u * (nbox - box0) * BOX * Tr::ROW + qbytes);
+          // fused append: this unit holds position T-1; its new rows ride along
+          const bool has_new = append && it.j == ((it.T - 1) >> Tr::UR_SHIFT);
+          if (has_new) {
+            const int pb = phys[((it.T - 1) >> p.block_shift) - bj0];
+            st_shared_s32(kdst + Tr::OFF_NEW + 4 * D, (pb >= 0 && pb < p.num_blocks) ? pb : -1);
+          }
+          const uint32_t nbytes = has_new ? static_cast<uint32_t>(4 * D) : 0u;
+          mbar_arrive_expect_tx(bar, 2u * (nbox - box0) * BOX * Tr::ROW + qbytes + nbytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             if (i >= box0 && i < nbox) {
@@ -556,6 +570,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
                                   (static_cast<int64_t>(it.s) * p.q_stride + static_cast<int64_t>(it.kvh) * G * D) * 2;
             bulk_load(kdst + 2 * Tr::TILE, qsrc, qbytes, bar);
+          }
+          if (has_new) {
+            const int64_t off = (static_cast<int64_t>(it.s) * p.new_stride + static_cast<int64_t>(it.kvh) * D) * 2;
+            bulk_load(kdst + Tr::OFF_NEW, static_cast<const uint8_t*>(p.k_new) + off, 2 * D, bar);
+            bulk_load(kdst + Tr::OFF_NEW + 2 * D, static_cast<const uint8_t*>(p.v_new) + off, 2 * D, bar);
           }
           ++issued;
           if (++pst == NS) {
@@ -769,6 +788,66 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     }
   };
 
+  // Fused append: the unit holding position T-1 carries the new K/V rows in
+  // 16-bit source format.  Lanes convert them to the cache format (a copy, or
+  // the cache write's quantisation for 8-bit caches), overwrite the stale
+  // row of the tile and store the row into its cache slot.  Each unit is
+  // processed by exactly one warp, so nothing else reads that slot here.
+  auto append_row = [&](int st) {
+    uint8_t* stage = const_cast<uint8_t*>(wbase) + Tr::OFF_STAGES + st * STG;
+    const uint8_t* staged = stage + Tr::OFF_NEW;
+    const int pos = it.T - 1;
+    const int r = pos - it.j * UR;
+    const int pb = *reinterpret_cast<const int*>(staged + 4 * D);
+    constexpr int CH = Tr::ROW / 16;  // 16-byte chunks of a cache row
+    if (lane < 2 * CH) {
+      const int which = lane / CH, ch = lane % CH;  // 0: K, 1: V
+      uint4 w;
+      if constexpr (!k8bit) {
+        w = *reinterpret_cast<const uint4*>(staged + which * 2 * D + ch * 16);
+      } else {
+        // 16 source values -> 16 cache bytes
+        const uint4* src = reinterpret_cast<const uint4*>(staged + which * 2 * D + ch * 32);
+        const uint4 a = src[0], b = src[1];
+        const uint32_t pairs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const float inv = __ldg((which ? p.v_inv_scale : p.k_inv_scale) + it.kvh);
+        int zp = 0;
+        if constexpr (std::is_same<KVT, i8_t>::value) zp = __ldg((which ? p.v_zero_point : p.k_zero_point) + it.kvh);
+        uint32_t out4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float2 x0, x1;
+          if (p.new_dtype == PA_BF16) {
+            x0 = widen2<bf16_t>(pairs[2 * i]);
+            x1 = widen2<bf16_t>(pairs[2 * i + 1]);
+          } else {
+            x0 = widen2<f16_t>(pairs[2 * i]);
+            x1 = widen2<f16_t>(pairs[2 * i + 1]);
+          }
+          const float y0 = __fmul_rn(x0.x, inv), y1 = __fmul_rn(x0.y, inv);
+          const float y2 = __fmul_rn(x1.x, inv), y3 = __fmul_rn(x1.y, inv);
+          if constexpr (std::is_same<KVT, i8_t>::value) {
+            out4[i] = (static_cast<uint32_t>(int8_code(y0, zp)) & 0xffu) |
+                      ((static_cast<uint32_t>(int8_code(y1, zp)) & 0xffu) << 8) |
+                      ((static_cast<uint32_t>(int8_code(y2, zp)) & 0xffu) << 16) |
+                      ((static_cast<uint32_t>(int8_code(y3, zp)) & 0xffu) << 24);
+          } else {
+            out4[i] = e4m3x2_code(y0, y1) | (e4m3x2_code(y2, y3) << 16);
+          }
+        }
+        w = make_uint4(out4[0], out4[1], out4[2], out4[3]);
+      }
+      *reinterpret_cast<uint4*>(stage + which * Tr::TILE + chunk_off(r, ch)) = w;
+      if (pb >= 0) {
+        const int64_t crow = (static_cast<int64_t>(pb) * Hkv + it.kvh) * B + (pos & (B - 1));
+        uint8_t* cache = static_cast<uint8_t*>(which ? p.v_cache : p.k_cache);
+        *reinterpret_cast<uint4*>(cache + crow * Tr::ROW + ch * 16) = w;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
+    __syncwarp();
+  };
+
   while (it.valid) {
     // ---- one fragment: units j0 .. jend-1 of segment (s, kvh)
     if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
@@ -777,7 +856,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     }
     {
       // the query group rode on the fragment's first stage
-      const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * Tr::STAGE + 2 * Tr::TILE;
+      const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * STG + 2 * Tr::TILE;
       const bool row_ok = gid < G;
 #pragma unroll
       for (int s = 0; s < Tr::KS; ++s) {
@@ -812,7 +891,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     for (int i = 0; i < Tr::KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     bool timed_out = false;
     for (;;) {
-      const uint32_t stage_u32 = wbase_u32 + Tr::OFF_STAGES + cst * Tr::STAGE;
+      const uint32_t stage_u32 = wbase_u32 + Tr::OFF_STAGES + cst * STG;
+      if (append && it.j == ((it.T - 1) >> Tr::UR_SHIFT)) append_row(cst);
       const int n_valid = min(UR, it.T - it.j * UR);
       const int lo_rel = it.lo - it.j * UR;  // positions before the window (> 0 only in its first unit)
       if (n_valid == UR && lo_rel <= 0) {
@@ -921,8 +1001,8 @@ template <typename QT, typename KVT, int D, int GM, int UR>
 struct DecodeVariant {
   using Tr = DecodeTraits<QT, KVT, D, GM, UR>;
 
-  static size_t smem_bytes(int num_seqs, int warps, int stages) {
-    return 1024 + static_cast<size_t>(warps) * Tr::warp_smem(stages) +
+  static size_t smem_bytes(int num_seqs, int warps, int stages, int stage) {
+    return 1024 + static_cast<size_t>(warps) * Tr::warp_smem(stages, stage) +
            static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1) * 4, 16)) + static_cast<size_t>(warps) * 64;
   }
 
@@ -931,7 +1011,7 @@ struct DecodeVariant {
   // kStageBytesPerWarp of K/V per consumer; the consumers per CTA maximise
   // resident consumer warps per SM (ties: more per CTA, i.e. fewer producer
   // warps).  PA_DECODE_STAGES / PA_DECODE_WARPS override both (tuning).
-  static bool geometry(int num_seqs, DecodeGeometry* g) {
+  static bool geometry(int num_seqs, int append, DecodeGeometry* g) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     int sms = 0, optin = 0;
@@ -941,7 +1021,8 @@ struct DecodeVariant {
     // allow every size the device allows, once: geometries of other batch
     // sizes are cached and launched later without touching the attribute
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess) return false;
-    int ns = kStageBytesPerWarp / Tr::STAGE;
+    const int stage = append ? Tr::STAGE_APPEND : Tr::STAGE;
+    int ns = kStageBytesPerWarp / stage;
     ns = ns < 2 ? 2 : (ns > Tr::MAX_NS ? Tr::MAX_NS : ns);
     const int env_ns = tuning_override("PA_DECODE_STAGES");
     if (env_ns >= 2 && env_ns <= Tr::MAX_NS) ns = env_ns;
@@ -949,7 +1030,7 @@ struct DecodeVariant {
     int best_w = 0, best_occ = 0, best_warps = 0;
     for (int w = 1; w <= Tr::MAX_W; ++w) {
       if (env_w > 0 && w != env_w) continue;
-      const size_t smem = smem_bytes(num_seqs, w, ns);
+      const size_t smem = smem_bytes(num_seqs, w, ns, stage);
       if (smem > static_cast<size_t>(optin)) break;
       int occ = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (w + 1) * 32, smem) != cudaSuccess) return false;
@@ -960,8 +1041,9 @@ struct DecodeVariant {
       }
     }
     if (best_w == 0) return false;
-    const size_t smem = smem_bytes(num_seqs, best_w, ns);
+    const size_t smem = smem_bytes(num_seqs, best_w, ns, stage);
     g->warps_per_cta = best_w;
+    g->stage_bytes = stage;
     g->stages = ns;
     g->ctas = sms * best_occ;
     g->smem_bytes = smem;

@@ -42,14 +42,14 @@
 // dispatcher sees only the declarations, so every kernel is instantiated and
 // registered in exactly one translation unit.
 #define PA_DECLARE_VARIANT(QT, KVT, D, GM, UR)                                                   \
-  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(int num_seqs, DecodeGeometry* geo);      \
+  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(int num_seqs, int append, DecodeGeometry* geo); \
   cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR(const DecodeGeometry& geo,           \
                                                               const DecodeParams& p,              \
                                                               const CUtensorMap& tk,              \
                                                               const CUtensorMap& tv, cudaStream_t stream);
 #define PA_DEFINE_VARIANT(QT, KVT, D, GM, UR)                                                      \
-  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(int num_seqs, DecodeGeometry* geo) {      \
-    return DecodeVariant<QT, KVT, D, GM, UR>::geometry(num_seqs, geo);                             \
+  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(int num_seqs, int append, DecodeGeometry* geo) { \
+    return DecodeVariant<QT, KVT, D, GM, UR>::geometry(num_seqs, append, geo);                     \
   }                                                                                                \
   cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR(const DecodeGeometry& geo,           \
                                                               const DecodeParams& p,              \

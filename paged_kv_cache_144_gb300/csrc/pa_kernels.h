@@ -65,6 +65,16 @@ struct DecodeParams {
   int block_shift;              // log2(block_size)
   int partition_units;          // 0: balanced split; >0: fixed partitions of this many units
   int window;                   // > 0: attend to the last `window` positions only; 0: all
+  // fused append (k_new == nullptr: off): the rows of position seq_len-1
+  const void* k_new;            // [num_seqs][num_kv_heads][head_dim] at new_stride elements per sequence
+  const void* v_new;
+  int64_t new_stride;
+  int new_dtype;                // PA_F16 / PA_BF16
+  const float* k_inv_scale;     // 8-bit caches: the cache write's multipliers
+  const float* v_inv_scale;
+  void* k_cache;                // pools, for storing the appended rows
+  void* v_cache;
+  int stage_bytes;              // bytes of one pipeline stage (DecodeGeometry::stage_bytes)
   float* part_records;          // split-K partial records (workspace)
   int* seg_counters;            // [num_seqs * num_kv_heads] arrival counters (workspace)
   unsigned int* err;            // per-device error word
@@ -78,6 +88,7 @@ struct DecodeKey {
   int head_dim;   // 64 / 128
   int gmax;       // 1 / 4 / 8 (query heads per KV head, rounded up)
   int unit_rows;  // 16 / 32 / 64 rows per work unit
+  int append;     // 1: fused append (each stage also stages the new K/V rows)
 };
 
 // Launch geometry of one variant on the current device.
@@ -87,12 +98,13 @@ struct DecodeGeometry {
   int ctas;            // resident CTAs over the whole device
   size_t smem_bytes;   // dynamic shared memory per CTA
   int record_floats;   // floats per partial record
+  int stage_bytes;     // bytes of one pipeline stage
   int unit_rows;       // rows per work unit (TMA box height = min(unit_rows, block_size))
 };
 
 // Fills `geo` for `key` and `num_seqs` on the current device; false if the
 // variant is not compiled in or the device cannot run it.
-bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo);
+bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo);  // key.append selects the stage size
 
 // Geometry and kernel attributes of the last rejected decode launch on this thread.
 const char* launch_failure_note();
