@@ -33,6 +33,7 @@ from .attention import (
     paged_decode_attention,
     paged_decode_attention_one,
     paged_append_decode,
+    paged_multi_query_attention,
     dequantize_kv,
 )
 from .online_softmax import online_softmax_attention, merge_partials, partial_state

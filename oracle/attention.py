@@ -29,6 +29,12 @@ Readings where the pages are silent (each also listed in the design doc):
     float64(scale[h]), one float32 scale and one integer zero point per KV
     head, separately for K and V (codec in ``codecs``).
   * a sequence of length 0 attends to nothing; its output is defined as 0.
+  * several queries per sequence (the explainer's related-work and outlook
+    sections tie paged KV memory to speculative decoding, which verifies a
+    few proposed tokens in one step; no formula is given): with q_len = L,
+    the L newest positions T-L .. T-1 of a sequence are queries and query i
+    attends to the positions up to and including its own, T-L+i (causal
+    among the new tokens, all older rows visible).
   * sliding window (named as a limitation of the paged kernel in the
     "局限性与未来工作" list of the dihengye.cn notes, no definition given):
     with a window W > 0 the single query of a sequence of length T, which sits
@@ -181,3 +187,34 @@ def paged_append_decode(q, k_new, v_new, k_cache, v_cache, block_tables, seq_len
                                  k_scale=k_scale, v_scale=v_scale, window=window, k_zero_point=k_zero_point,
                                  v_zero_point=v_zero_point)
     return out, kc, vc
+
+
+def paged_multi_query_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size, *,
+                                q_fmt="f16", kv_fmt="f16", k_scale=None, v_scale=None, window=0,
+                                k_zero_point=None, v_zero_point=None):
+    """out[S, L, H_q, d]: query i of sequence s (position T-L+i) attends to positions
+    max(0, T-L+i-W+1) .. T-L+i (W = window, 0 = no lower bound).  q is [S, L, H_q, d]."""
+    S, L, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    if Hq % Hkv != 0:
+        raise ValueError("H_q must be a multiple of H_kv")
+    G = Hq // Hkv
+    Kc = dequantize_kv(k_cache, kv_fmt, k_scale, k_zero_point)
+    Vc = dequantize_kv(v_cache, kv_fmt, v_scale, v_zero_point)
+    qf = storage_to_f64(q, q_fmt)
+    sc = _scale64(scale)
+    out = np.zeros((S, L, Hq, d), dtype=np.float64)
+    for s in range(S):
+        T = int(seq_lens[s])
+        for kvh in range(Hkv):
+            K = gather_sequence(Kc, block_tables[s], T, block_size, kvh)
+            V = gather_sequence(Vc, block_tables[s], T, block_size, kvh)
+            for i in range(L):
+                pos = T - L + i
+                if pos < 0:
+                    continue            # the sequence is shorter than its query count: nothing to attend
+                lo = max(0, pos - window + 1) if window and window > 0 else 0
+                for g in range(G):
+                    h = kvh * G + g
+                    out[s, i, h] = dense_decode_attention(qf[s, i, h], K[lo:pos + 1], V[lo:pos + 1], sc)
+    return out

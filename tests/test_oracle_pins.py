@@ -747,3 +747,77 @@ def test_append_decode_writes_only_the_newest_slot():
     changed = np.argwhere(np.any(k2 != kc, axis=(1, 3)) | np.any(v2 != vc, axis=(1, 3)))
     want = {(int(tables[s][(int(lens[s]) - 1) // 4]), (int(lens[s]) - 1) % 4) for s in range(4)}
     assert {(int(b), int(r)) for b, r in changed} <= want
+
+
+# ----------------------------------------------------------------------------- several queries per sequence
+
+def _tiny_multi(rng, S, L, Hq, Hkv, d, B, max_len):
+    q1, kc, vc, tables, lens = _tiny_paged(rng, S, Hq, Hkv, d, B, max_len)
+    lens = np.maximum(lens, L).astype(np.int32)
+    nbs = -(-lens // B)
+    need = int(nbs.sum()) + 2
+    kc = rng.standard_normal((need, Hkv, B, d)).astype(np.float16)
+    vc = rng.standard_normal((need, Hkv, B, d)).astype(np.float16)
+    perm = rng.permutation(need)
+    tables = np.full((S, int(nbs.max())), -1, dtype=np.int32)
+    c = 0
+    for s in range(S):
+        tables[s, :nbs[s]] = perm[c:c + nbs[s]]
+        c += nbs[s]
+    q = rng.standard_normal((S, L, Hq, d)).astype(np.float16)
+    return q, kc, vc, tables, lens
+
+
+def test_multi_query_one_query_is_decode():
+    rng = np.random.default_rng(35)
+    q, kc, vc, tables, lens = _tiny_multi(rng, 3, 1, 4, 2, 8, 4, 30)
+    a = oracle.paged_multi_query_attention(q, kc, vc, tables, lens, 0.5, 4)
+    b = oracle.paged_decode_attention(q[:, 0], kc, vc, tables, lens, 0.5, 4)
+    assert np.array_equal(a[:, 0], b)
+
+
+def check_multi_query_prefix(fn, seed=36, window=0):
+    """Query i equals single-query decode of the same sequence cut to length T-L+i+1."""
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for L in (2, 3, 5):
+        q, kc, vc, tables, lens = _tiny_multi(rng, 3, L, 4, 2, 8, 4, 30)
+        out = fn(q, kc, vc, tables, lens, 0.5, 4, window=window)
+        for i in range(L):
+            cut = (lens - L + i + 1).astype(np.int32)
+            ref = oracle.paged_decode_attention(q[:, i], kc, vc, tables, cut, 0.5, 4, window=window)
+            worst = max(worst, float(np.max(np.abs(out[:, i] - ref))))
+    return worst
+
+
+def test_multi_query_equals_decode_of_each_prefix():
+    assert check_multi_query_prefix(oracle.paged_multi_query_attention) == 0.0
+    assert check_multi_query_prefix(oracle.paged_multi_query_attention, window=6) == 0.0
+
+
+def test_multi_query_brute_force():
+    rng = np.random.default_rng(37)
+    q, kc, vc, tables, lens = _tiny_multi(rng, 2, 3, 2, 1, 4, 2, 12)
+    out = oracle.paged_multi_query_attention(q, kc, vc, tables, lens, 0.7, 2)
+    for s in range(2):
+        T = int(lens[s])
+        for i in range(3):
+            for h in range(2):
+                rk, rv = [], []
+                for p in range(T - 3 + i + 1):
+                    blk = int(tables[s][p // 2])
+                    rk.append([float(x) for x in kc[blk, 0, p % 2]])
+                    rv.append([float(x) for x in vc[blk, 0, p % 2]])
+                ref = _brute_force_one([float(x) for x in q[s, i, h]], rk, rv, float(np.float32(0.7)))
+                assert np.max(np.abs(np.array(ref) - out[s, i, h])) <= 1e-12
+
+
+def _multi_not_causal(q, kc, vc, tables, lens, scale, B, window=0, **kw):
+    # planted: every query sees the whole sequence
+    S, L = q.shape[:2]
+    return np.stack([oracle.paged_decode_attention(q[:, i], kc, vc, tables, lens, scale, B, window=window)
+                     for i in range(L)], axis=1)
+
+
+def test_multi_query_pins_catch_planted_mistake():
+    assert check_multi_query_prefix(_multi_not_causal) > 1e-3
