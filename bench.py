@@ -42,7 +42,8 @@ METRIC = "paged-decode KV-read HBM GB/s & % of GB300 peak; decode attn tokens/s"
 UNIT = "GB/s"
 FMT_BYTES = {"f16": 2, "bf16": 2, "e4m3": 1, "i8": 1, "f32": 4}
 KERNEL_SOURCES = ["pa_common.cuh", "pa_decode.cuh", "pa_decode_variants.h", "pa_decode_dispatch.cu",
-                  "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_fp8.cu", "pa_decode_int8.cu", "pa_api.cu",
+                  "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_fp8.cu", "pa_decode_int8.cu",
+                  "pa_decode_rows16.cu", "pa_decode_append16.cu", "pa_decode_append8.cu", "pa_api.cu",
                   "pa_kernels.h"]
 WORKLOAD_TEXT = {
     "tiny": "4 seqs, cached len ~U{1..128} + 1, 4 heads MHA, d 64, B 16, fp16",

@@ -167,7 +167,18 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            "PagedAttention: OS仮想メモリ式の管理": a new token's rows go into
  *            the slot of its position).  16-byte aligned bases,
  *            new_stride*2 % 16 == 0.  Sequences with seq_lens[s] == 0 write
- *            nothing.
+ *            nothing.  Needs q_len 1.
+ *   q_len    queries per sequence (0 or 1: one).  With q_len = L the L
+ *            newest positions T-L .. T-1 of each sequence (T = seq_lens[s],
+ *            rows already in the cache) are queries: q and out are
+ *            [num_seqs][L][num_heads][head_dim] (q at q_stride >= L*num_heads*
+ *            head_dim elements per sequence, out packed) and query i attends
+ *            to positions up to its own, T-L+i (with a window: the last
+ *            `window` of them).  A query whose position is negative (T < L)
+ *            gets out = 0.  L * (num_heads / num_kv_heads) <= 16, else
+ *            PA_ERR_UNSUPPORTED.  This is the verification step of
+ *            speculative decoding, which the explainer names alongside paged
+ *            KV memory.
  */
 typedef struct pa_decode_options {
   size_t struct_size;
@@ -180,6 +191,7 @@ typedef struct pa_decode_options {
   int64_t new_stride;
   const float* k_inv_scale;
   const float* v_inv_scale;
+  int32_t q_len;
 } pa_decode_options;
 
 int pa_decode_ex(void* out, pa_dtype out_dtype,
@@ -192,6 +204,12 @@ int pa_decode_ex(void* out, pa_dtype out_dtype,
                  float scale, int block_size, int partition_size,
                  void* workspace, size_t workspace_bytes,
                  const pa_decode_options* opt, void* stream);
+
+/* Workspace bytes pa_decode_ex needs with these options (q_len changes the
+ * size of the split records); same rules as pa_decode_workspace_bytes. */
+size_t pa_decode_workspace_bytes_ex(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int max_blocks_per_seq, int partition_size,
+                                    pa_dtype kv_dtype, const pa_decode_options* opt);
 
 /*
  * pa_decode_launch_config - the launch geometry pa_decode uses for these

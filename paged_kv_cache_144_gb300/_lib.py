@@ -28,7 +28,8 @@ class DecodeOptions(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_size_t), ("window", ctypes.c_int32),
                 ("k_zero_point", ctypes.c_void_p), ("v_zero_point", ctypes.c_void_p),
                 ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("new_dtype", ctypes.c_int32),
-                ("new_stride", ctypes.c_int64), ("k_inv_scale", ctypes.c_void_p), ("v_inv_scale", ctypes.c_void_p)]
+                ("new_stride", ctypes.c_int64), ("k_inv_scale", ctypes.c_void_p), ("v_inv_scale", ctypes.c_void_p),
+                ("q_len", ctypes.c_int32)]
 
     def __init__(self, **kw):
         super().__init__(struct_size=ctypes.sizeof(DecodeOptions), **kw)
@@ -45,6 +46,8 @@ class CacheWriteOptions(ctypes.Structure):
 
 _SIGNATURES = {
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_decode_workspace_bytes_ex": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                           ctypes.POINTER(DecodeOptions)]),
     "pa_decode": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
                          _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp]),
     "pa_decode_ex": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
@@ -209,9 +212,14 @@ def _require_cuda(name, t, contiguous=True):
 
 
 def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                           partition_size=0, kv_dtype=PA_BF16) -> int:
-    n = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                                  partition_size, kv_dtype)
+                           partition_size=0, kv_dtype=PA_BF16, q_len=1) -> int:
+    if q_len > 1:
+        opt = DecodeOptions(q_len=int(q_len))
+        n = int(load().pa_decode_workspace_bytes_ex(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                    max_blocks_per_seq, partition_size, kv_dtype, ctypes.byref(opt)))
+    else:
+        n = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                      partition_size, kv_dtype)
     if n == SIZE_MAX:
         raise PagedAttnError("pa_decode_workspace_bytes", PA_ERR_SHAPE, "sizes rejected or no usable device")
     return n
@@ -239,6 +247,12 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
                  ("v_zero_point", v_zero_point), ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale)):
         _require_cuda(n, t)
     _require_cuda("q", q, contiguous=False)
+    q_len = 1
+    if q.dim() == 4:                       # [S, L, H_q, d]: several queries per sequence
+        q_len = q.shape[1]
+        if q.stride(3) != 1 or q.stride(2) != q.shape[3] or q.stride(1) != q.shape[2] * q.shape[3]:
+            raise ValueError("the queries of a sequence must be contiguous")
+        q = q.view(q.shape[0], q_len * q.shape[2], q.shape[3]) if q.is_contiguous() else q
     new_stride, new_dtype = 0, PA_F16
     if k_new is not None or v_new is not None:
         _require_cuda("k_new", k_new, contiguous=False)
@@ -250,6 +264,7 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
     if q.stride(2) != 1 or q.stride(1) != q.shape[2]:
         raise ValueError("q rows must be contiguous per sequence")
     S, Hq, D = q.shape
+    Hq //= q_len
     NB = k_cache.shape[0]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (_ptr(out), dtype_code(out), _ptr(q), dtype_code(q), q.stride(0),
@@ -257,10 +272,10 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
             _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
             S, Hq, int(num_kv_heads), D, float(scale), int(block_size), int(partition_size),
             _ptr(workspace), ws_bytes)
-    if window or k_zero_point is not None or v_zero_point is not None or k_new is not None:
+    if window or k_zero_point is not None or v_zero_point is not None or k_new is not None or q_len > 1:
         opt = DecodeOptions(window=int(window), k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point),
                             k_new=_ptr(k_new), v_new=_ptr(v_new), new_dtype=new_dtype, new_stride=new_stride,
-                            k_inv_scale=_ptr(k_inv_scale), v_inv_scale=_ptr(v_inv_scale))
+                            k_inv_scale=_ptr(k_inv_scale), v_inv_scale=_ptr(v_inv_scale), q_len=q_len)
         st = pa_decode_ex(*args, ctypes.byref(opt), _stream(stream))
         _check("pa_decode_ex", st)
     else:

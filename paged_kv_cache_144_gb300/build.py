@@ -31,6 +31,9 @@ SOURCES = [
     "pa_decode_bf16.cu",
     "pa_decode_fp8.cu",
     "pa_decode_int8.cu",
+    "pa_decode_rows16.cu",
+    "pa_decode_append16.cu",
+    "pa_decode_append8.cu",
 ]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

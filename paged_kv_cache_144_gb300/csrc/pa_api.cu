@@ -96,19 +96,23 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t num_blocks, i
   return r == CUDA_SUCCESS;
 }
 
-int gmax_for_group(int g) { return g <= 1 ? 1 : (g <= 4 ? 4 : 8); }
+// Compiled maximum of A rows (q_len * G (query, head) pairs) serving `rows`.
+int gmax_for_rows(int rows) { return rows <= 1 ? 1 : (rows <= 4 ? 4 : (rows <= 8 ? 8 : 16)); }
 
 // Rows per work unit: 32 for 16-bit caches (16 KB of K + V per stage at
-// d = 128), 64 for FP8 caches with B >= 16 (the same 16 KB per stage, half
+// d = 128), 64 for 8-bit caches with B >= 16 (the same 16 KB per stage, half
 // the refills per byte of 32 rows).  A unit spans at most four blocks, so
-// 64-row units need B >= 16.  PA_DECODE_UNIT_ROWS (16, 32; 64 for FP8)
-// overrides it (tuning).
-int unit_rows_for(int kv_dtype, int block_size) {
-  const bool fp8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8;  // 8-bit cache
-  const int env = pa::tuning_override("PA_DECODE_UNIT_ROWS");
+// 64-row units need B >= 16.  Segments with more than 8 A rows (several
+// queries per sequence) use 16-row units: their accumulators fill the
+// registers.  PA_DECODE_UNIT_ROWS (16, 32; 64 for 8-bit caches) overrides it
+// (tuning).
+int unit_rows_for(int kv_dtype, int block_size, int gmax, bool append) {
+  const bool q8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8;  // 8-bit cache
+  const int env = append ? -1 : pa::tuning_override("PA_DECODE_UNIT_ROWS");  // fused append: defaults only
   if (env == 16 || env == 32) return env;
-  if (env == 64 && fp8 && block_size >= 16) return 64;
-  return fp8 && block_size >= 16 ? 64 : 32;
+  if (env == 64 && q8 && block_size >= 16 && gmax <= 8) return 64;
+  if (gmax > 8) return 16;
+  return q8 && block_size >= 16 ? 64 : 32;
 }
 
 // Shape checks shared by pa_decode and pa_decode_workspace_bytes.
@@ -141,13 +145,15 @@ struct DecodePlan {
 // Resolves the variant, launch geometry and workspace need.  `have_ws` tells
 // whether the caller supplied a workspace (balanced mode needs one).
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
-              int partition_size, int q_dtype, int kv_dtype, bool have_ws, DecodePlan* plan, bool append = false) {
+              int partition_size, int q_dtype, int kv_dtype, bool have_ws, DecodePlan* plan, bool append = false,
+              int q_len = 1) {
   plan->key.append = append ? 1 : 0;
   plan->key.q_dtype = q_dtype;
   plan->key.kv_dtype = kv_dtype;
   plan->key.head_dim = head_dim;
-  plan->key.gmax = gmax_for_group(num_heads / num_kv_heads);
-  plan->key.unit_rows = unit_rows_for(kv_dtype, block_size);
+  // several queries per sequence are served by the 16-row variants only
+  plan->key.gmax = q_len > 1 ? 16 : gmax_for_rows(num_heads / num_kv_heads);
+  plan->key.unit_rows = unit_rows_for(kv_dtype, block_size, plan->key.gmax, append);
   if (!pa::decode_geometry(plan->key, num_seqs, &plan->geo)) return PA_ERR_UNSUPPORTED;
   const int ur = plan->geo.unit_rows;
   const int max_units = static_cast<int>((static_cast<int64_t>(max_blocks_per_seq) * block_size + ur - 1) / ur);
@@ -191,9 +197,17 @@ PA_EXPORT const char* pa_status_string(int status) {
   }
 }
 
-PA_EXPORT size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                                           int block_size, int max_blocks_per_seq, int partition_size,
-                                           pa_dtype kv_dtype) {
+PA_EXPORT size_t pa_decode_workspace_bytes_ex(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                              int block_size, int max_blocks_per_seq, int partition_size,
+                                              pa_dtype kv_dtype, const pa_decode_options* opt) {
+  pa_decode_options o;
+  memset(&o, 0, sizeof(o));
+  if (opt) {
+    if (opt->struct_size < sizeof(size_t)) return static_cast<size_t>(-1);
+    memcpy(&o, opt, opt->struct_size < sizeof(o) ? opt->struct_size : sizeof(o));
+  }
+  const int q_len = o.q_len <= 0 ? 1 : o.q_len;
+  if (num_kv_heads > 0 && q_len * (num_heads / num_kv_heads) > 16) return static_cast<size_t>(-1);
   if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                          partition_size, kv_dtype) != PA_OK)
     return static_cast<size_t>(-1);
@@ -201,9 +215,16 @@ PA_EXPORT size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return static_cast<size_t>(-1);
   DecodePlan plan;
   if (make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, partition_size, q_dtype,
-                kv_dtype, true, &plan) != PA_OK)
+                kv_dtype, true, &plan, false, q_len) != PA_OK)
     return static_cast<size_t>(-1);
   return plan.bytes;
+}
+
+PA_EXPORT size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                           int block_size, int max_blocks_per_seq, int partition_size,
+                                           pa_dtype kv_dtype) {
+  return pa_decode_workspace_bytes_ex(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                      partition_size, kv_dtype, nullptr);
 }
 
 PA_EXPORT int pa_decode_launch_config(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -240,8 +261,11 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
     if (opt->struct_size < sizeof(size_t)) return PA_ERR_SHAPE;
     memcpy(&o, opt, opt->struct_size < sizeof(o) ? opt->struct_size : sizeof(o));
   }
-  if (o.window < 0) return PA_ERR_SHAPE;
+  if (o.window < 0 || o.q_len < 0) return PA_ERR_SHAPE;
+  const int q_len = o.q_len == 0 ? 1 : o.q_len;
+  if (num_kv_heads > 0 && q_len * (num_heads / num_kv_heads) > 16) return PA_ERR_UNSUPPORTED;
   const bool append = o.k_new != nullptr || o.v_new != nullptr;
+  if (append && q_len != 1) return PA_ERR_UNSUPPORTED;
   if (append) {
     if (!o.k_new || !o.v_new) return PA_ERR_NULL;
     if (o.new_dtype != PA_F16 && o.new_dtype != PA_BF16) return PA_ERR_DTYPE;
@@ -262,13 +286,13 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   if ((kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8) && (!k_scale || !v_scale)) return PA_ERR_NULL;
   if (kv_dtype == PA_INT8 && (!o.k_zero_point || !o.v_zero_point)) return PA_ERR_NULL;
   if (num_blocks <= 0 || num_blocks * num_kv_heads * block_size >= (int64_t{1} << 31)) return PA_ERR_SHAPE;
-  if (q_stride < static_cast<int64_t>(num_heads) * head_dim) return PA_ERR_SHAPE;
+  if (q_stride < static_cast<int64_t>(q_len) * num_heads * head_dim) return PA_ERR_SHAPE;
   if (!aligned16(q) || (q_stride * 2) % 16 != 0 || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
 
   DecodePlan plan;
   const bool have_ws = workspace != nullptr && workspace_bytes > 0;
   const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                           partition_size, q_dtype, kv_dtype, have_ws, &plan, append);
+                           partition_size, q_dtype, kv_dtype, have_ws, &plan, append, q_len);
   if (pr != PA_OK) return pr;
   if (plan.bytes > 0 && (!have_ws || workspace_bytes < plan.bytes || !aligned16(workspace))) return PA_ERR_WORKSPACE;
 
@@ -304,6 +328,7 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.block_shift = __builtin_ctz(static_cast<unsigned>(block_size));
   p.partition_units = plan.partition_units;
   p.window = o.window;
+  p.q_len = q_len;
   p.k_new = append ? o.k_new : nullptr;
   p.v_new = append ? o.v_new : nullptr;
   p.new_stride = o.new_stride;
@@ -312,7 +337,6 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.v_inv_scale = o.v_inv_scale;
   p.k_cache = const_cast<void*>(k_cache);
   p.v_cache = const_cast<void*>(v_cache);
-  p.stage_bytes = plan.geo.stage_bytes;
   p.stages = plan.geo.stages;
   p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)

@@ -153,9 +153,11 @@ __device__ __forceinline__ int find_seq(const int* prefix, int S, long long u) {
   return lo;
 }
 
-// First attended position of a sequence of length T (sliding window).
+// First attended position of a sequence of length T: that of its first
+// query (position T - q_len) under a sliding window, else 0.
 __device__ __forceinline__ int window_lo(const DecodeParams& p, int T) {
-  return (p.window > 0 && T > p.window) ? T - p.window : 0;
+  const int first = T - p.q_len + 1;
+  return (p.window > 0 && first > p.window) ? first - p.window : 0;
 }
 
 __device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
@@ -231,131 +233,142 @@ struct MergeSlots {
 };
 
 // Merges the nfr partial (m, l, acc) records of one segment with the
-// online-softmax recurrence and writes out[orow .. orow+G-1].  Run by the
-// warp that arrived last.  Lane f holds record f's (m, l) and weights
+// online-softmax recurrence and writes the output rows of its R = q_len * G
+// (query, head) rows.  Run by the warp that arrived last.  Lane f holds record f's (m, l) and weights
 // e^(m_f - M); the warp then walks the records RB at a time with all their
 // loads in flight, lane i owning head_dim columns [i*D/32, (i+1)*D/32) of
 // every head.
 template <int GM, int D, int REC>
-__device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int G,
-                                              float vs, void* out, int out_dtype, int64_t orow) {
-  constexpr int EPL = D / 32;       // columns per lane
-  constexpr int NF = EPL * GM;      // floats per lane per record (contiguous)
+__device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
+                                              int G, int num_heads, float vs, void* out, int out_dtype,
+                                              int64_t seq_row0) {
+  constexpr int EPL = D / 32;                 // columns per lane
+  constexpr int RC = GM > 8 ? 8 : GM;         // rows merged per pass (bounds the registers)
+  constexpr int NF = EPL * RC;                // floats per lane per record and pass
   constexpr int RB = NF >= 32 ? 2 : (NF >= 16 ? 4 : 8);  // 64 floats in flight per lane (registers)
   const int e0 = lane * EPL;
-  // records 0..31: slot, m and l on lane f (kept for the second pass)
-  int slot0 = 0;
-  float m0[GM], l0[GM], M[GM], L[GM];
+#pragma unroll 1
+  for (int c0 = 0; c0 < GM; c0 += RC) {
+    if (GM > 8 && c0 >= R) break;
+    // records 0..31: slot, m and l of rows c0 .. c0+RC-1 on lane f (kept for the second pass)
+    int slot0 = 0;
+    float m0[RC], l0[RC], M[RC], L[RC];
 #pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    m0[g] = -INFINITY;
-    l0[g] = 0.f;
-    L[g] = 0.f;
-  }
-  if (lane < nfr) {
-    slot0 = ms.slot(lane);
-    const float* rf = records + static_cast<int64_t>(slot0) * REC + GM * D;
-#pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      m0[g] = __ldcg(rf + g);
-      l0[g] = __ldcg(rf + GM + g);
+    for (int g = 0; g < RC; ++g) {
+      m0[g] = -INFINITY;
+      l0[g] = 0.f;
+      L[g] = 0.f;
     }
-  }
+    if (lane < nfr) {
+      slot0 = ms.slot(lane);
+      const float* rf = records + static_cast<int64_t>(slot0) * REC + GM * D + c0;
 #pragma unroll
-  for (int g = 0; g < GM; ++g) M[g] = m0[g];
-  for (int f0 = 32; f0 < nfr; f0 += 32) {
-    if (f0 + lane < nfr) {
-      const float* rf = records + static_cast<int64_t>(ms.slot(f0 + lane)) * REC + GM * D;
-#pragma unroll
-      for (int g = 0; g < GM; ++g) M[g] = fmaxf(M[g], __ldcg(rf + g));
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < GM; ++g)
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
-  float o[NF];
-#pragma unroll
-  for (int i = 0; i < NF; ++i) o[i] = 0.f;
-  for (int f0 = 0; f0 < nfr; f0 += 32) {
-    const int nb = min(32, nfr - f0);
-    float wf[GM];
-    int my_slot = slot0;
-    float mf[GM], lf[GM];
-#pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      mf[g] = m0[g];
-      lf[g] = l0[g];
-    }
-    if (f0 > 0 && lane < nb) {
-      my_slot = ms.slot(f0 + lane);
-      const float* rf = records + static_cast<int64_t>(my_slot) * REC + GM * D;
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        mf[g] = __ldcg(rf + g);
-        lf[g] = __ldcg(rf + GM + g);
+      for (int g = 0; g < RC; ++g) {
+        m0[g] = __ldcg(rf + g);
+        l0[g] = __ldcg(rf + GM + g);
       }
     }
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      // M is finite: every record covers at least one valid row
-      wf[g] = lane < nb ? exp2f(mf[g] - M[g]) : 0.f;
-      L[g] += wf[g] * (lane < nb ? lf[g] : 0.f);
+    for (int g = 0; g < RC; ++g) M[g] = m0[g];
+    for (int f0 = 32; f0 < nfr; f0 += 32) {
+      if (f0 + lane < nfr) {
+        const float* rf = records + static_cast<int64_t>(ms.slot(f0 + lane)) * REC + GM * D + c0;
+#pragma unroll
+        for (int g = 0; g < RC; ++g) M[g] = fmaxf(M[g], __ldcg(rf + g));
+      }
     }
-    for (int k = 0; k < nb; k += RB) {
-      float v[RB][NF];
 #pragma unroll
-      for (int r = 0; r < RB; ++r) {
-        const int sr = __shfl_sync(0xffffffffu, my_slot, (k + r) & 31);
-        if (k + r < nb) {
-          const float* rf = records + static_cast<int64_t>(sr) * REC + e0 * GM;
-          if constexpr (NF % 4 == 0) {
+    for (int g = 0; g < RC; ++g)
 #pragma unroll
-            for (int i = 0; i < NF; i += 4) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(rf + i));
-              v[r][i] = x.x;
-              v[r][i + 1] = x.y;
-              v[r][i + 2] = x.z;
-              v[r][i + 3] = x.w;
-            }
-          } else {
+      for (int o = 1; o < 32; o <<= 1) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
+    float o[NF];  // [column e][row g] of this pass
 #pragma unroll
-            for (int i = 0; i < NF; i += 2) {
-              const float2 x = __ldcg(reinterpret_cast<const float2*>(rf + i));
-              v[r][i] = x.x;
-              v[r][i + 1] = x.y;
-            }
-          }
+    for (int i = 0; i < NF; ++i) o[i] = 0.f;
+    for (int f0 = 0; f0 < nfr; f0 += 32) {
+      const int nb = min(32, nfr - f0);
+      float wf[RC];
+      int my_slot = slot0;
+      float mf[RC], lf[RC];
+#pragma unroll
+      for (int g = 0; g < RC; ++g) {
+        mf[g] = m0[g];
+        lf[g] = l0[g];
+      }
+      if (f0 > 0 && lane < nb) {
+        my_slot = ms.slot(f0 + lane);
+        const float* rf = records + static_cast<int64_t>(my_slot) * REC + GM * D + c0;
+#pragma unroll
+        for (int g = 0; g < RC; ++g) {
+          mf[g] = __ldcg(rf + g);
+          lf[g] = __ldcg(rf + GM + g);
         }
       }
 #pragma unroll
-      for (int r = 0; r < RB; ++r) {
+      for (int g = 0; g < RC; ++g) {
+        // an empty record (m = -inf: its rows saw nothing) weighs 0
+        wf[g] = (lane < nb && mf[g] != -INFINITY) ? exp2f(mf[g] - M[g]) : 0.f;
+        L[g] += wf[g] * (lane < nb ? lf[g] : 0.f);
+      }
+      for (int k = 0; k < nb; k += RB) {
+        float v[RB][NF];
 #pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          const float w = __shfl_sync(0xffffffffu, wf[g], (k + r) & 31);
+        for (int r = 0; r < RB; ++r) {
+          const int sr = __shfl_sync(0xffffffffu, my_slot, (k + r) & 31);
           if (k + r < nb) {
+            const float* rf = records + static_cast<int64_t>(sr) * REC;
+            if constexpr (RC % 4 == 0) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[e * GM + g] = fmaf(w, v[r][e * GM + g], o[e * GM + g]);
+              for (int e = 0; e < EPL; ++e)
+#pragma unroll
+                for (int g = 0; g < RC; g += 4) {
+                  const float4 x = __ldcg(reinterpret_cast<const float4*>(rf + (e0 + e) * GM + c0 + g));
+                  v[r][e * RC + g] = x.x;
+                  v[r][e * RC + g + 1] = x.y;
+                  v[r][e * RC + g + 2] = x.z;
+                  v[r][e * RC + g + 3] = x.w;
+                }
+            } else {  // one row (GM == 1): the lane's EPL columns are contiguous
+#pragma unroll
+              for (int e = 0; e < EPL; e += 2) {
+                const float2 x = __ldcg(reinterpret_cast<const float2*>(rf + e0 + e));
+                v[r][e] = x.x;
+                v[r][e + 1] = x.y;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+#pragma unroll
+          for (int g = 0; g < RC; ++g) {
+            const float w = __shfl_sync(0xffffffffu, wf[g], (k + r) & 31);
+            if (k + r < nb) {
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) o[e * RC + g] = fmaf(w, v[r][e * RC + g], o[e * RC + g]);
+            }
           }
         }
       }
     }
-  }
 #pragma unroll
-  for (int g = 0; g < GM; ++g)
+    for (int g = 0; g < RC; ++g)
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) L[g] += __shfl_xor_sync(0xffffffffu, L[g], off);
+      for (int off = 1; off < 32; off <<= 1) L[g] += __shfl_xor_sync(0xffffffffu, L[g], off);
 #pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    if (g < G) {
-      const float inv = vs / L[g];
+    for (int g = 0; g < RC; ++g) {
+      const int row = c0 + g;
+      if (row < R) {
+        // row = (query row / G, head row % G) of the group
+        const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>(row / G) * num_heads + row % G : seq_row0 + row;
+        const float inv = L[g] > 0.f ? vs / L[g] : 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, (orow + g) * D + e0 + e, o[e * GM + g] * inv);
+        for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, orow * D + e0 + e, o[e * RC + g] * inv);
+      }
     }
   }
 }
 
-template <typename QT, typename KVT, int D, int GM, int UR_>
+template <typename QT, typename KVT, int D, int GM, int UR_, int AP>
 __global__ void __launch_bounds__((DecodeTraits<QT, KVT, D, GM, UR_>::MAX_W + 1) * 32, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const DecodeParams p) {
@@ -383,9 +396,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   const bool fixed = p.partition_units > 0;
 
   const int NS = p.stages;  // pipeline depth per consumer
-  const int STG = p.stage_bytes;
+  // fused append (AP): stages also carry the new K/V rows
+  constexpr bool append = AP != 0;
+  constexpr int STG = append ? Tr::STAGE_APPEND : Tr::STAGE;
   const int wsm = Tr::warp_smem(NS, STG);
-  const bool append = p.k_new != nullptr;
   // shared: prefix[S+1] (units before sequence s), lens[S] (clamped seq_lens),
   // scan scratch, then the producer's block-table ring (16 ints per consumer)
   int* prefix = reinterpret_cast<int*>(base + W * wsm);
@@ -434,7 +448,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // ---- 2. empty sequences attend to nothing: their outputs are zero
   for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
     if (lens[s] == 0) {
-      const int64_t n = static_cast<int64_t>(p.num_heads) * D;
+      const int64_t n = static_cast<int64_t>(p.q_len) * p.num_heads * D;
       for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
     }
   }
@@ -530,7 +544,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
           const int box0 = first_box(it, bj0);
           const int row_in_block = unit_in_block ? (it.j - (bj0 << upb_shift)) * UR : 0;
-          const uint32_t qbytes = new_frag ? static_cast<uint32_t>(G * D * 2) : 0u;
+          const int qlen = GM > 8 ? p.q_len : 1;  // only 16-row variants serve several queries
+          const uint32_t qbytes = new_frag ? static_cast<uint32_t>(qlen * G * D * 2) : 0u;
           // this unit's entries were fetched pf - 1 units before the newest fetch
           if (pf >= 3) {
             cp_async_wait<2>();
@@ -567,9 +582,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             }
           }
           if (new_frag) {
-            const uint8_t* qsrc = static_cast<const uint8_t*>(p.q) +
-                                  (static_cast<int64_t>(it.s) * p.q_stride + static_cast<int64_t>(it.kvh) * G * D) * 2;
-            bulk_load(kdst + 2 * Tr::TILE, qsrc, qbytes, bar);
+            // rows (query i, head g) of the group, query-major: [q_len][G][D]
+            for (int i = 0; i < qlen; ++i) {
+              const uint8_t* qsrc =
+                  static_cast<const uint8_t*>(p.q) +
+                  (static_cast<int64_t>(it.s) * p.q_stride + (static_cast<int64_t>(i) * p.num_heads + it.kvh * G) * D) * 2;
+              bulk_load(kdst + 2 * Tr::TILE + i * G * D * 2, qsrc, G * D * 2, bar);
+            }
           }
           if (has_new) {
             const int64_t off = (static_cast<int64_t>(it.s) * p.new_stride + static_cast<int64_t>(it.kvh) * D) * 2;
@@ -649,15 +668,25 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     return 32 * (i >> 1) + 4 * gid + 2 * (i & 1) + hf;
   };
 
-  uint32_t qa0[Tr::KS], qa1[Tr::KS];  // A operand (query group), rows gid < G; rows g+8 are zero
-  float m = -INFINITY, l = 0.f;       // running max / sum of head gid (log2 domain)
-  float acc[Tr::KS][4];               // O^T: rows = head_dim columns, cols = heads 2t, 2t+1
+  // Rows of the A operand: r = query * G + head (r < R = q_len * G).  Lane
+  // (g, t) holds rows g and, with 16-row variants, g + 8 (NH halves).  Only
+  // the 16-row variants serve several queries per sequence (MQ); the others
+  // compile the single-query case, whose rows share one set of bounds.
+  constexpr int NH = GM > 8 ? 2 : 1;
+  constexpr bool MQ = GM > 8;
+  const int QL = MQ ? p.q_len : 1;
+  const int R = QL * G;
+  uint32_t qa0[Tr::KS], qa1[Tr::KS];  // A operand, row g (zero when g >= R)
+  uint32_t qb0[Tr::KS], qb1[Tr::KS];  // A operand, row g + 8 (NH == 2)
+  float m[NH], l[NH];                 // running max / sum of rows g, g + 8 (log2 domain)
+  float acc[Tr::KS][NH][4];           // O^T: rows = head_dim columns, cols = A rows 8h + 2t, 8h + 2t + 1
+  int hi_abs[NH], lo_abs[NH];         // last / first position row g + 8h may see (MQ)
   float score_scale = p.qk_scale_log2;
   uint32_t zpk2 = 0u, zpv2 = 0u;  // INT8: f16x2(1152 + zero point) of this KV head
 
   // One unit: S^T = Q K^T, online-softmax update, O^T += V^T P^T.
   // FULL: all UR rows valid.
-  auto unit_step = [&](auto full_tag, uint32_t kt, int n_valid, int lo_rel) {
+  auto unit_step = [&](auto full_tag, uint32_t kt, int n_valid, int lo_rel, int j) {
     constexpr bool FULL = decltype(full_tag)::value;
     const uint32_t vt = kt + Tr::TILE;
     float sc[Tr::NT][4];
@@ -671,8 +700,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         for (int s = 0; s < Tr::KS; ++s) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kt + sb * sub_delta + moff[s], b0, b1, b2, b3);
-          mma16816<MB>(sc[2 * sb], qa0[s], 0u, qa1[s], 0u, b0, b1);
-          mma16816<MB>(sc[2 * sb + 1], qa0[s], 0u, qa1[s], 0u, b2, b3);
+          const uint32_t a1 = NH == 2 ? qb0[s] : 0u, a3 = NH == 2 ? qb1[s] : 0u;
+          mma16816<MB>(sc[2 * sb], qa0[s], a1, qa1[s], a3, b0, b1);
+          mma16816<MB>(sc[2 * sb + 1], qa0[s], a1, qa1[s], a3, b2, b3);
         }
       }
     } else {
@@ -687,54 +717,76 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             const int s = 4 * g + r;
             uint32_t b0, b1;
             widen4<KVT>(ws[r], zpk2, b0, b1);
-            mma16816<false>(sc[nt], qa0[s], 0u, qa1[s], 0u, b0, b1);
+            mma16816<false>(sc[nt], qa0[s], NH == 2 ? qb0[s] : 0u, qa1[s], NH == 2 ? qb1[s] : 0u, b0, b1);
           }
         }
       }
     }
-    // ---- online softmax on head gid's scores (quad lanes share a head)
-    float mx = -INFINITY;
+    // ---- online softmax per row (the quad of lanes g*4 .. g*4+3 shares rows g, g+8)
+    float mx[NH];
 #pragma unroll
-    for (int nt = 0; nt < Tr::NT; ++nt) {
+    for (int h = 0; h < NH; ++h) {
+      mx[h] = -INFINITY;
+      int hr = 0, lr = 0;  // this row's bounds in the unit (several queries per sequence)
+      if constexpr (MQ) {
+        hr = hi_abs[h] - j * UR;
+        lr = lo_abs[h] - j * UR;
+      }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float x = sc[nt][e] * score_scale;
-        if constexpr (!FULL) {
-          const int tok = nt * 8 + (k8bit ? sigma(2 * tig + e) : 2 * tig + e);
-          x = (tok < n_valid && tok >= lo_rel) ? x : -INFINITY;
+      for (int nt = 0; nt < Tr::NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float x = sc[nt][2 * h + e] * score_scale;
+          if constexpr (!FULL) {
+            const int tok = nt * 8 + (k8bit ? sigma(2 * tig + e) : 2 * tig + e);
+            bool ok = tok < n_valid && tok >= lo_rel;
+            if constexpr (MQ) ok = ok && tok <= hr && tok >= lr;
+            x = ok ? x : -INFINITY;
+          }
+          sc[nt][2 * h + e] = x;
+          mx[h] = fmaxf(mx[h], x);
         }
-        sc[nt][e] = x;
-        mx = fmaxf(mx, x);
+      }
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+    }
+    bool up = mx[0] > m[0];
+    if constexpr (NH == 2) up |= mx[1] > m[1];
+    if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float mn = fmaxf(m[h], mx[h]);
+        // a row that has seen nothing yet keeps alpha = 1 (its state is still empty);
+        // single-query rows see a token in every unit they process
+        const float alpha = (MQ && mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
+        m[h] = mn;
+        l[h] *= alpha;
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);      // row 8h + 2t
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);  // row 8h + 2t + 1
+#pragma unroll
+        for (int i = 0; i < Tr::KS; ++i) {
+          acc[i][h][0] *= a0;
+          acc[i][h][1] *= a1;
+          acc[i][h][2] *= a0;
+          acc[i][h][3] *= a1;
+        }
       }
     }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (__any_sync(0xffffffffu, mx > m)) {
-      const float mn = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - mn);
-      m = mn;
-      l *= alpha;
-      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);      // head 2t
-      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);  // head 2t+1
+    // P^T as the B operand of each 16-token k-step, per row half, split hi + lo
+    uint32_t ph[Tr::NSB][NH][2], pl[Tr::NSB][NH][2];
 #pragma unroll
-      for (int i = 0; i < Tr::KS; ++i) {
-        acc[i][0] *= a0;
-        acc[i][1] *= a1;
-        acc[i][2] *= a0;
-        acc[i][3] *= a1;
+    for (int h = 0; h < NH; ++h) {
+      const float ms = (MQ && m[h] == -INFINITY) ? 0.f : m[h];  // exp2(-inf - ms) = 0 for an empty row
+#pragma unroll
+      for (int nt = 0; nt < Tr::NT; ++nt) {
+        const float p0 = fast_exp2(sc[nt][2 * h] - ms);
+        const float p1 = fast_exp2(sc[nt][2 * h + 1] - ms);
+        l[h] += p0 + p1;
+        const uint32_t hp = pack2<MB>(p0, p1);
+        const float2 hf = unpack2<MB>(hp);
+        ph[nt >> 1][h][nt & 1] = hp;
+        pl[nt >> 1][h][nt & 1] = pack2<MB>(p0 - hf.x, p1 - hf.y);
       }
-    }
-    // P^T as the B operand of each 16-token k-step, split hi + lo
-    uint32_t ph[Tr::NSB][2], pl[Tr::NSB][2];
-#pragma unroll
-    for (int nt = 0; nt < Tr::NT; ++nt) {
-      const float p0 = fast_exp2(sc[nt][0] - m);
-      const float p1 = fast_exp2(sc[nt][1] - m);
-      l += p0 + p1;
-      const uint32_t h = pack2<MB>(p0, p1);
-      const float2 hf = unpack2<MB>(h);
-      ph[nt >> 1][nt & 1] = h;
-      pl[nt >> 1][nt & 1] = pack2<MB>(p0 - hf.x, p1 - hf.y);
     }
     // rows past the end of the sequence, and rows before a sliding window,
     // may hold anything (or were not loaded): zero them in V
@@ -758,8 +810,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         for (int i = 0; i < Tr::KS; ++i) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(vt + sb * sub_delta + moff[i], a0, a1, a2, a3);
-          mma16816<MB>(acc[i], a0, a1, a2, a3, ph[sb][0], ph[sb][1]);
-          mma16816<MB>(acc[i], a0, a1, a2, a3, pl[sb][0], pl[sb][1]);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            mma16816<MB>(acc[i][h], a0, a1, a2, a3, ph[sb][h][0], ph[sb][h][1]);
+            mma16816<MB>(acc[i][h], a0, a1, a2, a3, pl[sb][h][0], pl[sb][h][1]);
+          }
         }
       }
     } else {
@@ -779,10 +834,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           widen4<KVT>(lo23, zpv2, d2l, d3l);
           widen4<KVT>(hi01, zpv2, d0h, d1h);
           widen4<KVT>(hi23, zpv2, d2h, d3h);
-          mma16816<false>(acc[2 * jj], d0l, d1l, d0h, d1h, ph[sb][0], ph[sb][1]);
-          mma16816<false>(acc[2 * jj], d0l, d1l, d0h, d1h, pl[sb][0], pl[sb][1]);
-          mma16816<false>(acc[2 * jj + 1], d2l, d3l, d2h, d3h, ph[sb][0], ph[sb][1]);
-          mma16816<false>(acc[2 * jj + 1], d2l, d3l, d2h, d3h, pl[sb][0], pl[sb][1]);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            mma16816<false>(acc[2 * jj][h], d0l, d1l, d0h, d1h, ph[sb][h][0], ph[sb][h][1]);
+            mma16816<false>(acc[2 * jj][h], d0l, d1l, d0h, d1h, pl[sb][h][0], pl[sb][h][1]);
+            mma16816<false>(acc[2 * jj + 1][h], d2l, d3l, d2h, d3h, ph[sb][h][0], ph[sb][h][1]);
+            mma16816<false>(acc[2 * jj + 1][h], d2l, d3l, d2h, d3h, pl[sb][h][0], pl[sb][h][1]);
+          }
         }
       }
     }
@@ -857,24 +915,40 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     {
       // the query group rode on the fragment's first stage
       const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * STG + 2 * Tr::TILE;
-      const bool row_ok = gid < G;
 #pragma unroll
-      for (int s = 0; s < Tr::KS; ++s) {
-        // columns of k-step s held by this lane: (d, d+1) for a0, (d2, d2+1) for a2
-        const int d = k8bit ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 16 * s + 2 * tig;
-        const int d2 = k8bit ? d + 2 : d + 8;
-        uint32_t w0 = 0u, w1 = 0u;
-        if (row_ok) {
-          w0 = *reinterpret_cast<const uint32_t*>(qr + (gid * D + d) * 2);
-          w1 = *reinterpret_cast<const uint32_t*>(qr + (gid * D + d2) * 2);
+      for (int h = 0; h < NH; ++h) {
+        const int row = gid + 8 * h;
+        const bool row_ok = row < R;
+#pragma unroll
+        for (int s = 0; s < Tr::KS; ++s) {
+          // columns of k-step s held by this lane: (d, d+1) for a0/a1, (d2, d2+1) for a2/a3
+          const int d = k8bit ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 16 * s + 2 * tig;
+          const int d2 = k8bit ? d + 2 : d + 8;
+          uint32_t w0 = 0u, w1 = 0u;
+          if (row_ok) {
+            w0 = *reinterpret_cast<const uint32_t*>(qr + (row * D + d) * 2);
+            w1 = *reinterpret_cast<const uint32_t*>(qr + (row * D + d2) * 2);
+          }
+          if constexpr (k8bit && std::is_same<QT, bf16_t>::value) {
+            const float2 f0 = widen2<bf16_t>(w0), f1 = widen2<bf16_t>(w1);
+            w0 = pack2<false>(f0.x, f0.y);
+            w1 = pack2<false>(f1.x, f1.y);
+          }
+          if (h == 0) {
+            qa0[s] = w0;
+            qa1[s] = w1;
+          } else {
+            qb0[s] = w0;
+            qb1[s] = w1;
+          }
         }
-        if constexpr (k8bit && std::is_same<QT, bf16_t>::value) {
-          const float2 f0 = widen2<bf16_t>(w0), f1 = widen2<bf16_t>(w1);
-          w0 = pack2<false>(f0.x, f0.y);
-          w1 = pack2<false>(f1.x, f1.y);
+        // query i = row / G sits at position T - q_len + i and sees positions up to
+        // it (and, under a window, the last `window` of them); padding rows see all
+        if constexpr (MQ) {
+          const int qi = row < R ? row / G : QL - 1;
+          hi_abs[h] = it.T - QL + qi;
+          lo_abs[h] = p.window > 0 ? hi_abs[h] - p.window + 1 : 0;
         }
-        qa0[s] = w0;
-        qa1[s] = w1;
       }
     }
     score_scale = p.qk_scale_log2;
@@ -885,20 +959,27 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       zpk2 = zk | (zk << 16);
       zpv2 = zv | (zv << 16);
     }
-    m = -INFINITY;
-    l = 0.f;
 #pragma unroll
-    for (int i = 0; i < Tr::KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int h = 0; h < NH; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < Tr::KS; ++i) acc[i][h][0] = acc[i][h][1] = acc[i][h][2] = acc[i][h][3] = 0.f;
+    }
+    // a unit is FULL when every row sees all of its tokens
+    const int full_lo = p.window > 0 ? it.T - 1 - p.window + 1 : 0;  // first position the last query sees
+    const int full_hi = it.T - QL;                                   // last position the first query sees
     bool timed_out = false;
     for (;;) {
       const uint32_t stage_u32 = wbase_u32 + Tr::OFF_STAGES + cst * STG;
       if (append && it.j == ((it.T - 1) >> Tr::UR_SHIFT)) append_row(cst);
       const int n_valid = min(UR, it.T - it.j * UR);
       const int lo_rel = it.lo - it.j * UR;  // positions before the window (> 0 only in its first unit)
-      if (n_valid == UR && lo_rel <= 0) {
-        unit_step(std::true_type{}, stage_u32, UR, 0);
+      const bool full = MQ ? (it.j * UR >= full_lo && it.j * UR + UR - 1 <= full_hi) : (n_valid == UR && lo_rel <= 0);
+      if (full) {
+        unit_step(std::true_type{}, stage_u32, UR, 0, it.j);
       } else {
-        unit_step(std::false_type{}, stage_u32, n_valid, lo_rel);
+        unit_step(std::false_type{}, stage_u32, n_valid, lo_rel, it.j);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(wbase_u32 + Tr::OFF_EMPTY + 8 * cst);  // the stage may be refilled
@@ -918,42 +999,60 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
     // ---- end of fragment: write the output or a partial record
     {
-      float lt = l + __shfl_xor_sync(0xffffffffu, l, 1);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 2);            // head gid's sum
-      const float l0 = __shfl_sync(0xffffffffu, lt, 8 * tig);      // head 2t
-      const float l1 = __shfl_sync(0xffffffffu, lt, 8 * tig + 4);  // head 2t+1
-      const int h0 = 2 * tig, h1 = 2 * tig + 1;
+      float lt[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        lt[h] = l[h] + __shfl_xor_sync(0xffffffffu, l[h], 1);
+        lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], 2);  // row gid + 8h's sum
+      }
       float vs = 1.f;
       if constexpr (k8bit) vs = __ldg(p.v_scale + it.kvh);
-      const int64_t orow = static_cast<int64_t>(it.s) * p.num_heads + static_cast<int64_t>(it.kvh) * G;
+      // output row of A row r: out[s][r / G][kvh * G + r % G]
+      const int64_t seq_row0 = static_cast<int64_t>(it.s) * QL * p.num_heads + static_cast<int64_t>(it.kvh) * G;
+      auto out_row = [&](int r) -> int64_t {
+        if constexpr (!MQ) return seq_row0 + r;  // one query: row = head
+        return seq_row0 + static_cast<int64_t>(r / G) * p.num_heads + r % G;
+      };
       if (it.slot < 0) {
-        const float i0 = vs / l0, i1 = vs / l1;
 #pragma unroll
-        for (int i = 0; i < Tr::KS; ++i) {
+        for (int h = 0; h < NH; ++h) {
+          const int r0 = 8 * h + 2 * tig, r1 = r0 + 1;
+          const float l0 = __shfl_sync(0xffffffffu, lt[h], 8 * tig);      // row r0
+          const float l1 = __shfl_sync(0xffffffffu, lt[h], 8 * tig + 4);  // row r1
+          const float i0 = l0 > 0.f ? vs / l0 : 0.f, i1 = l1 > 0.f ? vs / l1 : 0.f;  // a row that saw nothing: 0
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int d = dim_of(i, hf);
-            if (h0 < G) store_out(p.out, p.out_dtype, (orow + h0) * D + d, acc[i][2 * hf] * i0);
-            if (h1 < G) store_out(p.out, p.out_dtype, (orow + h1) * D + d, acc[i][2 * hf + 1] * i1);
+          for (int i = 0; i < Tr::KS; ++i) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int d = dim_of(i, hf);
+              if (r0 < R) store_out(p.out, p.out_dtype, out_row(r0) * D + d, acc[i][h][2 * hf] * i0);
+              if (r1 < R) store_out(p.out, p.out_dtype, out_row(r1) * D + d, acc[i][h][2 * hf + 1] * i1);
+            }
           }
         }
       } else {
         float* rec = p.part_records + static_cast<int64_t>(it.slot) * Tr::REC;
 #pragma unroll
-        for (int i = 0; i < Tr::KS; ++i) {
+        for (int h = 0; h < NH; ++h) {
+          const int r0 = 8 * h + 2 * tig;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int d = dim_of(i, hf);
-            if constexpr (GM == 1) {
-              if (tig == 0) rec[d] = acc[i][2 * hf];
-            } else {
-              if (h0 < GM) *reinterpret_cast<float2*>(rec + d * GM + h0) = make_float2(acc[i][2 * hf], acc[i][2 * hf + 1]);
+          for (int i = 0; i < Tr::KS; ++i) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int d = dim_of(i, hf);
+              if constexpr (GM == 1) {
+                if (tig == 0) rec[d] = acc[i][h][2 * hf];
+              } else {
+                if (r0 < GM)
+                  *reinterpret_cast<float2*>(rec + d * GM + r0) = make_float2(acc[i][h][2 * hf], acc[i][h][2 * hf + 1]);
+              }
             }
           }
-        }
-        if (tig == 0 && gid < GM) {
-          rec[GM * D + gid] = m;
-          rec[GM * D + GM + gid] = lt;
+          const int row = gid + 8 * h;
+          if (tig == 0 && row < GM) {
+            rec[GM * D + row] = m[h];
+            rec[GM * D + GM + row] = lt[h];
+          }
         }
         __threadfence();
         __syncwarp();
@@ -984,7 +1083,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           ms.U = U;
           ms.nw_eff = nw_eff;
           ms.seg_start = seg_start;
-          merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, G, vs, p.out, p.out_dtype, orow);
+          merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype,
+                                        seq_row0);
           if (lane == 0) p.seg_counters[it.s * Hkv + it.kvh] = 0;
         }
       }
@@ -997,7 +1097,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
 // ----------------------------------------------------------------- host side of one variant
 
-template <typename QT, typename KVT, int D, int GM, int UR>
+template <typename QT, typename KVT, int D, int GM, int UR, int AP>
 struct DecodeVariant {
   using Tr = DecodeTraits<QT, KVT, D, GM, UR>;
 
@@ -1011,17 +1111,17 @@ struct DecodeVariant {
   // kStageBytesPerWarp of K/V per consumer; the consumers per CTA maximise
   // resident consumer warps per SM (ties: more per CTA, i.e. fewer producer
   // warps).  PA_DECODE_STAGES / PA_DECODE_WARPS override both (tuning).
-  static bool geometry(int num_seqs, int append, DecodeGeometry* g) {
+  static bool geometry(int num_seqs, DecodeGeometry* g) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     int sms = 0, optin = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-    auto kern = paged_decode_kernel<QT, KVT, D, GM, UR>;
+    auto kern = paged_decode_kernel<QT, KVT, D, GM, UR, AP>;
     // allow every size the device allows, once: geometries of other batch
     // sizes are cached and launched later without touching the attribute
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess) return false;
-    const int stage = append ? Tr::STAGE_APPEND : Tr::STAGE;
+    const int stage = AP ? Tr::STAGE_APPEND : Tr::STAGE;
     int ns = kStageBytesPerWarp / stage;
     ns = ns < 2 ? 2 : (ns > Tr::MAX_NS ? Tr::MAX_NS : ns);
     const int env_ns = tuning_override("PA_DECODE_STAGES");
@@ -1055,11 +1155,11 @@ struct DecodeVariant {
   static cudaError_t launch(const DecodeGeometry& g, const DecodeParams& p, const CUtensorMap& tk,
                             const CUtensorMap& tv, cudaStream_t stream) {
     (void)cudaGetLastError();  // an earlier unrelated error must not be reported as this launch's
-    paged_decode_kernel<QT, KVT, D, GM, UR><<<g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, stream>>>(tk, tv, p);
+    paged_decode_kernel<QT, KVT, D, GM, UR, AP><<<g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, stream>>>(tk, tv, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, paged_decode_kernel<QT, KVT, D, GM, UR>) == cudaSuccess)
+      if (cudaFuncGetAttributes(&fa, paged_decode_kernel<QT, KVT, D, GM, UR, AP>) == cudaSuccess)
         note_launch_failure(g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, g.stages, fa.maxThreadsPerBlock,
                             fa.maxDynamicSharedSizeBytes, fa.numRegs, fa.localSizeBytes);
     }

@@ -42,14 +42,14 @@ template <> constexpr int dtype_code<bf16_t>() { return PA_BF16; }
 template <> constexpr int dtype_code<e4m3_t>() { return PA_FP8_E4M3; }
 template <> constexpr int dtype_code<i8_t>() { return PA_INT8; }
 
-#define PA_MATCH(QT, KVT, D, GM, UR)                                                        \
+#define PA_MATCH(QT, KVT, D, GM, UR, AP)                                                                   \
   (key.q_dtype == dtype_code<QT>() && key.kv_dtype == dtype_code<KVT>() && key.head_dim == D && key.gmax == GM && \
-   key.unit_rows == UR)
+   key.unit_rows == UR && key.append == AP)
 
 namespace {
 bool compute_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
-#define PA_GEO(QT, KVT, D, GM, UR) \
-  if (PA_MATCH(QT, KVT, D, GM, UR)) return decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR(num_seqs, key.append, geo);
+#define PA_GEO(QT, KVT, D, GM, UR, AP) \
+  if (PA_MATCH(QT, KVT, D, GM, UR, AP)) return decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(num_seqs, geo);
   PA_DECODE_VARIANTS(PA_GEO)
 #undef PA_GEO
   return false;
@@ -86,8 +86,9 @@ bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
 
 cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,
                           const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-#define PA_LAUNCH(QT, KVT, D, GM, UR) \
-  if (PA_MATCH(QT, KVT, D, GM, UR)) return decode_launch_##QT##_##KVT##_##D##_##GM##_##UR(geo, p, tk, tv, stream);
+#define PA_LAUNCH(QT, KVT, D, GM, UR, AP) \
+  if (PA_MATCH(QT, KVT, D, GM, UR, AP))    \
+    return decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(geo, p, tk, tv, stream);
   PA_DECODE_VARIANTS(PA_LAUNCH)
 #undef PA_LAUNCH
   return cudaErrorInvalidValue;

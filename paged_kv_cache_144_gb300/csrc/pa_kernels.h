@@ -65,6 +65,7 @@ struct DecodeParams {
   int block_shift;              // log2(block_size)
   int partition_units;          // 0: balanced split; >0: fixed partitions of this many units
   int window;                   // > 0: attend to the last `window` positions only; 0: all
+  int q_len;                    // queries per sequence (their positions are the q_len newest)
   // fused append (k_new == nullptr: off): the rows of position seq_len-1
   const void* k_new;            // [num_seqs][num_kv_heads][head_dim] at new_stride elements per sequence
   const void* v_new;
@@ -74,7 +75,6 @@ struct DecodeParams {
   const float* v_inv_scale;
   void* k_cache;                // pools, for storing the appended rows
   void* v_cache;
-  int stage_bytes;              // bytes of one pipeline stage (DecodeGeometry::stage_bytes)
   float* part_records;          // split-K partial records (workspace)
   int* seg_counters;            // [num_seqs * num_kv_heads] arrival counters (workspace)
   unsigned int* err;            // per-device error word

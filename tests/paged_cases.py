@@ -44,6 +44,7 @@ def out_tolerance(ref: np.ndarray, out_fmt: str) -> np.ndarray:
 
 
 def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda", window=0):
+    """q of shape [S, L, H_q, d] (L > 1) decodes L queries per sequence (pa_decode_ex q_len)."""
     """Fill the cache (FP8: quantising writes), append the new token, decode.
 
     Returns (out float64 numpy, k_cache numpy, v_cache numpy, device error bits).
@@ -75,12 +76,14 @@ def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", d
                          kc, vc, new_slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz, v_zero_point=vz)
     tables = torch.from_numpy(batch.block_tables).to(device)
     lens = torch.from_numpy(batch.seq_lens).to(device)
-    out = torch.empty((batch.num_seqs, batch.num_heads, batch.head_dim), dtype=getattr(torch, TORCH_DT[out_fmt]),
-                      device=device)
+    q_len = vals["q"].shape[1] if vals["q"].ndim == 4 else 1
+    oshape = (batch.num_seqs, batch.num_heads, batch.head_dim) if q_len == 1 else \
+        (batch.num_seqs, q_len, batch.num_heads, batch.head_dim)
+    out = torch.empty(oshape, dtype=getattr(torch, TORCH_DT[out_fmt]), device=device)
     ws = None
     if workspace == "auto":
         n = pa.decode_workspace_bytes(batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, B,
-                                      batch.max_blocks_per_seq, partition_size, pa.dtype_code(kc))
+                                      batch.max_blocks_per_seq, partition_size, pa.dtype_code(kc), q_len=q_len)
         ws = pa.new_workspace(n, device) if n else None
     pa.decode(out, q, kc, vc, tables, lens, batch.num_kv_heads, batch.scale, B, k_scale=ks, v_scale=vs,
               partition_size=partition_size, workspace=ws, window=window, k_zero_point=kz, v_zero_point=vz)
@@ -105,10 +108,10 @@ def run_oracle(batch, vals, window=0):
     kc, vc = oracle.reshape_and_cache(vals["k_new"], vals["v_new"], kc, vc, batch.new_slots, B,
                                       src_fmt=src_fmt, kv_fmt=kv, k_inv_scale=kis, v_inv_scale=vis,
                                       k_zero_point=kz, v_zero_point=vz)
-    ref = oracle.paged_decode_attention(vals["q"], kc, vc, batch.block_tables, batch.seq_lens, batch.scale, B,
-                                        q_fmt=batch.q_fmt, kv_fmt=kv, k_scale=vals.get("k_scale"),
-                                        v_scale=vals.get("v_scale"), window=window, k_zero_point=kz,
-                                        v_zero_point=vz)
+    fn = oracle.paged_multi_query_attention if vals["q"].ndim == 4 else oracle.paged_decode_attention
+    ref = fn(vals["q"], kc, vc, batch.block_tables, batch.seq_lens, batch.scale, B, q_fmt=batch.q_fmt, kv_fmt=kv,
+             k_scale=vals.get("k_scale"), v_scale=vals.get("v_scale"), window=window, k_zero_point=kz,
+             v_zero_point=vz)
     return ref, kc, vc
 
 

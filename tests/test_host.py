@@ -103,6 +103,16 @@ def test_decode_ex_options_validation(lib):
                       vs=A, D=64, q_stride=32 * 64) == pa.PA_ERR_UNSUPPORTED
 
 
+def test_decode_ex_multi_query_validation(lib):
+    # 32 q heads / 8 KV heads: G = 4, so q_len 4 fills 16 A rows and q_len 5 is too many
+    assert _decode_ex(pa.DecodeOptions(q_len=5), q_stride=5 * 32 * 128) == pa.PA_ERR_UNSUPPORTED
+    assert _decode_ex(pa.DecodeOptions(q_len=4), q_stride=3 * 32 * 128) == pa.PA_ERR_SHAPE
+    assert _decode_ex(pa.DecodeOptions(q_len=-1)) == pa.PA_ERR_SHAPE
+    assert _decode_ex(pa.DecodeOptions(q_len=2, k_new=0x10000, v_new=0x20000, new_dtype=pa.PA_BF16,
+                                       new_stride=8 * 128), q_stride=2 * 32 * 128) == pa.PA_ERR_UNSUPPORTED
+    assert _decode_ex(pa.DecodeOptions(q_len=4), q_stride=4 * 32 * 128, S=0) == pa.PA_OK
+
+
 def test_cache_write_int8_validation(lib):
     def rc(opt, **kw):
         a = dict(k=A, v=A2, src=pa.PA_BF16, ks=8 * 128, vs=8 * 128, kc=A, vc=A2, kv=pa.PA_INT8, nb=10, sm=A, N=3,

@@ -221,7 +221,8 @@ def _bf16_amax_per_head(*arrays) -> np.ndarray:
     return m.numpy().astype(np.float32)
 
 
-def host_values(batch: DecodeBatch, seed: int = 0, *, q_mult: float = 1.0, nan_tails: bool = True):
+def host_values(batch: DecodeBatch, seed: int = 0, *, q_mult: float = 1.0, nan_tails: bool = True,
+                q_len: int = 1):
     """Numpy storage arrays for a (small) batch.
 
     16-bit caches: every cached position gets N(0,1) values; slots that no
@@ -236,7 +237,8 @@ def host_values(batch: DecodeBatch, seed: int = 0, *, q_mult: float = 1.0, nan_t
     S, Hq, Hkv, d, B, NB = (batch.num_seqs, batch.num_heads, batch.num_kv_heads,
                             batch.head_dim, batch.block_size, batch.num_blocks)
     out = {}
-    out["q"] = _normal_storage(rng, (S, Hq, d), batch.q_fmt, q_mult)
+    # q_len > 1: [S, q_len, H_q, d], the queries of the q_len newest positions
+    out["q"] = _normal_storage(rng, (S, Hq, d) if q_len == 1 else (S, q_len, Hq, d), batch.q_fmt, q_mult)
     if batch.kv_fmt in ("f16", "bf16"):
         k = _normal_storage(rng, (NB, Hkv, B, d), batch.kv_fmt)
         v = _normal_storage(rng, (NB, Hkv, B, d), batch.kv_fmt)
