@@ -66,20 +66,21 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def algorithmic_bytes(batch, window: int = 0) -> dict:
+def algorithmic_bytes(batch, window: int = 0, q_len: int = 1) -> dict:
     """Bytes a step must move at minimum (attended tokens only; tails, workspace and scales excluded).
 
     With a sliding window only the last `window` positions of each sequence and the
-    block-table entries of the blocks holding them count.
+    block-table entries of the blocks holding them count.  With q_len queries per
+    sequence the KV rows are still read once; q and out count q_len times.
     """
     S, Hq, Hkv, D, B = batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
     b_kv = FMT_BYTES[batch.kv_fmt]
     b_q = FMT_BYTES[batch.q_fmt]
     T = batch.seq_lens.astype(np.int64)
-    lo = np.maximum(T - window, 0) if window > 0 else np.zeros_like(T)
+    lo = np.maximum(T - q_len + 1 - window, 0) if window > 0 else np.zeros_like(T)
     kv = int((T - lo).sum()) * Hkv * D * b_kv * 2
     blocks = int(((T + B - 1) // B - lo // B).sum())
-    decode = kv + S * Hq * D * b_q + S * Hq * D * b_q + blocks * 4 + 4 * S
+    decode = kv + q_len * (S * Hq * D * b_q + S * Hq * D * b_q) + blocks * 4 + 4 * S
     src_b = b_q if batch.kv_fmt in ("e4m3", "i8") else b_kv
     append = S * Hkv * D * (src_b + b_kv) * 2 + 8 * S
     return {"kv": kv, "decode": decode, "append": append, "step": decode + append}
@@ -329,9 +330,13 @@ def run_ours(args):
     q, k_new, v_new = vals["q"], vals["k_new"], vals["v_new"]
     ks, vs = vals.get("k_scale"), vals.get("v_scale")
     kis, vis = vals.get("k_inv_scale"), vals.get("v_inv_scale")
-    out = torch.empty((S, Hq, D), dtype=q.dtype, device=dev)
+    if args.q_len > 1:   # the q_len newest positions are queries: [S, L, H_q, d]
+        gq = torch.Generator(device=dev)
+        gq.manual_seed(args.seed * 7 + 3)
+        q = torch.randn((S, args.q_len, Hq, D), generator=gq, device=dev, dtype=torch.float32).to(q.dtype)
+    out = torch.empty(q.shape, dtype=q.dtype, device=dev)
     nws = pa.decode_workspace_bytes(S, Hq, Hkv, D, B, batch.max_blocks_per_seq, args.partition_size,
-                                    pa.dtype_code(vals["k_cache"]))
+                                    pa.dtype_code(vals["k_cache"]), q_len=args.q_len)
     ws = pa.new_workspace(nws, dev) if nws else None
     geometry = pa.pa_decode_launch_config(S, Hq, Hkv, D, B, batch.max_blocks_per_seq, args.partition_size,
                                           pa.dtype_code(q), pa.dtype_code(vals["k_cache"]))
@@ -434,7 +439,7 @@ def run_ours(args):
         e2e_s = max_over_ranks(e2e_s, world)
         e2e = (e2e_s, h2d, d2h)
 
-    ab = algorithmic_bytes(batch, args.window)
+    ab = algorithmic_bytes(batch, args.window, args.q_len)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     total_step_bytes = sum_over_ranks(float(ab["step"]), world)
     total_kv = sum_over_ranks(float(ab["kv"]), world)
@@ -462,6 +467,7 @@ def run_ours(args):
             "context_tokens": int(batch.seq_lens.sum()), "kv_dtype": batch.kv_fmt, "q_dtype": batch.q_fmt,
             "split": "balanced" if args.partition_size == 0 else f"fixed {args.partition_size} tokens",
             "window": args.window or None,
+            "q_len": args.q_len,
             "step": ("pa_decode_ex with the new token's cache write fused (one launch)" if args.fused
                      else "reshape_and_cache(1 new token/seq) + pa_decode"),
             "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
@@ -470,7 +476,7 @@ def run_ours(args):
         },
         "pct_of_hbm_peak": round(100.0 * value / peaks["hbm_gbs"], 2),
         "kv_read_gbps": round(total_kv / (ms_step * 1e-3) / 1e9, 2),
-        "decode_tokens_per_s": round(total_seqs / (ms_step * 1e-3), 1),
+        "decode_tokens_per_s": round(total_seqs * args.q_len / (ms_step * 1e-3), 1),
         "context_tokens_per_s": round(total_ctx / (ms_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (pa_decode, one launch)",
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -702,6 +708,8 @@ def main():
                     choices=["tiny", "gqa_32x4k", "long_32k", "fp8_mix", "int8_mix", "beam_cow"])
     ap.add_argument("--fused", action="store_true",
                     help="one launch per step: the new token's cache write fused into pa_decode_ex")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="queries per sequence (the q_len newest positions; speculative verification)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window decode over the last W positions (bytes counted over the window)")
     ap.add_argument("--partition-size", type=int, default=0)
@@ -714,6 +722,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.q_len > 1 and args.fused:
+        ap.error("--fused appends one token per sequence (q_len 1)")
     if args.impl == "reference":
         if args.workload == "beam_cow":
             ap.error("the reference arm times the batch workloads")

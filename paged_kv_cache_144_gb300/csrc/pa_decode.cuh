@@ -975,8 +975,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       if (append && it.j == ((it.T - 1) >> Tr::UR_SHIFT)) append_row(cst);
       const int n_valid = min(UR, it.T - it.j * UR);
       const int lo_rel = it.lo - it.j * UR;  // positions before the window (> 0 only in its first unit)
-      const bool full = MQ ? (it.j * UR >= full_lo && it.j * UR + UR - 1 <= full_hi) : (n_valid == UR && lo_rel <= 0);
-      if (full) {
+      if constexpr (MQ) {
+        // one (masked) copy of the unit step: two inlined copies do not fit the
+        // registers of the 16-row variants
+        (void)full_lo;
+        (void)full_hi;
+        unit_step(std::false_type{}, stage_u32, n_valid, lo_rel, it.j);
+      } else if (n_valid == UR && lo_rel <= 0) {
         unit_step(std::true_type{}, stage_u32, UR, 0, it.j);
       } else {
         unit_step(std::false_type{}, stage_u32, n_valid, lo_rel, it.j);
@@ -1020,13 +1025,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const float l0 = __shfl_sync(0xffffffffu, lt[h], 8 * tig);      // row r0
           const float l1 = __shfl_sync(0xffffffffu, lt[h], 8 * tig + 4);  // row r1
           const float i0 = l0 > 0.f ? vs / l0 : 0.f, i1 = l1 > 0.f ? vs / l1 : 0.f;  // a row that saw nothing: 0
+          const int64_t o0 = out_row(r0) * D, o1 = out_row(r1) * D;
+          const bool w0 = r0 < R, w1 = r1 < R;
 #pragma unroll
           for (int i = 0; i < Tr::KS; ++i) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               const int d = dim_of(i, hf);
-              if (r0 < R) store_out(p.out, p.out_dtype, out_row(r0) * D + d, acc[i][h][2 * hf] * i0);
-              if (r1 < R) store_out(p.out, p.out_dtype, out_row(r1) * D + d, acc[i][h][2 * hf + 1] * i1);
+              if (w0) store_out(p.out, p.out_dtype, o0 + d, acc[i][h][2 * hf] * i0);
+              if (w1) store_out(p.out, p.out_dtype, o1 + d, acc[i][h][2 * hf + 1] * i1);
             }
           }
         }
