@@ -164,14 +164,14 @@ __device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, c
   const int Hkv = p.num_kv_heads;
   const int s = find_seq(prefix, p.num_seqs, it.u);
   const int nu = (prefix[s + 1] - prefix[s]) / Hkv;
-  const long long r = it.u - prefix[s];
+  const int r = static_cast<int>(it.u - prefix[s]);  // < 2^31: unit counts are int32
   it.s = s;
   it.nu = nu;
   it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
   it.lo = window_lo(p, it.T);
   it.ulo = it.lo >> ur_shift;
-  it.kvh = static_cast<int>(r / nu);
-  it.j0 = it.ulo + static_cast<int>(r % nu);
+  it.kvh = r / nu;
+  it.j0 = it.ulo + (r - it.kvh * nu);
   it.j = it.j0;
   const long long seg_start = prefix[s] + static_cast<long long>(it.kvh) * nu;
   const long long seg_end = seg_start + nu;
