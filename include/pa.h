@@ -72,6 +72,7 @@ typedef enum {
 #define PA_DEVERR_SEQ_LEN 4u  /* seq_len < 0 or > max_blocks_per_seq*block_size */
 #define PA_DEVERR_TIMEOUT 8u  /* a bounded wait on an async copy gave up */
 #define PA_DEVERR_PAIR 16u    /* copy_blocks id outside [0, num_blocks) */
+#define PA_DEVERR_INTERNAL 32u /* a sizing invariant of the library failed (a bug; the result is wrong) */
 
 /*
  * pa_decode_workspace_bytes
@@ -80,7 +81,8 @@ typedef enum {
  *   count).  Returns 0 when the call needs no workspace (single pass) and
  *   (size_t)-1 when the sizes are rejected or no device is usable.
  *   The workspace must be zero-filled once before its first use; every
- *   completed pa_decode leaves it ready for the next call.
+ *   completed pa_decode leaves it ready for the next call (a call that set
+ *   PA_DEVERR_TIMEOUT may leave counters behind: zero it again after one).
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                  int block_size, int max_blocks_per_seq, int partition_size,

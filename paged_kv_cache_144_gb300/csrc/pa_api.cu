@@ -139,6 +139,8 @@ struct DecodePlan {
   int partition_units;      // as passed to the kernel (0 = balanced), in 8-row units
   size_t counters_bytes;
   size_t records;
+  int pending_cap;          // segments one consumer warp may have to merge
+  size_t pending_offset;    // bytes from the workspace start to the pending lists
   size_t bytes;             // total workspace bytes required
 };
 
@@ -164,16 +166,26 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
   if (pu == max_units) {  // one fragment per segment: no partial records
     plan->counters_bytes = 0;
     plan->records = 0;
+    plan->pending_cap = 0;
+    plan->pending_offset = 0;
     plan->bytes = 0;
     return PA_OK;
   }
   plan->counters_bytes = (static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int) + 255) / 256 * 256;
+  const size_t warps = static_cast<size_t>(plan->geo.ctas) * plan->geo.warps_per_cta;
   if (pu == 0) {
-    plan->records = 2ull * plan->geo.ctas * plan->geo.warps_per_cta;
+    // balanced split: only the first and the last fragment of a warp's range
+    // can be part of a split segment
+    plan->records = 2 * warps;
+    plan->pending_cap = 2;
   } else {
-    plan->records = static_cast<size_t>(num_seqs) * num_kv_heads * ((max_units + pu - 1) / pu);
+    // fixed partitions: dealt round-robin over the warps
+    const size_t parts = static_cast<size_t>(num_seqs) * num_kv_heads * ((max_units + pu - 1) / pu);
+    plan->records = parts;
+    plan->pending_cap = static_cast<int>((parts + warps - 1) / warps);
   }
-  plan->bytes = plan->counters_bytes + plan->records * plan->geo.record_floats * sizeof(float);
+  plan->pending_offset = plan->counters_bytes + (plan->records * plan->geo.record_floats * sizeof(float) + 255) / 256 * 256;
+  plan->bytes = plan->pending_offset + warps * plan->pending_cap * sizeof(int);
   return PA_OK;
 }
 
@@ -339,6 +351,8 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.v_cache = const_cast<void*>(v_cache);
   p.stages = plan.geo.stages;
   p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
+  p.pending = plan.bytes ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + plan.pending_offset) : nullptr;
+  p.pending_cap = plan.pending_cap;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)
                               : nullptr;
   const int st = cuda_status(pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream)),

@@ -906,6 +906,36 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     __syncwarp();
   };
 
+  // Merge of split segment x = s * H_kv + kvh by the warp that arrived last.
+  // 8-bit variants defer their merges until after the unit loop (list in the
+  // workspace): their unit loop needs every register, and an inlined merge
+  // inside it costs more than the merge itself.  16-bit variants merge at once.
+  constexpr bool kDeferMerge = Tr::B8;
+  int npend = 0;
+  int* const pend = p.pending + static_cast<int64_t>(blockIdx.x * W + c) * p.pending_cap;
+  auto merge_seg = [&](int x) {
+    const int s = x / Hkv, kvh = x - (x / Hkv) * Hkv;
+    const int per = (prefix[s + 1] - prefix[s]) / Hkv;  // units (balanced) or partitions (fixed) per KV head
+    MergeSlots ms;
+    ms.fixed = fixed;
+    ms.fixed_base = prefix[s] + kvh * per;
+    ms.U = U;
+    ms.nw_eff = nw_eff;
+    ms.seg_start = prefix[s] + static_cast<long long>(kvh) * per;
+    ms.first_w = 0;
+    int nfr = per;
+    if (!fixed) {
+      const long long seg_last = ms.seg_start + per - 1;
+      ms.first_w = static_cast<int>(((ms.seg_start + 1) * nw_eff - 1) / U);
+      nfr = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U) - ms.first_w + 1;
+    }
+    float vs = 1.f;
+    if constexpr (k8bit) vs = __ldg(p.v_scale + kvh);
+    const int64_t seq_row0 = static_cast<int64_t>(s) * QL * p.num_heads + static_cast<int64_t>(kvh) * G;
+    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0);
+    if (lane == 0) p.seg_counters[x] = 0;
+  };
+
   while (it.valid) {
     // ---- one fragment: units j0 .. jend-1 of segment (s, kvh)
     if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
@@ -1066,38 +1096,41 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         int old = 0;
         if (lane == 0) old = atomicAdd(p.seg_counters + it.s * Hkv + it.kvh, 1);
         old = __shfl_sync(0xffffffffu, old, 0);
-        // fragments of this segment and where their records live
-        int nfr, first_slot_w = 0;
-        long long seg_start = 0;
-        int parts = 0;
+        // fragments of this segment
+        int nfr;
         if (fixed) {
-          parts = (prefix[it.s + 1] - prefix[it.s]) / Hkv;
-          nfr = parts;
+          nfr = (prefix[it.s + 1] - prefix[it.s]) / Hkv;
         } else {
-          seg_start = prefix[it.s] + static_cast<long long>(it.kvh) * it.nu;
+          const long long seg_start = prefix[it.s] + static_cast<long long>(it.kvh) * it.nu;
           const long long seg_last = seg_start + it.nu - 1;
-          const int wf = static_cast<int>(((seg_start + 1) * nw_eff - 1) / U);
-          const int wl = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U);
-          nfr = wl - wf + 1;
-          first_slot_w = wf;
+          nfr = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U) - static_cast<int>(((seg_start + 1) * nw_eff - 1) / U) + 1;
         }
-        if (old == nfr - 1) {
-          __threadfence();
-          MergeSlots ms;
-          ms.fixed = fixed;
-          ms.fixed_base = fixed ? prefix[it.s] + it.kvh * parts : 0;
-          ms.first_w = first_slot_w;
-          ms.U = U;
-          ms.nw_eff = nw_eff;
-          ms.seg_start = seg_start;
-          merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype,
-                                        seq_row0);
-          if (lane == 0) p.seg_counters[it.s * Hkv + it.kvh] = 0;
+        if (old == nfr - 1) {  // last to arrive: this warp merges the segment
+          if constexpr (kDeferMerge) {
+            if (npend < p.pending_cap) {
+              if (lane == 0) pend[npend] = it.s * Hkv + it.kvh;
+              ++npend;
+            } else if (lane == 0) {
+              raise_error(p.err, PA_DEVERR_INTERNAL);
+            }
+          } else {
+            __threadfence();  // the other fragments' records, published before their arrivals
+            merge_seg(it.s * Hkv + it.kvh);
+          }
         }
       }
     }
     ++it.j;
     iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
+  }
+
+  // ---- deferred split merges (8-bit variants)
+  if constexpr (kDeferMerge) {
+    if (npend > 0) {
+      __syncwarp();
+      __threadfence();  // the other fragments' records, published before their arrivals
+      for (int i = 0; i < npend; ++i) merge_seg(pend[i]);
+    }
   }
 }
 

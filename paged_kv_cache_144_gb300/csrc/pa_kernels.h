@@ -77,6 +77,8 @@ struct DecodeParams {
   void* v_cache;
   float* part_records;          // split-K partial records (workspace)
   int* seg_counters;            // [num_seqs * num_kv_heads] arrival counters (workspace)
+  int* pending;                 // [consumer warps][pending_cap] segments a warp merges after its loop (workspace)
+  int pending_cap;
   unsigned int* err;            // per-device error word
   int stages;                   // K/V pipeline stages per warp
 };
