@@ -274,16 +274,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Two e4m3 codes (low 16 bits) -> f16x2, exact (every e4m3 value is an f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(w16));
-  return d;
-}
-
 // Four 8-bit cache codes w (byte i = element i) -> two f16x2 words: elements
 // (0, 1) in lo and (2, 3) in hi, low index in the low half, exact.
-//  * e4m3: hardware conversion.
+//  * e4m3: hardware conversion of each 16-bit half (exact: every e4m3 value is an f16).
 //  * int8 (value = code - zero point): each code c is placed as the low byte
 //    of the f16 pattern 0x64xx after flipping its sign bit, which reads as
 //    1024 + (c + 128); subtracting zp2 = f16x2(1152 + zero point) leaves
@@ -292,8 +285,11 @@ template <typename T>
 __device__ __forceinline__ void widen4(uint32_t w, uint32_t zp2, uint32_t& lo, uint32_t& hi);
 template <>
 __device__ __forceinline__ void widen4<e4m3_t>(uint32_t w, uint32_t /*zp2*/, uint32_t& lo, uint32_t& hi) {
-  lo = e4m3x2_to_f16x2(w & 0xffffu);
-  hi = e4m3x2_to_f16x2(w >> 16);
+  // the two byte pairs are the word's 16-bit halves: no masking or shifting
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 template <>
 __device__ __forceinline__ void widen4<i8_t>(uint32_t w, uint32_t zp2, uint32_t& lo, uint32_t& hi) {
