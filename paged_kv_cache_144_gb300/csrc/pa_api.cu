@@ -103,7 +103,8 @@ int gmax_for_rows(int rows) { return rows <= 1 ? 1 : (rows <= 4 ? 4 : (rows <= 8
 // d = 128), 64 for 8-bit caches with B >= 16 (the same 16 KB per stage, half
 // the refills per byte of 32 rows).  A unit spans at most four blocks, so
 // 64-row units need B >= 16.  Segments with more than 8 A rows (several
-// queries per sequence) use 16-row units: their accumulators fill the
+// queries per sequence) use 16-row units for 16-bit caches and 32-row units
+// for 8-bit caches (8 KB of K + V per stage): their accumulators fill the
 // registers.  PA_DECODE_UNIT_ROWS (16, 32; 64 for 8-bit caches) overrides it
 // (tuning).
 int unit_rows_for(int kv_dtype, int block_size, int gmax, bool append) {
@@ -111,7 +112,7 @@ int unit_rows_for(int kv_dtype, int block_size, int gmax, bool append) {
   const int env = append ? -1 : pa::tuning_override("PA_DECODE_UNIT_ROWS");  // fused append: defaults only
   if (env == 16 || env == 32) return env;
   if (env == 64 && q8 && block_size >= 16 && gmax <= 8) return 64;
-  if (gmax > 8) return 16;
+  if (gmax > 8) return q8 ? 32 : 16;  // 16-row variants: 8 KB of K + V per stage either way
   return q8 && block_size >= 16 ? 64 : 32;
 }
 

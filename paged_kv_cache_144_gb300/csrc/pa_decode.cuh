@@ -907,10 +907,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   };
 
   // Merge of split segment x = s * H_kv + kvh by the warp that arrived last.
-  // 8-bit variants defer their merges until after the unit loop (list in the
-  // workspace): their unit loop needs every register, and an inlined merge
-  // inside it costs more than the merge itself.  16-bit variants merge at once.
-  constexpr bool kDeferMerge = Tr::B8;
+  // 8-bit and 16-row variants defer their merges until after the unit loop
+  // (list in the workspace): their unit loop needs every register, and an
+  // inlined merge inside it costs more than the merge itself.  The other
+  // variants merge at once.
+  constexpr bool kDeferMerge = Tr::B8 || GM > 8;
   int npend = 0;
   int* const pend = p.pending + static_cast<int64_t>(blockIdx.x * W + c) * p.pending_cap;
   auto merge_seg = [&](int x) {
@@ -1124,7 +1125,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
   }
 
-  // ---- deferred split merges (8-bit variants)
+  // ---- deferred split merges (8-bit and 16-row variants)
   if constexpr (kDeferMerge) {
     if (npend > 0) {
       __syncwarp();
