@@ -906,14 +906,27 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     __syncwarp();
   };
 
-  // Merge of split segment x = s * H_kv + kvh by the warp that arrived last.
-  // 8-bit and 16-row variants defer their merges until after the unit loop
-  // (list in the workspace): their unit loop needs every register, and an
-  // inlined merge inside it costs more than the merge itself.  The other
-  // variants merge at once.
-  constexpr bool kDeferMerge = Tr::B8 || GM > 8;
+  // Merge of split segment x = s * H_kv + kvh by the warp that arrived last,
+  // after the unit loop (list in the workspace): an inlined merge inside the
+  // loop costs the loop registers, and the arrival itself does not wait: its
+  // atomic's result is looked at only at the next fragment end ("settle").
   int npend = 0;
   int* const pend = p.pending + static_cast<int64_t>(blockIdx.x * W + c) * p.pending_cap;
+  int arr_old = 0, arr_x = -1, arr_nfr = 0;  // the arrival not settled yet (x < 0: none)
+  auto settle = [&]() {
+    if (arr_x >= 0) {
+      const int old = __shfl_sync(0xffffffffu, arr_old, 0);
+      if (old == arr_nfr - 1) {  // last to arrive: this warp merges the segment
+        if (npend < p.pending_cap) {
+          if (lane == 0) pend[npend] = arr_x;
+          ++npend;
+        } else if (lane == 0) {
+          raise_error(p.err, PA_DEVERR_INTERNAL);
+        }
+      }
+      arr_x = -1;
+    }
+  };
   auto merge_seg = [&](int x) {
     const int s = x / Hkv, kvh = x - (x / Hkv) * Hkv;
     const int per = (prefix[s + 1] - prefix[s]) / Hkv;  // units (balanced) or partitions (fixed) per KV head
@@ -1092,11 +1105,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             rec[GM * D + GM + row] = lt[h];
           }
         }
-        __threadfence();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(p.seg_counters + it.s * Hkv + it.kvh, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
         // fragments of this segment
         int nfr;
         if (fixed) {
@@ -1106,32 +1114,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const long long seg_last = seg_start + it.nu - 1;
           nfr = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U) - static_cast<int>(((seg_start + 1) * nw_eff - 1) / U) + 1;
         }
-        if (old == nfr - 1) {  // last to arrive: this warp merges the segment
-          if constexpr (kDeferMerge) {
-            if (npend < p.pending_cap) {
-              if (lane == 0) pend[npend] = it.s * Hkv + it.kvh;
-              ++npend;
-            } else if (lane == 0) {
-              raise_error(p.err, PA_DEVERR_INTERNAL);
-            }
-          } else {
-            __threadfence();  // the other fragments' records, published before their arrivals
-            merge_seg(it.s * Hkv + it.kvh);
-          }
-        }
+        settle();
+        __syncwarp();  // every lane's record stores come before lane 0's release
+        if (lane == 0) arr_old = atom_add_release_gpu(p.seg_counters + it.s * Hkv + it.kvh, 1);
+        arr_x = it.s * Hkv + it.kvh;
+        arr_nfr = nfr;
       }
     }
     ++it.j;
     iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
   }
 
-  // ---- deferred split merges (8-bit and 16-row variants)
-  if constexpr (kDeferMerge) {
-    if (npend > 0) {
-      __syncwarp();
-      __threadfence();  // the other fragments' records, published before their arrivals
-      for (int i = 0; i < npend; ++i) merge_seg(pend[i]);
-    }
+  // ---- the split merges this warp won
+  settle();
+  if (npend > 0) {
+    __syncwarp();
+    __threadfence();  // acquire: the other fragments' records, released by their arrivals
+    for (int i = 0; i < npend; ++i) merge_seg(pend[i]);
   }
 }
 
