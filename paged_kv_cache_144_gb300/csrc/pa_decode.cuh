@@ -48,10 +48,12 @@
 //    per-head K scale multiplies the scores, the V scale the final divide,
 //    and q is rounded to f16 for the product.
 //  * Split segments: a warp whose range covers only part of a segment writes
-//    its (m, l, acc) record to the workspace and bumps the segment's arrival
-//    counter; the warp that arrives last merges all records with the same
-//    recurrence, writes out[s, kvh*G .. kvh*G+G-1] and resets the counter.
-//    Nothing waits on another warp, so the kernel cannot deadlock.
+//    its (m, l, acc) record to the workspace and arrives on the segment's
+//    counter (a release atomic whose result it reads one fragment later, so
+//    arriving never stalls it); the warp that arrived last merges all records
+//    with the same recurrence after its own unit loop, writes
+//    out[s, kvh*G .. kvh*G+G-1] and resets the counter.  Nothing waits on
+//    another warp, so the kernel cannot deadlock.
 //  * Every wait on an mbarrier is bounded by %globaltimer; on expiry the warp
 //    records PA_DEVERR_TIMEOUT, waits (bounded) for its own copies and
 //    returns.
@@ -234,10 +236,10 @@ struct MergeSlots {
 
 // Merges the nfr partial (m, l, acc) records of one segment with the
 // online-softmax recurrence and writes the output rows of its R = q_len * G
-// (query, head) rows.  Run by the warp that arrived last.  Lane f holds record f's (m, l) and weights
-// e^(m_f - M); the warp then walks the records RB at a time with all their
-// loads in flight, lane i owning head_dim columns [i*D/32, (i+1)*D/32) of
-// every head.
+// (query, head) rows.  Run by the warp that arrived last, after its unit
+// loop.  Lane f holds record f's (m, l) and weights e^(m_f - M); the warp
+// then walks the records RB at a time with all their loads in flight, lane i
+// owning head_dim columns [i*D/32, (i+1)*D/32) of every head.
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
                                               int G, int num_heads, float vs, void* out, int out_dtype,

@@ -44,9 +44,9 @@ def out_tolerance(ref: np.ndarray, out_fmt: str) -> np.ndarray:
 
 
 def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda", window=0):
-    """q of shape [S, L, H_q, d] (L > 1) decodes L queries per sequence (pa_decode_ex q_len)."""
-    """Fill the cache (FP8: quantising writes), append the new token, decode.
+    """Fill the cache (8-bit caches: quantising writes), append the new token, decode.
 
+    q of shape [S, L, H_q, d] (L > 1) decodes L queries per sequence (pa_decode_ex q_len).
     Returns (out float64 numpy, k_cache numpy, v_cache numpy, device error bits).
     """
     import torch

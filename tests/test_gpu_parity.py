@@ -50,6 +50,16 @@ def test_long_group8_extreme_logits(q_mult):
     _check(b, workloads.host_values(b, seed=2, q_mult=q_mult))
 
 
+@pytest.mark.parametrize("wl,P", [("long_32k", 16), ("fp8_mix", 64), ("int8_mix", 64)])
+def test_fixed_small_partitions_many_merges_per_warp(wl, P):
+    """Fixed partitions of one unit or so: every warp processes and later merges many split segments
+    (its list of won merges is sized from the partition count)."""
+    kw = dict(num_seqs=4, lengths=("const", 3000)) if wl == "long_32k" else \
+        dict(num_seqs=24, lengths=("lognormal", 6.5, 1.0, 16, 3000))
+    b = workloads.make_batch(wl, seed=71, **kw)
+    _check(b, workloads.host_values(b, seed=71), partition_size=P)
+
+
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
