@@ -343,29 +343,35 @@ def run_ours(args):
     no_pairs = torch.empty((0, 2), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
+    pdl = not args.no_pdl
+
+    def step(i):
+        # one step as a serving loop issues it: nothing between its launches, so the decode's set-up
+        # (lengths, prefix sums, block-table prefetch) overlaps the launch before it (pdl)
         kc, vc = caches[i % replicas]
         if args.fused:
             # one launch: the cache write of the new rows fused into the decode
-            if ev is not None:
-                ev[0].record(stream)
             pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                       partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
                       k_zero_point=kz, v_zero_point=vz, k_new=k_new, v_new=v_new, k_inv_scale=kis,
-                      v_inv_scale=vis)
-            if ev is not None:
-                ev[1].record(stream)
+                      v_inv_scale=vis, pdl=pdl)
             return
         pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
                              v_zero_point=vz, stream=stream)
         pa.copy_blocks(kc, vc, no_pairs, stream=stream)          # no shared block is written: no launch
-        if ev is not None:
-            ev[0].record(stream)
         pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                   partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                  k_zero_point=kz, v_zero_point=vz)
-        if ev is not None:
-            ev[1].record(stream)
+                  k_zero_point=kz, v_zero_point=vz, pdl=pdl)
+
+    def decode_alone(i, ev):
+        # the decode kernel by itself, an ordinary launch between two events (the roofline's duration)
+        kc, vc = caches[i % replicas]
+        extra = dict(k_new=k_new, v_new=v_new, k_inv_scale=kis, v_inv_scale=vis) if args.fused else {}
+        ev[0].record(stream)
+        pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
+                  partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
+                  k_zero_point=kz, v_zero_point=vz, **extra)
+        ev[1].record(stream)
 
     uuid = None
     try:
@@ -386,13 +392,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(K):
-        step(args.warmup + i, dec_ev[i])
+        step(args.warmup + i)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = sampler.stop() if sampler else None
     elapsed_ms = t_start.elapsed_time(t_end)
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+    # second timed region: K decode launches alone, each between two events on the launching stream
+    for i in range(3):
+        decode_alone(i, dec_ev[0])
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        decode_alone(args.warmup + i, dec_ev[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    dec_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in dec_ev])), world)
     err = pa.get_device_error()
     if err != 0:
         raise RuntimeError(f"device error bits {err} in the timed region")
@@ -418,13 +433,13 @@ def run_ours(args):
                 pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                           partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
                           k_zero_point=kz, v_zero_point=vz, k_new=d_k, v_new=d_v, k_inv_scale=kis,
-                          v_inv_scale=vis)
+                          v_inv_scale=vis, pdl=pdl)
             else:
                 pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis,
                                      k_zero_point=kz, v_zero_point=vz, stream=stream)
                 pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                           partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                          k_zero_point=kz, v_zero_point=vz)
+                          k_zero_point=kz, v_zero_point=vz, pdl=pdl)
             h_out.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -469,7 +484,10 @@ def run_ours(args):
             "window": args.window or None,
             "q_len": args.q_len,
             "step": ("pa_decode_ex with the new token's cache write fused (one launch)" if args.fused
-                     else "reshape_and_cache(1 new token/seq) + pa_decode"),
+                     else "reshape_and_cache(1 new token/seq) + pa_decode") +
+                    (", decode launched with programmatic dependent launch" if pdl else ""),
+            "kernel_timing": "a second timed loop of K decode launches alone (ordinary launches), "
+                             "CUDA events around each on the launching stream, same KV rotation",
             "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
             "seed": args.seed,
             "launch": geometry,
@@ -559,15 +577,20 @@ def run_beam(args):
                                           pa.PA_F16)
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
+    pdl = not args.no_pdl
+
+    def step(i):
         kc, vc = caches[i % replicas]
         pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
+        pa.decode(out, q, kc, vc, tables, lens, H, sc["scale"], B, partition_size=args.partition_size,
+                  workspace=ws, stream=stream, pdl=pdl)
+
+    def decode_alone(i, ev):
+        kc, vc = caches[i % replicas]
+        ev[0].record(stream)
         pa.decode(out, q, kc, vc, tables, lens, H, sc["scale"], B, partition_size=args.partition_size,
                   workspace=ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+        ev[1].record(stream)
 
     sampler = None
     try:
@@ -586,15 +609,23 @@ def run_beam(args):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(K):
-        step(args.warmup + i, dec_ev[i])
+        step(args.warmup + i)
     t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(3):
+        decode_alone(i, dec_ev[0])
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        decode_alone(args.warmup + i, dec_ev[i])
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
     if pa.get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
     ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / K
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+    dec_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in dec_ev])), world)
     peaks = load_peaks()
     total_step = sum_over_ranks(float(decode_bytes + append_bytes), world)
     value = total_step / (ms_step * 1e-3) / 1e9
@@ -608,7 +639,10 @@ def run_beam(args):
         "config": {"workload": f"beam_cow: {WORKLOAD_TEXT['beam_cow']}", "num_seqs": S, "num_heads": Hq,
                    "num_kv_heads": H, "head_dim": D, "block_size": B, "context_tokens": int(lens_np.sum()),
                    "cow_pairs": n_pairs, "unique_kv_bytes": unique_kv, "logical_kv_bytes": logical_kv,
-                   "step": "reshape_and_cache(1 new token/beam) + pa_decode",
+                   "step": "reshape_and_cache(1 new token/beam) + pa_decode" +
+                           (", decode launched with programmatic dependent launch" if pdl else ""),
+                   "kernel_timing": "a second timed loop of K decode launches alone (ordinary launches), "
+                                    "CUDA events around each on the launching stream",
                    "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 "
                          f"({l2 / 1e6:.0f} MB); the shared prompt is read by all beams within one launch",
                    "seed": args.seed, "launch": geometry},
@@ -715,6 +749,8 @@ def main():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--replicas", type=int, default=0, help="KV pool replicas to rotate (0 = enough for > 4x L2)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch the step's decode as an ordinary launch (no programmatic dependent launch)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -181,6 +181,17 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            PA_ERR_UNSUPPORTED.  This is the verification step of
  *            speculative decoding, which the explainer names alongside paged
  *            KV memory.
+ *   pdl      nonzero: launch with programmatic dependent launch, so that the
+ *            decode's set-up overlaps the kernel launched just before it on
+ *            `stream` (typically pa_reshape_and_cache of the same step, whose
+ *            kernel lets its dependents start at once).  During that overlap
+ *            the decode reads seq_lens and block_tables only; it reads q, the
+ *            caches, the scales and the new rows, and writes out, the cache
+ *            and the workspace, only after that kernel has finished.  So with
+ *            pdl on, seq_lens and block_tables must not be written by the
+ *            kernel launched just before this call (host copies and earlier
+ *            kernels are fine).  0: an ordinary launch.  Engineering addition
+ *            with no counterpart in the pages.
  */
 typedef struct pa_decode_options {
   size_t struct_size;
@@ -194,6 +205,7 @@ typedef struct pa_decode_options {
   const float* k_inv_scale;
   const float* v_inv_scale;
   int32_t q_len;
+  int32_t pdl;
 } pa_decode_options;
 
 int pa_decode_ex(void* out, pa_dtype out_dtype,

@@ -356,7 +356,8 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.pending_cap = plan.pending_cap;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)
                               : nullptr;
-  const int st = cuda_status(pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream)),
+  const int st = cuda_status(pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream),
+                                              o.pdl != 0),
                               "pa_decode launch");
   if (st != PA_OK) {
     const size_t n = strlen(g_last_error);

@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const float* __restrict__ k_inv_scale, const float* __restrict__ v_inv_scale,
     const int32_t* __restrict__ k_zero_point, const int32_t* __restrict__ v_zero_point, unsigned int* err) {
   constexpr int EPL = D / 32;  // elements per lane: 2 or 4
+  // a decode launched after this write with programmatic serialization may
+  // start its set-up now; it waits for this grid before it reads the cache
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;
@@ -100,6 +103,7 @@ constexpr int kCopyBytesPerCta = 16384;  // 256 threads x 16 B x 4
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_blocks,
     int64_t block_bytes, const int32_t* __restrict__ pairs, unsigned int* err) {
+  griddep_launch_dependents();  // as in the cache write: dependents wait before reading the pools
   const int pair = blockIdx.y;
   const int32_t src = pairs[2 * pair];
   const int32_t dst = pairs[2 * pair + 1];

@@ -118,11 +118,26 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16-byte asynchronous copy global -> shared, cached in L2 only (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's committed cp.async groups are pending.
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Programmatic dependent launch.  griddep_wait: returns once the grid this
+// one was allowed to overlap (launched just before it on the stream with the
+// programmatic-serialization attribute on this one) has finished and its
+// writes are visible; returns at once when there is no such grid.
+// griddep_launch_dependents: lets a grid launched after this one with that
+// attribute start now instead of when this grid's blocks exit.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -362,6 +377,18 @@ __device__ __forceinline__ void store_out(void* out, int dtype, int64_t i, float
   } else {
     reinterpret_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
   }
+}
+
+// Shared-memory loads ordered with the surrounding memory operations (after a cp.async wait).
+__device__ __forceinline__ float lds_f32_ordered(uint32_t addr) {
+  float r;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(addr) : "memory");
+  return r;
+}
+__device__ __forceinline__ float4 lds_f32x4_ordered(uint32_t addr) {
+  float4 r;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr) : "memory");
+  return r;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

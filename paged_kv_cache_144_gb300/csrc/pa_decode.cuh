@@ -113,6 +113,8 @@ struct DecodeTraits {
   __host__ __device__ static constexpr int warp_smem(int ns, int stage) { return OFF_STAGES + ns * stage; }
   // partial record: acc as [D][GM] (head fastest), then m[GM], l[GM]
   static constexpr int REC = align_up_c(GM * (D + 2), 4);
+  // the split merge stages records in a consumer's (at least two) idle stages
+  static_assert(2 * STAGE >= REC * 4, "a record fits the stages of one consumer");
 };
 
 // Length of sequence s clamped to the table's capacity (error bit if outside).
@@ -237,135 +239,92 @@ struct MergeSlots {
 // Merges the nfr partial (m, l, acc) records of one segment with the
 // online-softmax recurrence and writes the output rows of its R = q_len * G
 // (query, head) rows.  Run by the warp that arrived last, after its unit
-// loop.  Lane f holds record f's (m, l) and weights e^(m_f - M); the warp
-// then walks the records RB at a time with all their loads in flight, lane i
-// owning head_dim columns [i*D/32, (i+1)*D/32) of every head.
+// loop, when its own pipeline stages are idle: the records are copied into
+// those stages (buf, room for cap records) a batch at a time with cp.async,
+// every copy of a batch in flight at once, and folded from shared memory.
+// A batch whose records raise the running maximum rescales what was folded
+// before (the same recurrence across batches).  Lane i owns head_dim columns
+// i, i + 32, ... of every row.  Records are folded in fragment order, so the
+// result does not depend on which warp merges.
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
                                               int G, int num_heads, float vs, void* out, int out_dtype,
-                                              int64_t seq_row0) {
-  constexpr int EPL = D / 32;                 // columns per lane
-  constexpr int RC = GM > 8 ? 8 : GM;         // rows merged per pass (bounds the registers)
-  constexpr int NF = EPL * RC;                // floats per lane per record and pass
-  constexpr int RB = NF >= 32 ? 2 : (NF >= 16 ? 4 : 8);  // 64 floats in flight per lane (registers)
-  const int e0 = lane * EPL;
+                                              int64_t seq_row0, uint32_t buf, int cap) {
+  constexpr int EPL = D / 32;       // columns per lane
+  constexpr int CH = REC / 4;       // 16-byte chunks of one record
+  constexpr uint32_t RECB = REC * 4;
+  static_assert(REC % 4 == 0, "records are whole 16-byte chunks");
+  cap = cap < 32 ? cap : 32;        // slots of a batch are held one per lane
+  float M[GM], L[GM], o[EPL][GM];
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+    M[g] = -INFINITY;
+    L[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e][g] = 0.f;
+  }
 #pragma unroll 1
-  for (int c0 = 0; c0 < GM; c0 += RC) {
-    if (GM > 8 && c0 >= R) break;
-    // records 0..31: slot, m and l of rows c0 .. c0+RC-1 on lane f (kept for the second pass)
-    int slot0 = 0;
-    float m0[RC], l0[RC], M[RC], L[RC];
-#pragma unroll
-    for (int g = 0; g < RC; ++g) {
-      m0[g] = -INFINITY;
-      l0[g] = 0.f;
-      L[g] = 0.f;
+  for (int f0 = 0; f0 < nfr; f0 += cap) {
+    const int nb = min(cap, nfr - f0);
+    const int my_slot = lane < nb ? ms.slot(f0 + lane) : 0;
+#pragma unroll 1
+    for (int k = 0; k < nb; ++k) {
+      const float* src = records + static_cast<int64_t>(__shfl_sync(0xffffffffu, my_slot, k)) * REC;
+      for (int ch = lane; ch < CH; ch += 32) cp_async16(buf + k * RECB + ch * 16, src + ch * 4);
     }
-    if (lane < nfr) {
-      slot0 = ms.slot(lane);
-      const float* rf = records + static_cast<int64_t>(slot0) * REC + GM * D + c0;
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();  // every lane's copies have landed
+    // running maximum over this batch; what was folded before is rescaled to it
 #pragma unroll
-      for (int g = 0; g < RC; ++g) {
-        m0[g] = __ldcg(rf + g);
-        l0[g] = __ldcg(rf + GM + g);
-      }
+    for (int g = 0; g < GM; ++g) {
+      float mb = M[g];
+      for (int k = 0; k < nb; ++k) mb = fmaxf(mb, lds_f32_ordered(buf + k * RECB + (GM * D + g) * 4));
+      const float w = M[g] == -INFINITY ? 0.f : exp2f(M[g] - mb);  // nothing folded yet: 0
+      L[g] *= w;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[e][g] *= w;
+      M[g] = mb;
     }
+#pragma unroll 1
+    for (int k = 0; k < nb; ++k) {
+      const uint32_t rk = buf + k * RECB;
+      float wk[GM];
 #pragma unroll
-    for (int g = 0; g < RC; ++g) M[g] = m0[g];
-    for (int f0 = 32; f0 < nfr; f0 += 32) {
-      if (f0 + lane < nfr) {
-        const float* rf = records + static_cast<int64_t>(ms.slot(f0 + lane)) * REC + GM * D + c0;
-#pragma unroll
-        for (int g = 0; g < RC; ++g) M[g] = fmaxf(M[g], __ldcg(rf + g));
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < RC; ++g)
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
-    float o[NF];  // [column e][row g] of this pass
-#pragma unroll
-    for (int i = 0; i < NF; ++i) o[i] = 0.f;
-    for (int f0 = 0; f0 < nfr; f0 += 32) {
-      const int nb = min(32, nfr - f0);
-      float wf[RC];
-      int my_slot = slot0;
-      float mf[RC], lf[RC];
-#pragma unroll
-      for (int g = 0; g < RC; ++g) {
-        mf[g] = m0[g];
-        lf[g] = l0[g];
-      }
-      if (f0 > 0 && lane < nb) {
-        my_slot = ms.slot(f0 + lane);
-        const float* rf = records + static_cast<int64_t>(my_slot) * REC + GM * D + c0;
-#pragma unroll
-        for (int g = 0; g < RC; ++g) {
-          mf[g] = __ldcg(rf + g);
-          lf[g] = __ldcg(rf + GM + g);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < RC; ++g) {
+      for (int g = 0; g < GM; ++g) {
+        const float mk = lds_f32_ordered(rk + (GM * D + g) * 4);
         // an empty record (m = -inf: its rows saw nothing) weighs 0
-        wf[g] = (lane < nb && mf[g] != -INFINITY) ? exp2f(mf[g] - M[g]) : 0.f;
-        L[g] += wf[g] * (lane < nb ? lf[g] : 0.f);
+        wk[g] = mk == -INFINITY ? 0.f : exp2f(mk - M[g]);
+        L[g] = fmaf(wk[g], lds_f32_ordered(rk + (GM * D + GM + g) * 4), L[g]);
       }
-      for (int k = 0; k < nb; k += RB) {
-        float v[RB][NF];
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          const int sr = __shfl_sync(0xffffffffu, my_slot, (k + r) & 31);
-          if (k + r < nb) {
-            const float* rf = records + static_cast<int64_t>(sr) * REC;
-            if constexpr (RC % 4 == 0) {
+      for (int e = 0; e < EPL; ++e) {
+        const uint32_t a = rk + static_cast<uint32_t>((lane + 32 * e) * GM) * 4;  // acc[d][0..GM) of column d
+        if constexpr (GM % 4 == 0) {
 #pragma unroll
-              for (int e = 0; e < EPL; ++e)
-#pragma unroll
-                for (int g = 0; g < RC; g += 4) {
-                  const float4 x = __ldcg(reinterpret_cast<const float4*>(rf + (e0 + e) * GM + c0 + g));
-                  v[r][e * RC + g] = x.x;
-                  v[r][e * RC + g + 1] = x.y;
-                  v[r][e * RC + g + 2] = x.z;
-                  v[r][e * RC + g + 3] = x.w;
-                }
-            } else {  // one row (GM == 1): the lane's EPL columns are contiguous
-#pragma unroll
-              for (int e = 0; e < EPL; e += 2) {
-                const float2 x = __ldcg(reinterpret_cast<const float2*>(rf + e0 + e));
-                v[r][e] = x.x;
-                v[r][e + 1] = x.y;
-              }
-            }
+          for (int g = 0; g < GM; g += 4) {
+            const float4 x = lds_f32x4_ordered(a + g * 4);
+            o[e][g] = fmaf(wk[g], x.x, o[e][g]);
+            o[e][g + 1] = fmaf(wk[g + 1], x.y, o[e][g + 1]);
+            o[e][g + 2] = fmaf(wk[g + 2], x.z, o[e][g + 2]);
+            o[e][g + 3] = fmaf(wk[g + 3], x.w, o[e][g + 3]);
           }
-        }
+        } else {
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-#pragma unroll
-          for (int g = 0; g < RC; ++g) {
-            const float w = __shfl_sync(0xffffffffu, wf[g], (k + r) & 31);
-            if (k + r < nb) {
-#pragma unroll
-              for (int e = 0; e < EPL; ++e) o[e * RC + g] = fmaf(w, v[r][e * RC + g], o[e * RC + g]);
-            }
-          }
+          for (int g = 0; g < GM; ++g) o[e][g] = fmaf(wk[g], lds_f32_ordered(a + g * 4), o[e][g]);
         }
       }
     }
+    __syncwarp();  // every lane has read the batch before the next one overwrites it
+  }
 #pragma unroll
-    for (int g = 0; g < RC; ++g)
+  for (int g = 0; g < GM; ++g) {
+    if (g < R) {
+      // row g = (query g / G, head g % G) of the group
+      const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>(g / G) * num_heads + g % G : seq_row0 + g;
+      const float inv = L[g] > 0.f ? vs / L[g] : 0.f;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) L[g] += __shfl_xor_sync(0xffffffffu, L[g], off);
-#pragma unroll
-    for (int g = 0; g < RC; ++g) {
-      const int row = c0 + g;
-      if (row < R) {
-        // row = (query row / G, head row % G) of the group
-        const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>(row / G) * num_heads + row % G : seq_row0 + row;
-        const float inv = L[g] > 0.f ? vs / L[g] : 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, orow * D + e0 + e, o[e * RC + g] * inv);
-      }
+      for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, orow * D + lane + 32 * e, o[e][g] * inv);
     }
   }
 }
@@ -447,15 +406,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     if (threadIdx.x == 0) prefix[S] = carry;
   }
 
-  // ---- 2. empty sequences attend to nothing: their outputs are zero
-  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
-    if (lens[s] == 0) {
-      const int64_t n = static_cast<int64_t>(p.q_len) * p.num_heads * D;
-      for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
-    }
-  }
-
-  // ---- 3. barriers of every consumer ring
+  // ---- 2. barriers of every consumer ring
   if (threadIdx.x == 0) {
     for (int c = 0; c < W; ++c) {
       const uint32_t cb = base_u32 + c * wsm;
@@ -469,7 +420,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   }
   __syncthreads();
 
-  // ---- 4. the share of consumer c (global consumer id gc)
+  // ---- 3. the share of consumer c (global consumer id gc)
   const int nw_total = gridDim.x * W;
   const long long U = prefix[S];
   long long want = (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp;
@@ -524,6 +475,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       if (++ah.j == ah.jend) iter_next_fragment(ah, prefix, p, fixed, Tr::UR_SHIFT);
     };
     while (ah.valid && pf < kTablePrefetch) fetch_tables();
+    // Everything above reads only seq_lens and block_tables.  Under a
+    // programmatic dependent launch the grid before this one on the stream
+    // may still be running (it may be writing the cache, q or out); the first
+    // copy of K/V or q, and every write, comes after it has finished.  The
+    // consumers start only on data this warp copies, so they are ordered
+    // after this wait as well.
+    griddep_wait();
+    // empty sequences attend to nothing: their outputs are zero
+    for (int s = blockIdx.x * 32 + lane; s < S; s += gridDim.x * 32) {
+      if (lens[s] == 0) {
+        const int64_t n = static_cast<int64_t>(p.q_len) * p.num_heads * D;
+        for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
+      }
+    }
     while (__any_sync(0xffffffffu, it.valid)) {
       bool did = false;
       if (it.valid) {
@@ -948,7 +913,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     float vs = 1.f;
     if constexpr (k8bit) vs = __ldg(p.v_scale + kvh);
     const int64_t seq_row0 = static_cast<int64_t>(s) * QL * p.num_heads + static_cast<int64_t>(kvh) * G;
-    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0);
+    // this warp's stages are idle after its unit loop: the records are staged there
+    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
+                                  wbase_u32 + Tr::OFF_STAGES, (NS * STG) / (Tr::REC * 4));
     if (lane == 0) p.seg_counters[x] = 0;
   };
 
@@ -1195,10 +1162,26 @@ struct DecodeVariant {
   }
 
   static cudaError_t launch(const DecodeGeometry& g, const DecodeParams& p, const CUtensorMap& tk,
-                            const CUtensorMap& tv, cudaStream_t stream) {
+                            const CUtensorMap& tv, cudaStream_t stream, bool pdl) {
     (void)cudaGetLastError();  // an earlier unrelated error must not be reported as this launch's
-    paged_decode_kernel<QT, KVT, D, GM, UR, AP><<<g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, stream>>>(tk, tv, p);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (pdl) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(g.ctas);
+      cfg.blockDim = dim3((g.warps_per_cta + 1) * 32);
+      cfg.dynamicSmemBytes = g.smem_bytes;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<QT, KVT, D, GM, UR, AP>, tk, tv, p);
+      if (e == cudaSuccess) e = cudaGetLastError();
+    } else {
+      paged_decode_kernel<QT, KVT, D, GM, UR, AP><<<g.ctas, (g.warps_per_cta + 1) * 32, g.smem_bytes, stream>>>(tk, tv, p);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) {
       cudaFuncAttributes fa;
       if (cudaFuncGetAttributes(&fa, paged_decode_kernel<QT, KVT, D, GM, UR, AP>) == cudaSuccess)

@@ -85,10 +85,10 @@ bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
 }
 
 cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,
-                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream, bool pdl) {
 #define PA_LAUNCH(QT, KVT, D, GM, UR, AP) \
   if (PA_MATCH(QT, KVT, D, GM, UR, AP))    \
-    return decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(geo, p, tk, tv, stream);
+    return decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(geo, p, tk, tv, stream, pdl);
   PA_DECODE_VARIANTS(PA_LAUNCH)
 #undef PA_LAUNCH
   return cudaErrorInvalidValue;

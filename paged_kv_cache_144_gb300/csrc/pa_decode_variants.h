@@ -75,7 +75,8 @@
   cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(const DecodeGeometry& geo,    \
                                                               const DecodeParams& p,              \
                                                               const CUtensorMap& tk,              \
-                                                              const CUtensorMap& tv, cudaStream_t stream);
+                                                              const CUtensorMap& tv, cudaStream_t stream, \
+                                                              bool pdl);
 #define PA_DEFINE_VARIANT(QT, KVT, D, GM, UR, AP)                                                  \
   bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(int num_seqs, DecodeGeometry* geo) { \
     return DecodeVariant<QT, KVT, D, GM, UR, AP>::geometry(num_seqs, geo);                         \
@@ -83,8 +84,9 @@
   cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(const DecodeGeometry& geo,    \
                                                               const DecodeParams& p,              \
                                                               const CUtensorMap& tk,              \
-                                                              const CUtensorMap& tv, cudaStream_t stream) { \
-    return DecodeVariant<QT, KVT, D, GM, UR, AP>::launch(geo, p, tk, tv, stream);                  \
+                                                              const CUtensorMap& tv, cudaStream_t stream, \
+                                                              bool pdl) {                         \
+    return DecodeVariant<QT, KVT, D, GM, UR, AP>::launch(geo, p, tk, tv, stream, pdl);             \
   }
 
 namespace pa {

@@ -111,7 +111,11 @@ bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo);  
 // Geometry and kernel attributes of the last rejected decode launch on this thread.
 const char* launch_failure_note();
 
+// pdl: launch with programmatic stream serialization, so that the kernel's
+// set-up (which reads only seq_lens and block_tables) overlaps the kernel
+// before it on the stream; the kernel waits for that one before anything else.
 cudaError_t launch_decode(const DecodeKey& key, const DecodeGeometry& geo, const DecodeParams& p,
-                          const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);
+                          const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream,
+                          bool pdl = false);
 
 }  // namespace pa

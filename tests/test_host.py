@@ -246,3 +246,45 @@ def test_shard_sequences_covers_all():
         spans = [workloads.shard_sequences(n, r, w) for r in range(w)]
         assert spans[0][0] == 0 and spans[-1][1] == n
         assert all(spans[i][1] == spans[i + 1][0] for i in range(w - 1))
+
+
+def _c_layout(struct_name, fields):
+    """sizeof and offsetof of a pa.h struct, from a C program compiled with the system compiler."""
+    import os
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    body = "".join(f'  printf("%zu\\n", offsetof({struct_name}, {f}));\n' for f in fields)
+    src = ("#include <stddef.h>\n#include <stdio.h>\n#include \"pa.h\"\n"
+           f"int main(void) {{\n  printf(\"%zu\\n\", sizeof({struct_name}));\n{body}  return 0;\n}}\n")
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        with open(c, "w") as fh:
+            fh.write(src)
+        subprocess.run([cc, "-std=c99", "-I", inc, c, "-o", exe], check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()
+    return int(out[0]), [int(x) for x in out[1:]]
+
+
+@pytest.mark.parametrize("cls,cname", [(pa.DecodeOptions, "pa_decode_options"),
+                                       (_lib.CacheWriteOptions, "pa_cache_write_options")])
+def test_option_structs_match_the_header_layout(cls, cname):
+    names = [n for n, _ in cls._fields_]
+    size, offsets = _c_layout(cname, names)
+    assert ctypes.sizeof(cls) == size
+    assert [getattr(cls, n).offset for n in names] == offsets
+
+
+def test_decode_ex_pdl_option_validation(lib):
+    # the launch mode changes no argument rule: empty batches succeed, bad shapes still fail
+    assert _decode_ex(pa.DecodeOptions(pdl=1), S=0) == pa.PA_OK
+    assert _decode_ex(pa.DecodeOptions(pdl=1, window=-1)) == pa.PA_ERR_SHAPE
+    assert _decode_ex(pa.DecodeOptions(pdl=1), B=12) == pa.PA_ERR_UNSUPPORTED
+    # a caller compiled before the field existed (shorter struct_size) reads it as 0
+    old = pa.DecodeOptions(pdl=1)
+    old.struct_size = pa.DecodeOptions.pdl.offset
+    assert _decode_ex(old, S=0) == pa.PA_OK
