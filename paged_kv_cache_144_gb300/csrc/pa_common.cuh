@@ -379,18 +379,6 @@ __device__ __forceinline__ void store_out(void* out, int dtype, int64_t i, float
   }
 }
 
-// Shared-memory loads ordered with the surrounding memory operations (after a cp.async wait).
-__device__ __forceinline__ float lds_f32_ordered(uint32_t addr) {
-  float r;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(addr) : "memory");
-  return r;
-}
-__device__ __forceinline__ float4 lds_f32x4_ordered(uint32_t addr) {
-  float4 r;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr) : "memory");
-  return r;
-}
-
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 r;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -240,26 +240,26 @@ struct MergeSlots {
 // online-softmax recurrence and writes the output rows of its R = q_len * G
 // (query, head) rows.  Run by the warp that arrived last, after its unit
 // loop, when its own pipeline stages are idle: the records are copied into
-// those stages (buf, room for cap records) a batch at a time with cp.async,
-// every copy of a batch in flight at once, and folded from shared memory.
-// A batch whose records raise the running maximum rescales what was folded
-// before (the same recurrence across batches).  Lane i owns head_dim columns
-// i, i + 32, ... of every row.  Records are folded in fragment order, so the
-// result does not depend on which warp merges.
+// those stages (buf / bufp, room for cap records) a batch at a time with
+// cp.async, every copy of a batch in flight at once, and folded from shared
+// memory.  Lane k holds record k's (m, l) of the batch and its weights
+// e^(m_k - M); a batch whose records raise the running maximum M rescales
+// what was folded before (the same recurrence across batches).  Lane i owns
+// head_dim columns i, i + 32, ... of every row.  Records are folded in
+// fragment order, so the result does not depend on which warp merges.
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
                                               int G, int num_heads, float vs, void* out, int out_dtype,
-                                              int64_t seq_row0, uint32_t buf, int cap) {
+                                              int64_t seq_row0, uint32_t buf, const float* bufp, int cap) {
   constexpr int EPL = D / 32;       // columns per lane
   constexpr int CH = REC / 4;       // 16-byte chunks of one record
-  constexpr uint32_t RECB = REC * 4;
   static_assert(REC % 4 == 0, "records are whole 16-byte chunks");
-  cap = cap < 32 ? cap : 32;        // slots of a batch are held one per lane
-  float M[GM], L[GM], o[EPL][GM];
+  cap = cap < 32 ? cap : 32;        // the records of a batch are held one per lane
+  float M[GM], Lp[GM], o[EPL][GM];  // running max, this lane's share of the sum, accumulator
 #pragma unroll
   for (int g = 0; g < GM; ++g) {
     M[g] = -INFINITY;
-    L[g] = 0.f;
+    Lp[g] = 0.f;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e][g] = 0.f;
   }
@@ -270,48 +270,49 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
 #pragma unroll 1
     for (int k = 0; k < nb; ++k) {
       const float* src = records + static_cast<int64_t>(__shfl_sync(0xffffffffu, my_slot, k)) * REC;
-      for (int ch = lane; ch < CH; ch += 32) cp_async16(buf + k * RECB + ch * 16, src + ch * 4);
+      for (int ch = lane; ch < CH; ch += 32) cp_async16(buf + static_cast<uint32_t>(k * REC + ch * 4) * 4, src + ch * 4);
     }
     cp_async_commit();
     cp_async_wait<0>();
     __syncwarp();  // every lane's copies have landed
-    // running maximum over this batch; what was folded before is rescaled to it
+    float wk[GM];  // lane k: weight of record k per row
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
-      float mb = M[g];
-      for (int k = 0; k < nb; ++k) mb = fmaxf(mb, lds_f32_ordered(buf + k * RECB + (GM * D + g) * 4));
-      const float w = M[g] == -INFINITY ? 0.f : exp2f(M[g] - mb);  // nothing folded yet: 0
-      L[g] *= w;
+      const float mk = lane < nb ? bufp[lane * REC + GM * D + g] : -INFINITY;
+      const float lk = lane < nb ? bufp[lane * REC + GM * D + GM + g] : 0.f;
+      float mb = mk;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) o[e][g] *= w;
-      M[g] = mb;
+      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+      const float mn = fmaxf(M[g], mb);
+      const float resc = M[g] == -INFINITY ? 0.f : exp2f(M[g] - mn);  // nothing folded yet: 0
+      Lp[g] *= resc;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[e][g] *= resc;
+      M[g] = mn;
+      // an empty record (m = -inf: its rows saw nothing) weighs 0
+      wk[g] = mk == -INFINITY ? 0.f : exp2f(mk - mn);
+      Lp[g] = fmaf(wk[g], lk, Lp[g]);
     }
-#pragma unroll 1
+#pragma unroll 2
     for (int k = 0; k < nb; ++k) {
-      const uint32_t rk = buf + k * RECB;
-      float wk[GM];
+      const float* rk = bufp + k * REC + lane * GM;  // acc[d][0..GM) of column d = lane (+ 32 e)
+      float w[GM];
 #pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        const float mk = lds_f32_ordered(rk + (GM * D + g) * 4);
-        // an empty record (m = -inf: its rows saw nothing) weighs 0
-        wk[g] = mk == -INFINITY ? 0.f : exp2f(mk - M[g]);
-        L[g] = fmaf(wk[g], lds_f32_ordered(rk + (GM * D + GM + g) * 4), L[g]);
-      }
+      for (int g = 0; g < GM; ++g) w[g] = __shfl_sync(0xffffffffu, wk[g], k);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        const uint32_t a = rk + static_cast<uint32_t>((lane + 32 * e) * GM) * 4;  // acc[d][0..GM) of column d
         if constexpr (GM % 4 == 0) {
 #pragma unroll
           for (int g = 0; g < GM; g += 4) {
-            const float4 x = lds_f32x4_ordered(a + g * 4);
-            o[e][g] = fmaf(wk[g], x.x, o[e][g]);
-            o[e][g + 1] = fmaf(wk[g + 1], x.y, o[e][g + 1]);
-            o[e][g + 2] = fmaf(wk[g + 2], x.z, o[e][g + 2]);
-            o[e][g + 3] = fmaf(wk[g + 3], x.w, o[e][g + 3]);
+            const float4 x = *reinterpret_cast<const float4*>(rk + 32 * e * GM + g);
+            o[e][g] = fmaf(w[g], x.x, o[e][g]);
+            o[e][g + 1] = fmaf(w[g + 1], x.y, o[e][g + 1]);
+            o[e][g + 2] = fmaf(w[g + 2], x.z, o[e][g + 2]);
+            o[e][g + 3] = fmaf(w[g + 3], x.w, o[e][g + 3]);
           }
         } else {
 #pragma unroll
-          for (int g = 0; g < GM; ++g) o[e][g] = fmaf(wk[g], lds_f32_ordered(a + g * 4), o[e][g]);
+          for (int g = 0; g < GM; ++g) o[e][g] = fmaf(w[g], rk[32 * e * GM + g], o[e][g]);
         }
       }
     }
@@ -319,10 +320,13 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
   }
 #pragma unroll
   for (int g = 0; g < GM; ++g) {
+    float L = Lp[g];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     if (g < R) {
       // row g = (query g / G, head g % G) of the group
       const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>(g / G) * num_heads + g % G : seq_row0 + g;
-      const float inv = L[g] > 0.f ? vs / L[g] : 0.f;
+      const float inv = L > 0.f ? vs / L : 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, orow * D + lane + 32 * e, o[e][g] * inv);
     }
@@ -915,7 +919,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     const int64_t seq_row0 = static_cast<int64_t>(s) * QL * p.num_heads + static_cast<int64_t>(kvh) * G;
     // this warp's stages are idle after its unit loop: the records are staged there
     merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
-                                  wbase_u32 + Tr::OFF_STAGES, (NS * STG) / (Tr::REC * 4));
+                                  wbase_u32 + Tr::OFF_STAGES,
+                                  reinterpret_cast<const float*>(wbase + Tr::OFF_STAGES), (NS * STG) / (Tr::REC * 4));
     if (lane == 0) p.seg_counters[x] = 0;
   };
 
