@@ -276,12 +276,16 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 
 // atomic add with release semantics at GPU scope: this thread's earlier
 // writes (and those ordered before it by a warp barrier) become visible to
-// whoever observes the new value with acquire semantics
+// whoever observes the new value and then acquires (fence_acq_rel_gpu)
 __device__ __forceinline__ int atom_add_release_gpu(int* addr, int v) {
   int old;
   asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
   return old;
 }
+
+// Acquire-release fence at GPU scope: after observing values written by
+// release operations, this thread's later reads see what they released.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void st_shared_s32(uint32_t addr, int v) {
   asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");

@@ -1102,8 +1102,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // ---- the split merges this warp won
   settle();
   if (npend > 0) {
+    // acquire: the other fragments' records, released by their arrivals.
+    // Lane 0 observed those arrivals (its atomics' results); its fence, then
+    // the warp barrier, order every lane's reads after them.  (An acquire on
+    // every arrival would order the next unit's loads after the atomic and
+    // stall the unit loop.)
+    fence_acq_rel_gpu();
     __syncwarp();
-    __threadfence();  // acquire: the other fragments' records, released by their arrivals
     for (int i = 0; i < npend; ++i) merge_seg(pend[i]);
   }
 }
