@@ -357,7 +357,7 @@ def run_ours(args):
                       v_inv_scale=vis, pdl=pdl)
             return
         pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
-                             v_zero_point=vz, stream=stream)
+                             v_zero_point=vz, stream=stream, pdl=pdl)
         pa.copy_blocks(kc, vc, no_pairs, stream=stream)          # no shared block is written: no launch
         pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                   partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
@@ -436,7 +436,7 @@ def run_ours(args):
                           v_inv_scale=vis, pdl=pdl)
             else:
                 pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis,
-                                     k_zero_point=kz, v_zero_point=vz, stream=stream)
+                                     k_zero_point=kz, v_zero_point=vz, stream=stream, pdl=pdl)
                 pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                           partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
                           k_zero_point=kz, v_zero_point=vz, pdl=pdl)
@@ -488,7 +488,8 @@ def run_ours(args):
             "q_len": args.q_len,
             "step": ("pa_decode_ex with the new token's cache write fused (one launch)" if args.fused
                      else "reshape_and_cache(1 new token/seq) + pa_decode") +
-                    (", decode launched with programmatic dependent launch" if pdl else ""),
+                    ((", launched with programmatic dependent launch" if args.fused
+                      else ", both launched with programmatic dependent launch") if pdl else ""),
             "kernel_timing": "a second timed loop of K decode launches alone (ordinary launches), "
                              "CUDA events around each on the launching stream, same KV rotation",
             "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
@@ -584,7 +585,7 @@ def run_beam(args):
 
     def step(i):
         kc, vc = caches[i % replicas]
-        pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, stream=stream)
+        pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, stream=stream, pdl=pdl)
         pa.decode(out, q, kc, vc, tables, lens, H, sc["scale"], B, partition_size=args.partition_size,
                   workspace=ws, stream=stream, pdl=pdl)
 
@@ -643,7 +644,7 @@ def run_beam(args):
                    "num_kv_heads": H, "head_dim": D, "block_size": B, "context_tokens": int(lens_np.sum()),
                    "cow_pairs": n_pairs, "unique_kv_bytes": unique_kv, "logical_kv_bytes": logical_kv,
                    "step": "reshape_and_cache(1 new token/beam) + pa_decode" +
-                           (", decode launched with programmatic dependent launch" if pdl else ""),
+                           (", both launched with programmatic dependent launch" if pdl else ""),
                    "kernel_timing": "a second timed loop of K decode launches alone (ordinary launches), "
                                     "CUDA events around each on the launching stream",
                    "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 "

@@ -275,11 +275,19 @@ int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype,
  *            zero_point[h], -128, 127): the product rounded in float32, then
  *            to the nearest integer with ties to even; +-inf saturate and NaN
  *            becomes +127.
+ *   pdl      nonzero: launch with programmatic dependent launch.  The
+ *            kernel's first action is to wait until the kernel launched just
+ *            before it on `stream` has finished (nothing is read or written
+ *            before that), so only the launch itself overlaps that kernel's
+ *            end; the write then lets a decode launched after it with pdl
+ *            start its set-up at once.  0: an ordinary launch.  Engineering
+ *            addition with no counterpart in the pages.
  */
 typedef struct pa_cache_write_options {
   size_t struct_size;
   const int32_t* k_zero_point;
   const int32_t* v_zero_point;
+  int32_t pdl;
 } pa_cache_write_options;
 
 int pa_reshape_and_cache_ex(const void* k, const void* v, pa_dtype src_dtype,

@@ -38,7 +38,7 @@ class DecodeOptions(ctypes.Structure):
 class CacheWriteOptions(ctypes.Structure):
     """pa_cache_write_options (include/pa.h)."""
     _fields_ = [("struct_size", ctypes.c_size_t), ("k_zero_point", ctypes.c_void_p),
-                ("v_zero_point", ctypes.c_void_p)]
+                ("v_zero_point", ctypes.c_void_p), ("pdl", ctypes.c_int32)]
 
     def __init__(self, **kw):
         super().__init__(struct_size=ctypes.sizeof(CacheWriteOptions), **kw)
@@ -308,10 +308,12 @@ def decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_head
 
 
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *, k_inv_scale=None, v_inv_scale=None,
-                      k_zero_point=None, v_zero_point=None, stream=None):
+                      k_zero_point=None, v_zero_point=None, stream=None, pdl=False):
     """Write rows k[n], v[n] ([N, H_kv, d]) to cache slots slot_mapping[n] (pa_reshape_and_cache).
 
     INT8 caches (torch.int8) also take int32 per-KV-head zero points (pa_reshape_and_cache_ex).
+    pdl=True: programmatic dependent launch (pa_reshape_and_cache_ex): the kernel waits for the kernel before
+    it on the stream before touching memory, so only its launch overlaps that kernel's end.
     """
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("slot_mapping", slot_mapping),
                  ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale), ("k_zero_point", k_zero_point),
@@ -326,8 +328,9 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *, k_inv
     args = (_ptr(k), _ptr(v), dtype_code(k), k.stride(0), v.stride(0),
             _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), k_cache.shape[0],
             _ptr(slot_mapping), N, Hkv, D, int(block_size), _ptr(k_inv_scale), _ptr(v_inv_scale))
-    if k_zero_point is not None or v_zero_point is not None:
-        opt = CacheWriteOptions(k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point))
+    if k_zero_point is not None or v_zero_point is not None or pdl:
+        opt = CacheWriteOptions(k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point),
+                                pdl=1 if pdl else 0)
         st = pa_reshape_and_cache_ex(*args, ctypes.byref(opt), _stream(stream))
         _check("pa_reshape_and_cache_ex", st)
     else:

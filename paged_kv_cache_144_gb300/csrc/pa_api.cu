@@ -425,6 +425,7 @@ PA_EXPORT int pa_reshape_and_cache_ex(const void* k, const void* v, pa_dtype src
   a.v_inv_scale = v_inv_scale;
   a.k_zero_point = o.k_zero_point;
   a.v_zero_point = o.v_zero_point;
+  a.pdl = o.pdl != 0;
   return cuda_status(pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream)),
                      "pa_reshape_and_cache launch");
 }

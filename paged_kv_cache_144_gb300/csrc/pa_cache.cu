@@ -32,8 +32,12 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const float* __restrict__ k_inv_scale, const float* __restrict__ v_inv_scale,
     const int32_t* __restrict__ k_zero_point, const int32_t* __restrict__ v_zero_point, unsigned int* err) {
   constexpr int EPL = D / 32;  // elements per lane: 2 or 4
-  // a decode launched after this write with programmatic serialization may
-  // start its set-up now; it waits for this grid before it reads the cache
+  // Under a programmatic dependent launch, nothing is read or written before
+  // the kernel before this one on the stream has finished (an ordinary
+  // launch returns at once).  A decode launched after this write with
+  // programmatic serialization may then start its set-up; it waits for this
+  // grid before it reads the cache.
+  griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -133,20 +137,41 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
 
 }  // namespace
 
+// One cache-write launch, optionally with programmatic stream serialisation.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_rc(void (*kern)(KArgs...), unsigned grid, bool pdl, cudaStream_t stream, Args... args) {
+  if (!pdl) {
+    kern<<<grid, 256, 0, stream>>>(args...);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.num_tokens) * a.num_kv_heads * 2;
   if (rows == 0) return cudaSuccess;
   const int warps_per_cta = 8;
   const int64_t grid = (rows + warps_per_cta - 1) / warps_per_cta;
-#define PA_RC_LAUNCH(SRC, MODE, D)                                                              \
-  reshape_and_cache_kernel<SRC, MODE, D><<<static_cast<unsigned>(grid), 256, 0, stream>>>(     \
-      a.k, a.v, a.k_stride, a.v_stride, a.k_cache, a.v_cache, a.num_blocks, a.slot_mapping,     \
-      a.num_tokens, a.num_kv_heads, a.block_size, a.k_inv_scale, a.v_inv_scale, a.k_zero_point, \
-      a.v_zero_point, a.err)
+#define PA_RC_LAUNCH(SRC, MODE, D)                                                                    \
+  le = launch_rc(reshape_and_cache_kernel<SRC, MODE, D>, static_cast<unsigned>(grid), a.pdl, stream, a.k, a.v, \
+            a.k_stride, a.v_stride, a.k_cache, a.v_cache, a.num_blocks, a.slot_mapping, a.num_tokens,        \
+            a.num_kv_heads, a.block_size, a.k_inv_scale, a.v_inv_scale, a.k_zero_point, a.v_zero_point, a.err)
 #define PA_RC_D(SRC, MODE) \
   if (a.head_dim == 128) PA_RC_LAUNCH(SRC, MODE, 128); else PA_RC_LAUNCH(SRC, MODE, 64);
   const int mode = a.kv_dtype == PA_FP8_E4M3 ? kToFp8 : (a.kv_dtype == PA_INT8 ? kToInt8 : kCopy);
   (void)cudaGetLastError();
+  cudaError_t le = cudaSuccess;
   if (a.src_dtype == PA_F16) {
     if (mode == kToFp8) { PA_RC_D(f16_t, kToFp8) } else if (mode == kToInt8) { PA_RC_D(f16_t, kToInt8) }
     else { PA_RC_D(f16_t, kCopy) }
@@ -156,7 +181,7 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream) 
   }
 #undef PA_RC_D
 #undef PA_RC_LAUNCH
-  return cudaGetLastError();
+  return le;
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, int64_t block_bytes,

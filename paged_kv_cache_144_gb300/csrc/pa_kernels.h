@@ -36,6 +36,7 @@ struct ReshapeArgs {
   const int32_t* k_zero_point;  // INT8 only
   const int32_t* v_zero_point;  // INT8 only
   unsigned int* err;
+  bool pdl;                     // programmatic dependent launch (the kernel waits for its predecessor first)
 };
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, cudaStream_t stream);

@@ -164,3 +164,70 @@ def test_pdl_fused_append_after_a_decode():
     assert bits_equal(k1, rk) and bits_equal(v1, rv)
     assert np.max(np.abs(o1.astype(np.float64) - ref)) <= PA_TOL
     assert bits_equal(o1, o0) and bits_equal(k1, k0) and bits_equal(v1, v0)
+
+
+def _scaled_rows(rows, fmt, factor):
+    """rows (16-bit storage) times a power of two, exactly, in the same storage."""
+    t = torch.from_numpy(np.ascontiguousarray(rows).view(np.int16 if fmt == "bf16" else np.float16))
+    t = t.view(torch.bfloat16) if fmt == "bf16" else t
+    out = (t.float() * factor).to(t.dtype)
+    return out.view(torch.int16).numpy().view(np.uint16) if fmt == "bf16" else out.numpy()
+
+
+@pytest.mark.parametrize("name,kw", [CASES[1][:2], CASES[3][:2]])
+def test_pdl_cache_write_waits_for_the_decode_before_it(name, kw):
+    """A cache write launched with pdl right after a decode rewrites every row that decode reads (with
+    values of another scale); the decode must still see the old rows, the cache must end with the new."""
+    b, vals, ref, okc, ovc = _setup(name, kw, seed=15)
+    kv, B = b.kv_fmt, b.block_size
+    ksrc, vsrc, slots = _all_rows(b, okc, ovc)
+    knew, vnew = _scaled_rows(ksrc, kv, -4.0), _scaled_rows(vsrc, kv, 8.0)
+    kc, vc = to_torch(okc, kv, "cuda"), to_torch(ovc, kv, "cuda")
+    q = to_torch(vals["q"], b.q_fmt, "cuda")
+    tables = torch.from_numpy(b.block_tables).cuda()
+    lens = torch.from_numpy(b.seq_lens).cuda()
+    n = pa.decode_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads, b.head_dim, B, b.max_blocks_per_seq, 0,
+                                  pa.dtype_code(kc))
+    ws = pa.new_workspace(n, "cuda") if n else None
+    kn, vn, sl = to_torch(knew, kv, "cuda"), to_torch(vnew, kv, "cuda"), torch.from_numpy(slots).cuda()
+    torch.cuda.synchronize()
+    out = _decode(b, q, kc, vc, tables, lens, ws, 0, True)
+    pa.reshape_and_cache(kn, vn, kc, vc, sl, B, pdl=True)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    assert np.max(np.abs(out.cpu().numpy().astype(np.float64) - ref)) <= PA_TOL
+    rk, rv = oracle.reshape_and_cache(knew, vnew, okc, ovc, slots, B, src_fmt=kv, kv_fmt=kv)
+    assert bits_equal(to_numpy(kc, kv), rk) and bits_equal(to_numpy(vc, kv), rv)
+
+
+@pytest.mark.parametrize("name,kw", [CASES[0][:2], CASES[1][:2]])
+def test_pdl_chain_of_write_and_decode_steps(name, kw):
+    """Steps of (cache write of every row, pdl) -> (decode, pdl) on one stream and one workspace, each step
+    with rows of another scale: every decode sees its own step's rows and none of the next step's."""
+    b, vals, _, okc, ovc = _setup(name, kw, seed=16)
+    kv, B = b.kv_fmt, b.block_size
+    ksrc, vsrc, slots = _all_rows(b, okc, ovc)
+    kc, vc = to_torch(okc, kv, "cuda"), to_torch(ovc, kv, "cuda")
+    q = to_torch(vals["q"], b.q_fmt, "cuda")
+    tables = torch.from_numpy(b.block_tables).cuda()
+    lens = torch.from_numpy(b.seq_lens).cuda()
+    n = pa.decode_workspace_bytes(b.num_seqs, b.num_heads, b.num_kv_heads, b.head_dim, B, b.max_blocks_per_seq, 0,
+                                  pa.dtype_code(kc))
+    ws = pa.new_workspace(n, "cuda") if n else None
+    sl = torch.from_numpy(slots).cuda()
+    factors = [(0.5, 2.0), (-1.0, 0.25), (2.0, -1.0), (0.25, 4.0)]
+    rows = [(_scaled_rows(ksrc, kv, fk), _scaled_rows(vsrc, kv, fv)) for fk, fv in factors]
+    dev_rows = [(to_torch(a, kv, "cuda"), to_torch(c, kv, "cuda")) for a, c in rows]
+    torch.cuda.synchronize()
+    outs = []
+    for kn, vn in dev_rows:
+        pa.reshape_and_cache(kn, vn, kc, vc, sl, B, pdl=True)
+        outs.append(_decode(b, q, kc, vc, tables, lens, ws, 0, True))
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    for (knew, vnew), o in zip(rows, outs):
+        rk, rv = oracle.reshape_and_cache(knew, vnew, okc, ovc, slots, B, src_fmt=kv, kv_fmt=kv)
+        ref = oracle.paged_decode_attention(vals["q"], rk, rv, b.block_tables, b.seq_lens, b.scale, B,
+                                            q_fmt=b.q_fmt, kv_fmt=kv)
+        assert np.max(np.abs(o.cpu().numpy().astype(np.float64) - ref)) <= PA_TOL
+    assert bits_equal(to_numpy(kc, kv), rk) and bits_equal(to_numpy(vc, kv), rv)

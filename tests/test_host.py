@@ -288,3 +288,14 @@ def test_decode_ex_pdl_option_validation(lib):
     old = pa.DecodeOptions(pdl=1)
     old.struct_size = pa.DecodeOptions.pdl.offset
     assert _decode_ex(old, S=0) == pa.PA_OK
+
+
+def test_cache_write_pdl_option_validation(lib):
+    # the launch mode changes no argument rule
+    opt = _lib.CacheWriteOptions(pdl=1)
+    st = pa.pa_reshape_and_cache_ex(0x10000, 0x20000, pa.PA_BF16, 8 * 128, 8 * 128, 0x30000, 0x40000, pa.PA_BF16,
+                                    16, 0x50000, 0, 8, 128, 16, None, None, ctypes.byref(opt), None)
+    assert st == pa.PA_OK                    # no tokens: nothing to launch
+    st = pa.pa_reshape_and_cache_ex(0x10000, 0x20000, pa.PA_BF16, 8 * 128, 8 * 128, 0x30000, 0x40000, pa.PA_BF16,
+                                    16, 0x50000, 4, 8, 96, 16, None, None, ctypes.byref(opt), None)
+    assert st == pa.PA_ERR_UNSUPPORTED       # head_dim 96
