@@ -190,8 +190,11 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            and the workspace, only after that kernel has finished.  So with
  *            pdl on, seq_lens and block_tables must not be written by the
  *            kernel launched just before this call (host copies and earlier
- *            kernels are fine).  0: an ordinary launch.  Engineering addition
- *            with no counterpart in the pages.
+ *            kernels are fine).  0: an ordinary launch.  Either way the decode
+ *            lets a kernel launched after it with programmatic serialization
+ *            (pa_reshape_and_cache_ex with pdl) be scheduled at once; that
+ *            kernel waits for the decode before it touches memory.
+ *            Engineering addition with no counterpart in the pages.
  */
 typedef struct pa_decode_options {
   size_t struct_size;
@@ -275,13 +278,13 @@ int pa_reshape_and_cache(const void* k, const void* v, pa_dtype src_dtype,
  *            zero_point[h], -128, 127): the product rounded in float32, then
  *            to the nearest integer with ties to even; +-inf saturate and NaN
  *            becomes +127.
- *   pdl      nonzero: launch with programmatic dependent launch.  The
- *            kernel's first action is to wait until the kernel launched just
- *            before it on `stream` has finished (nothing is read or written
- *            before that), so only the launch itself overlaps that kernel's
- *            end; the write then lets a decode launched after it with pdl
- *            start its set-up at once.  0: an ordinary launch.  Engineering
- *            addition with no counterpart in the pages.
+ *   pdl      nonzero: launch with programmatic dependent launch.  Before
+ *            it reads or writes anything, the kernel waits until the kernel
+ *            launched just before it on `stream` has finished, so only the
+ *            launch overlaps that kernel.  0: an ordinary launch.  Either way
+ *            a decode launched after the write with pdl may start its set-up
+ *            at once (it reads the cache only after the write has finished).
+ *            Engineering addition with no counterpart in the pages.
  */
 typedef struct pa_cache_write_options {
   size_t struct_size;

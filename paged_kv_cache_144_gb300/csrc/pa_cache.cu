@@ -32,13 +32,13 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const float* __restrict__ k_inv_scale, const float* __restrict__ v_inv_scale,
     const int32_t* __restrict__ k_zero_point, const int32_t* __restrict__ v_zero_point, unsigned int* err) {
   constexpr int EPL = D / 32;  // elements per lane: 2 or 4
-  // Under a programmatic dependent launch, nothing is read or written before
-  // the kernel before this one on the stream has finished (an ordinary
-  // launch returns at once).  A decode launched after this write with
-  // programmatic serialization may then start its set-up; it waits for this
-  // grid before it reads the cache.
-  griddep_wait();
+  // A decode launched after this write with programmatic serialization may
+  // start its set-up now (it waits for this grid before it reads the cache).
+  // Under a programmatic dependent launch of this write, nothing is read or
+  // written before the kernel before it on the stream has finished (an
+  // ordinary launch returns at once).
   griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;

@@ -372,6 +372,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   int* scan_tmp = lens + S;
   const uint32_t table_ring_u32 = base_u32 + W * wsm + align_up_c((2 * S + 1 + NWARP) * 4, 16);
 
+  // A kernel launched after this one with programmatic serialization (the
+  // next step's cache write) may be scheduled now; it waits for this grid
+  // before it touches memory.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
@@ -588,6 +592,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   WorkIter it;
   start_iter(it, blockIdx.x * W + c);
   if (!it.valid) return;
+  // Under a programmatic dependent launch this CTA may be resident long
+  // before the kernel before it has finished; the bounded waits below start
+  // counting only after it has (at once otherwise).
+  griddep_wait();
   const uint8_t* wbase = base + c * wsm;
   const uint32_t wbase_u32 = base_u32 + c * wsm;
   int cst = 0, cpar = 0;
