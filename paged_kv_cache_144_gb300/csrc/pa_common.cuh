@@ -140,6 +140,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Prefetch of the 128-byte line holding addr into L2.
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -70,6 +70,7 @@ constexpr int kMinUnitsPerWarp = 2;            // smallest balanced share (small
 constexpr int kStageBytesPerWarp = 24 * 1024;  // default K/V pipeline bytes per consumer warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kTablePrefetch = 3;              // units whose table entries the producer fetches ahead
+constexpr int64_t kTableL2Bytes = 2 << 20;     // block tables up to this size are prefetched into L2 at entry
 
 // Integer tuning override from the environment (read once per name), or -1.
 int tuning_override(const char* name);
@@ -379,6 +380,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
+  }
+
+  // ---- 0. the block tables are brought into L2 while the lengths are read,
+  // so that the producers' first table reads (which need the lengths) hit L2
+  // (tables up to kTableL2Bytes; the block tables are never written here)
+  {
+    const int64_t tbytes = static_cast<int64_t>(S) * p.max_blocks_per_seq * 4;
+    if (tbytes <= kTableL2Bytes) {
+      const char* tb = reinterpret_cast<const char*>(p.block_tables);
+      for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i * 128 < tbytes;
+           i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        prefetch_l2(tb + i * 128);
+    }
   }
 
   // ---- 1. units per sequence and their exclusive prefix sums (every CTA)
