@@ -179,27 +179,35 @@ def _torch():
     return torch
 
 
+_DTYPE_CODES = None
+
+
 def dtype_code(t) -> int:
-    torch = _torch()
-    m = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3,
-         torch.int8: PA_INT8}
-    f8 = getattr(torch, "float8_e4m3fn", None)
-    if f8 is not None:
-        m[f8] = PA_FP8_E4M3
-    if t.dtype not in m:
+    global _DTYPE_CODES
+    m = _DTYPE_CODES
+    if m is None:  # built once: this runs on every call of the step
+        torch = _torch()
+        m = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.uint8: PA_FP8_E4M3,
+             torch.int8: PA_INT8}
+        f8 = getattr(torch, "float8_e4m3fn", None)
+        if f8 is not None:
+            m[f8] = PA_FP8_E4M3
+        _DTYPE_CODES = m
+    code = m.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    return m[t.dtype]
+    return code
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain integer: the signatures declare void*, so ctypes converts it
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
-    torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+        stream = _torch().cuda.current_stream()
+    return stream.cuda_stream
 
 
 def _require_cuda(name, t, contiguous=True):
@@ -209,6 +217,13 @@ def _require_cuda(name, t, contiguous=True):
         raise ValueError(f"{name} must be a CUDA tensor")
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _require_cuda_all(named):
+    """_require_cuda over (name, tensor) pairs in one call (the per-step path)."""
+    for name, t in named:
+        if t is not None and not (t.is_cuda and t.is_contiguous()):
+            _require_cuda(name, t)
 
 
 def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
@@ -245,10 +260,10 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
     pdl=True: programmatic dependent launch (pa_decode_ex): the set-up overlaps the kernel launched just
     before on the stream, so seq_lens and block_tables must not be written by that kernel.
     """
-    for n, t in (("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
-                 ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale), ("k_zero_point", k_zero_point),
-                 ("v_zero_point", v_zero_point), ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale)):
-        _require_cuda(n, t)
+    _require_cuda_all((("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
+                       ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale),
+                       ("k_zero_point", k_zero_point), ("v_zero_point", v_zero_point), ("k_inv_scale", k_inv_scale),
+                       ("v_inv_scale", v_inv_scale)))
     _require_cuda("q", q, contiguous=False)
     q_len = 1
     if q.dim() == 4:                       # [S, L, H_q, d]: several queries per sequence
@@ -315,10 +330,9 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size, *, k_inv
     pdl=True: programmatic dependent launch (pa_reshape_and_cache_ex): the kernel waits for the kernel before
     it on the stream before touching memory, so only its launch overlaps that kernel's end.
     """
-    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("slot_mapping", slot_mapping),
-                 ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale), ("k_zero_point", k_zero_point),
-                 ("v_zero_point", v_zero_point)):
-        _require_cuda(n, t)
+    _require_cuda_all((("k_cache", k_cache), ("v_cache", v_cache), ("slot_mapping", slot_mapping),
+                       ("k_inv_scale", k_inv_scale), ("v_inv_scale", v_inv_scale), ("k_zero_point", k_zero_point),
+                       ("v_zero_point", v_zero_point)))
     _require_cuda("k", k, contiguous=False)
     _require_cuda("v", v, contiguous=False)
     N, Hkv, D = k.shape
