@@ -419,16 +419,27 @@ def run_ours(args):
         h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
         h_slots, h_tables, h_lens = slots.cpu().pin_memory(), tables.cpu().pin_memory(), lens.cpu().pin_memory()
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-        d_slots, d_tables, d_lens = torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(lens)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_lens))
+        # The step's inputs are staged in one pinned host buffer and cross in one copy, as a serving loop
+        # stages them; each tensor sits at a 256-byte aligned offset (the library wants 16-byte bases).
+        parts = (h_q, h_k, h_v, h_slots, h_tables, h_lens)
+        offs, h2d = [], 0
+        for t in parts:
+            h2d = (h2d + 255) // 256 * 256
+            offs.append(h2d)
+            h2d += t.numel() * t.element_size()
+        h_stage = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+        d_stage = torch.empty(h2d, dtype=torch.uint8, device=dev)
+        views = []
+        for t, o in zip(parts, offs):
+            nb = t.numel() * t.element_size()
+            h_stage[o:o + nb].copy_(t.reshape(-1).view(torch.uint8))
+            views.append(d_stage[o:o + nb].view(t.dtype).view(t.shape))
+        d_q, d_k, d_v, d_slots, d_tables, d_lens = views
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step(i):
             kc, vc = caches[i % replicas]
-            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_tables, h_tables),
-                         (d_lens, h_lens)):
-                d.copy_(h, non_blocking=True)
+            d_stage.copy_(h_stage, non_blocking=True)
             if args.fused:
                 pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
                           partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
