@@ -736,9 +736,11 @@ def run_reference(args):
         one()
     wall = time.perf_counter() - t0
     value = step_bytes * args.steps / wall / 1e9
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     sample = (f"one (sequence, KV head) segment of {T} tokens (of {T_full}) x G={G} query heads per step, "
-              f"float64 numpy oracle, 1 thread")
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+              f"float64 numpy oracle, 1 thread" + (f"; rank 0 of {world} ran it alone" if world > 1 else ""))
+    # n_gpus is the N of the launch (the driver pairs this line with the other arm's at the same N)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wall / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}"},
