@@ -299,3 +299,30 @@ def test_cache_write_pdl_option_validation(lib):
     st = pa.pa_reshape_and_cache_ex(0x10000, 0x20000, pa.PA_BF16, 8 * 128, 8 * 128, 0x30000, 0x40000, pa.PA_BF16,
                                     16, 0x50000, 4, 8, 96, 16, None, None, ctypes.byref(opt), None)
     assert st == pa.PA_ERR_UNSUPPORTED       # head_dim 96
+
+
+def test_decode_ex_fused_append_validation(lib):
+    def app(**kw):
+        o = dict(k_new=0x10000, v_new=0x20000, new_dtype=pa.PA_BF16, new_stride=8 * 128)
+        o.update(kw)
+        return pa.DecodeOptions(**o)
+    assert _decode_ex(app(v_new=None)) == pa.PA_ERR_NULL                 # both rows or neither
+    assert _decode_ex(app(new_dtype=pa.PA_F32)) == pa.PA_ERR_DTYPE       # 16-bit source rows only
+    assert _decode_ex(app(new_dtype=pa.PA_F16)) == pa.PA_ERR_DTYPE       # a 16-bit cache takes its own type
+    assert _decode_ex(app(), kv_dtype=pa.PA_FP8_E4M3, ks=A, vs=A) == pa.PA_ERR_NULL  # quantising needs 1/scale
+    assert _decode_ex(app(new_stride=8 * 128 - 8)) == pa.PA_ERR_SHAPE    # a sequence's rows overlap
+    assert _decode_ex(app(k_new=0x10008)) == pa.PA_ERR_ALIGN             # 16-byte bases
+    assert _decode_ex(app(new_stride=8 * 128 + 4)) == pa.PA_ERR_ALIGN    # 16-byte row strides
+    assert _decode_ex(app(), S=0) == pa.PA_OK                           # nothing to append or attend
+
+
+def test_cache_write_and_copy_validation_edges(lib):
+    st = pa.pa_reshape_and_cache(0x10000, 0x20000, pa.PA_BF16, 8 * 128 - 8, 8 * 128, 0x30000, 0x40000, pa.PA_BF16,
+                                 16, 0x50000, 4, 8, 128, 16, None, None, None)
+    assert st == pa.PA_ERR_SHAPE          # k rows of a token overlap the next token's
+    st = pa.pa_reshape_and_cache(0x10000, 0x20000, pa.PA_BF16, 8 * 128, 8 * 128, 0x30000, 0x40000, pa.PA_INT8,
+                                 16, 0x50000, 4, 8, 128, 16, 0x60000, 0x70000, None)
+    assert st == pa.PA_ERR_NULL           # INT8 needs zero points (pa_reshape_and_cache_ex)
+    assert pa.pa_copy_blocks(0x30000, 0x40000, 16, 32 * 1024, 0x50000, 65536, None) == pa.PA_ERR_UNSUPPORTED
+    assert pa.pa_copy_blocks(0x30000, 0x40000, 16, 32 * 1024 + 8, 0x50000, 2, None) == pa.PA_ERR_ALIGN
+    assert pa.pa_copy_blocks(0x30000, 0x40000, 16, 32 * 1024, 0x50000, 0, None) == pa.PA_OK
