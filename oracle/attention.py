@@ -16,7 +16,7 @@ sequence's rows through its block table ([P1] Â§"PagedAttentionã®ãƒ¡ãƒ¢ãƒªç®¡ç
 logical block j -> physical block table[j]), convert to float64, form the
 scaled scores, take a max-subtracted softmax and multiply by V.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * cache layout: separate K and V pools of shape [num_blocks, H_kv, B, d];
     token position p of a sequence lives in physical block table[p // B],
     row p % B.  The layout is invisible to results.
