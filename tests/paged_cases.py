@@ -119,3 +119,57 @@ def bits_equal(a: np.ndarray, b: np.ndarray) -> bool:
     a = np.ascontiguousarray(a)
     b = np.ascontiguousarray(b)
     return a.shape == b.shape and np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def check_sequence(item):
+    """One sequence of a full-size run against the oracle (runs in an oracle worker process).
+
+    8-bit caches: the sequence's cache bytes must equal the oracle's quantisation of its bf16 rows (the
+    cached ones and the appended one); 16-bit caches: the appended rows must sit in their slot.  Then every
+    query head's output is compared with the oracle's attention over the sequence's blocks.
+    Returns (s, max abs error, None) or (s, error, reason of the first failure).
+    """
+    s, T, B = item["s"], item["T"], item["B"]
+    gk, gv = item["gk"], item["gv"]
+    nb = gk.shape[0]
+    kv = item["kv_fmt"]
+    if kv in ("e4m3", "i8"):
+        zkw = {k: item["qkw"][k] for k in ("k_zero_point", "v_zero_point") if k in item["qkw"]}
+        kr = np.concatenate([item["k_rows"], item["k_new"][None]])
+        vr = np.concatenate([item["v_rows"], item["v_new"][None]])
+        zero = np.zeros_like(gk)
+        ok, ov = oracle.reshape_and_cache(kr, vr, zero, zero, np.arange(T), B, src_fmt="bf16", kv_fmt=kv,
+                                          k_inv_scale=item["k_inv_scale"], v_inv_scale=item["v_inv_scale"], **zkw)
+        if not (bits_equal(gk, ok) and bits_equal(gv, ov)):
+            return s, float("inf"), f"{kv} cache bytes differ from the oracle's quantisation"
+        gk, gv = ok, ov
+    else:
+        r, p = (T - 1) // B, (T - 1) % B
+        if item["new_slot"] != int(item["table"][r]) * B + p:
+            return s, float("inf"), "slot of the appended token"
+        if not (bits_equal(gk[r, :, p], item["k_new"]) and bits_equal(gv[r, :, p], item["v_new"])):
+            return s, float("inf"), "appended rows not in their slot"
+    ref = oracle.paged_decode_attention(item["q"], gk, gv, np.arange(nb, dtype=np.int32)[None, :], np.array([T]),
+                                        item["scale"], B, q_fmt=item["q_fmt"], kv_fmt=kv, **item["qkw"])[0]
+    err = np.abs(item["out"] - ref)
+    if not np.all(err <= PA_TOL):
+        bad = np.nonzero(err.max(axis=1) > PA_TOL)[0]
+        return s, float(err.max()), f"heads {bad.tolist()} max abs err {err.max():.3e} > {PA_TOL}"
+    return s, float(err.max()), None
+
+
+_POOL = None
+
+
+def oracle_pool():
+    """A process pool for oracle work, started with spawn (safe after CUDA is initialised), one per session."""
+    global _POOL
+    if _POOL is None:
+        import multiprocessing as mp
+        import os
+        os.environ.setdefault("OMP_NUM_THREADS", "1")
+        n = max(1, min(16, os.cpu_count() or 1))
+        _POOL = mp.get_context("spawn").Pool(processes=n)
+        import atexit
+        atexit.register(_POOL.terminate)
+    return _POOL
