@@ -104,6 +104,15 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, 
  * last split to finish ("split-K").  seq_lens[s] == 0 gives out[s] = 0.
  * FP8 caches ([P2] "KV量子化") are dequantised in registers as
  * float(e4m3) * k_scale[kvh] (resp. v_scale[kvh]).
+ * With an 8-bit cache (FP8, or INT8 through pa_decode_ex) the two products
+ * run with f16 operands (the widened cache values are exact in f16) and fp32
+ * accumulation.  A bf16 query group (the G query rows of one sequence and KV
+ * head) is first multiplied by the power of two 2^e that puts its largest
+ * |q| in [2^14, 2^15), and the scores by 2^-e: no value overflows f16, and
+ * every element within a factor 2^28 of the group's largest is represented
+ * exactly (smaller elements may round as f16 subnormals, an absolute error
+ * below 2^-38 times the group's largest |q|).  Any finite bf16 query is
+ * accepted.
  *
  *   out            [num_seqs][num_heads][head_dim], out_dtype F32/F16/BF16
  *   q              [num_seqs][num_heads][head_dim] at q_stride elements per
@@ -340,6 +349,10 @@ int pa_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, size_t bloc
  *   - All calls share the one array per device: calls whose kernels overlap
  *     on the GPU (different streams without ordering) race and give wrong
  *     results.  Order them on one stream or use pa_decode with workspaces.
+ *   - Serves F16, BF16 and FP8 caches; an INT8 cache needs zero points,
+ *     which this call has no arguments for: PA_ERR_UNSUPPORTED.
+ *   - Every check of pa_decode runs before anything is enqueued; a rejected
+ *     call enqueues nothing (not even the clearing of the counters).
  *   - Returns PA_ERR_WORKSPACE (detail in pa_last_error_detail) when the
  *     sizes need more split workspace than the array holds; other errors as
  *     pa_decode.
@@ -373,6 +386,24 @@ const char* pa_last_error_detail(void);
 
 /* Library ABI version (major*100 + minor). */
 int pa_version(void);
+
+/*
+ * pa_debug_set_decode_wait - testing hook for the bounded waits of the decode
+ * kernel (engineering addition with no counterpart in the pages; process-wide,
+ * read at each later pa_decode / pa_decode_ex / pa_decode_noalloc call).
+ *   limit_ns         limit of every wait of a consumer warp on its pipeline
+ *                    barrier (and of the producer on a consumer's release);
+ *                    0 restores the default of 2 s.  A wait that runs out
+ *                    sets PA_DEVERR_TIMEOUT, the warp stops and the call's
+ *                    outputs are unspecified; the kernel still returns, after
+ *                    waiting (2 s at most) for its own copies in flight.
+ *   withhold_copies  nonzero: the producer warp issues no copy at all, so
+ *                    every consumer wait runs out (a barrier nothing
+ *                    completes): the way to exercise the timeout path without
+ *                    any fault.  0 for normal operation.
+ * After a call that timed out, zero the workspace before its next use.
+ */
+void pa_debug_set_decode_wait(uint64_t limit_ns, int withhold_copies);
 
 #ifdef __cplusplus
 }

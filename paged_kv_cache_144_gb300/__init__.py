@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     pa_copy_blocks, pa_decode_workspace_bytes,
     pa_get_device_error,
     pa_version, pa_decode_launch_config, pa_decode_noalloc, pa_decode_noalloc_capacity, decode_noalloc,
+    pa_debug_set_decode_wait,
     decode, reshape_and_cache, copy_blocks, decode_workspace_bytes, new_workspace, get_device_error,
     dtype_code,
 )

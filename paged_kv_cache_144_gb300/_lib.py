@@ -64,6 +64,7 @@ _SIGNATURES = {
     "pa_decode_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _i32, _vp,
                                  _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp]),
     "pa_decode_noalloc_capacity": (_sz, []),
+    "pa_debug_set_decode_wait": (None, [ctypes.c_uint64, _i32]),
     "pa_decode_launch_config": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]),
@@ -170,6 +171,11 @@ def pa_decode_launch_config(num_seqs, num_heads, num_kv_heads, head_dim, block_s
 
 def pa_version() -> int:
     return int(load().pa_version())
+
+
+def pa_debug_set_decode_wait(limit_ns: int, withhold_copies: bool) -> None:
+    """Testing hook: wait limit of the next decode launches (0 = default) and whether their copies are withheld."""
+    load().pa_debug_set_decode_wait(int(limit_ns), 1 if withhold_copies else 0)
 
 
 # ----------------------------------------------------------------------------- torch marshalling

@@ -3,6 +3,7 @@
 // the kernels.  No call here allocates device memory.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -261,12 +262,32 @@ PA_EXPORT int pa_decode_launch_config(int num_seqs, int num_heads, int num_kv_he
   return PA_OK;
 }
 
-PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
-                           const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
-                           const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                           int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
-                           int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
-                           void* workspace, size_t workspace_bytes, const pa_decode_options* opt, void* stream) {
+namespace {
+
+// Wait limit and copy withholding of the next decode launches (testing hook,
+// pa_debug_set_decode_wait); 0 = the default limit.
+std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<int> g_withhold_copies{0};
+
+// Everything one decode launch needs, validated: the plan, the kernel
+// parameters and the two tensor maps.  Filling it enqueues nothing.
+struct PreparedDecode {
+  DecodePlan plan;
+  pa::DecodeParams p;
+  CUtensorMap tk, tv;
+  bool pdl;
+  bool empty;  // num_seqs == 0: nothing to launch
+};
+
+// All host-side checks of pa_decode_ex, then the launch plan, parameters and
+// tensor maps.  Returns a pa_status; nothing is enqueued on any stream.
+int prepare_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
+                   const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                   const float* k_scale, const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim, float scale,
+                   int block_size, int partition_size, void* workspace, size_t workspace_bytes,
+                   const pa_decode_options* opt, PreparedDecode* d) {
+  d->empty = false;
   // options: fields beyond the caller's struct_size read as 0
   pa_decode_options o;
   memset(&o, 0, sizeof(o));
@@ -291,7 +312,10 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                     partition_size, kv_dtype);
   if (sh != PA_OK) return sh;
-  if (num_seqs == 0) return PA_OK;
+  if (num_seqs == 0) {
+    d->empty = true;
+    return PA_OK;
+  }
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_NULL;
   if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_DTYPE;
@@ -302,23 +326,22 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   if (q_stride < static_cast<int64_t>(q_len) * num_heads * head_dim) return PA_ERR_SHAPE;
   if (!aligned16(q) || (q_stride * 2) % 16 != 0 || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
 
-  DecodePlan plan;
+  DecodePlan& plan = d->plan;
   const bool have_ws = workspace != nullptr && workspace_bytes > 0;
   const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                            partition_size, q_dtype, kv_dtype, have_ws, &plan, append, q_len);
   if (pr != PA_OK) return pr;
   if (plan.bytes > 0 && (!have_ws || workspace_bytes < plan.bytes || !aligned16(workspace))) return PA_ERR_WORKSPACE;
 
-  CUtensorMap tk, tv;
   const int eb = dtype_bytes(kv_dtype);
   const int box_rows = block_size < plan.geo.unit_rows ? block_size : plan.geo.unit_rows;
-  if (!encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim, eb, box_rows) ||
-      !encode_cache_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, eb, box_rows))
+  if (!encode_cache_map(&d->tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim, eb, box_rows) ||
+      !encode_cache_map(&d->tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, eb, box_rows))
     return PA_ERR_CUDA;
 
   unsigned int* err = device_error_word();
   if (!err) return PA_ERR_CUDA;
-  pa::DecodeParams p;
+  pa::DecodeParams& p = d->p;
   p.err = err;
   p.out = out;
   p.out_dtype = out_dtype;
@@ -356,14 +379,44 @@ PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
   p.pending_cap = plan.pending_cap;
   p.part_records = plan.bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes)
                               : nullptr;
-  const int st = cuda_status(pa::launch_decode(plan.key, plan.geo, p, tk, tv, static_cast<cudaStream_t>(stream),
-                                              o.pdl != 0),
+  const uint64_t lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.wait_limit_ns = lim ? lim : pa::kDefaultWaitLimitNs;
+  p.withhold_copies = g_withhold_copies.load(std::memory_order_relaxed);
+  d->pdl = o.pdl != 0;
+  return PA_OK;
+}
+
+int launch_prepared(const PreparedDecode& d, void* stream) {
+  const int st = cuda_status(pa::launch_decode(d.plan.key, d.plan.geo, d.p, d.tk, d.tv,
+                                              static_cast<cudaStream_t>(stream), d.pdl),
                               "pa_decode launch");
   if (st != PA_OK) {
     const size_t n = strlen(g_last_error);
     snprintf(g_last_error + n, sizeof(g_last_error) - n, "; %s", pa::launch_failure_note());
   }
   return st;
+}
+
+}  // namespace
+
+PA_EXPORT int pa_decode_ex(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
+                           const void* k_cache, const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                           const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, float scale, int block_size, int partition_size,
+                           void* workspace, size_t workspace_bytes, const pa_decode_options* opt, void* stream) {
+  PreparedDecode d;
+  const int st = prepare_decode(out, out_dtype, q, q_dtype, q_stride, k_cache, v_cache, kv_dtype, num_blocks, k_scale,
+                                v_scale, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads,
+                                num_kv_heads, head_dim, scale, block_size, partition_size, workspace, workspace_bytes,
+                                opt, &d);
+  if (st != PA_OK || d.empty) return st;
+  return launch_prepared(d, stream);
+}
+
+PA_EXPORT void pa_debug_set_decode_wait(uint64_t limit_ns, int withhold_copies) {
+  g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  g_withhold_copies.store(withhold_copies ? 1 : 0, std::memory_order_relaxed);
 }
 
 PA_EXPORT int pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype, int64_t q_stride,
@@ -522,30 +575,28 @@ PA_EXPORT int pa_decode_noalloc(void* out, pa_dtype out_dtype, const void* q, pa
   const int sh = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                     partition_size, kv_dtype);
   if (sh != PA_OK) return sh;
+  // INT8 caches need zero points, which this entry point has no arguments for
+  if (kv_dtype == PA_INT8) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
-  if ((q_dtype != PA_F16 && q_dtype != PA_BF16) ||
-      (kv_dtype != q_dtype && kv_dtype != PA_FP8_E4M3 && kv_dtype != PA_INT8))
-    return PA_ERR_DTYPE;
-  DecodePlan plan;
-  const int pr = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                           partition_size, q_dtype, kv_dtype, true, &plan);
-  if (pr != PA_OK) return pr;
-  if (plan.bytes > kNoallocScratchBytes) {
-    snprintf(g_last_error, sizeof(g_last_error),
-             "pa_decode_noalloc: this call needs %zu bytes of split workspace, more than the fixed %zu",
-             plan.bytes, kNoallocScratchBytes);
-    return PA_ERR_WORKSPACE;
-  }
   void* scratch = noalloc_scratch_address();
   if (!scratch) return PA_ERR_CUDA;
-  // the arrival counters must start at zero; the records need no clearing
-  if (plan.counters_bytes > 0) {
-    const int st = cuda_status(
-        cudaMemsetAsync(scratch, 0, plan.counters_bytes, static_cast<cudaStream_t>(stream)), "pa_decode_noalloc memset");
-    if (st != PA_OK) return st;
+  // every check of pa_decode first: a rejected call enqueues nothing
+  PreparedDecode d;
+  const int st = prepare_decode(out, out_dtype, q, q_dtype, q_stride, k_cache, v_cache, kv_dtype, num_blocks, k_scale,
+                                v_scale, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads,
+                                num_kv_heads, head_dim, scale, block_size, partition_size, scratch,
+                                kNoallocScratchBytes, nullptr, &d);
+  if (st == PA_ERR_WORKSPACE && d.plan.bytes > kNoallocScratchBytes) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "pa_decode_noalloc: this call needs %zu bytes of split workspace, more than the fixed %zu",
+             d.plan.bytes, kNoallocScratchBytes);
   }
-  return pa_decode(out, out_dtype, q, q_dtype, q_stride, k_cache, v_cache, kv_dtype, num_blocks, k_scale, v_scale,
-                   block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads, num_kv_heads, head_dim, scale,
-                   block_size, partition_size, plan.bytes ? scratch : nullptr, plan.bytes ? kNoallocScratchBytes : 0,
-                   stream);
+  if (st != PA_OK || d.empty) return st;
+  // the arrival counters must start at zero; the records need no clearing
+  if (d.plan.counters_bytes > 0) {
+    const int ms = cuda_status(
+        cudaMemsetAsync(scratch, 0, d.plan.counters_bytes, static_cast<cudaStream_t>(stream)), "pa_decode_noalloc memset");
+    if (ms != PA_OK) return ms;
+  }
+  return launch_prepared(d, stream);
 }

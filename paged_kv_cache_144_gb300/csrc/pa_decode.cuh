@@ -46,7 +46,9 @@
 //    head_dim order of QK permuted so that a lane reads 16 contiguous bytes
 //    of a K row, and V transposed in registers with byte permutes; the
 //    per-head K scale multiplies the scores, the V scale the final divide,
-//    and q is rounded to f16 for the product.
+//    and a bf16 query enters the f16 product scaled by a power of two that
+//    puts the group's largest element at 2^14 .. 2^15 (no overflow, no lost
+//    bits within 2^28 of that element).
 //  * Split segments: a warp whose range covers only part of a segment writes
 //    its (m, l, acc) record to the workspace and arrives on the segment's
 //    counter (a release atomic whose result it reads one fragment later, so
@@ -68,7 +70,6 @@ namespace pa {
 
 constexpr int kMinUnitsPerWarp = 2;            // smallest balanced share (small batches spread wide)
 constexpr int kStageBytesPerWarp = 24 * 1024;  // default K/V pipeline bytes per consumer warp
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kTablePrefetch = 3;              // units whose table entries the producer fetches ahead
 constexpr int64_t kTableL2Bytes = 2 << 20;     // block tables up to this size are prefetched into L2 at entry
 
@@ -511,6 +512,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
       }
     }
+    if (p.withhold_copies) it.valid = false;  // testing hook: nothing is issued, every consumer wait runs out
     while (__any_sync(0xffffffffu, it.valid)) {
       bool did = false;
       if (it.valid) {
@@ -519,7 +521,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const uint64_t now = global_timer_ns();
           if (wait_since == 0) {
             wait_since = now;
-          } else if (now - wait_since > kWaitLimitNs) {
+          } else if (now - wait_since > p.wait_limit_ns) {
             raise_error(p.err, PA_DEVERR_TIMEOUT);
             it.valid = false;  // give up on this consumer; it times out on its own
           }
@@ -596,7 +598,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
       if (!__any_sync(0xffffffffu, did)) __nanosleep(64);
     }
-    cp_async_wait<0>();  // nothing of ours may still land in shared memory after exit
+    // Nothing of ours may still land in shared memory after the CTA exits.
+    // The table entries: cp.async groups.  The K/V/q copies: a consumer that
+    // gave up (or a ring this lane gave up on) may leave stages in flight, so
+    // the lane waits for the last phase it started on each stage of its
+    // ring to complete, with the full limit (a copy lands within
+    // microseconds; only a broken copy engine would exhaust it).
+    cp_async_wait<0>();
+    if (lane < W) {
+      for (int i = 0; i < NS; ++i) {
+        const int n_i = issued / NS + (i < issued % NS ? 1 : 0);  // phases started on stage i
+        if (n_i > 0 && !mbar_wait_bounded(cbase + Tr::OFF_FULL + 8 * i, (n_i - 1) & 1, kDefaultWaitLimitNs))
+          raise_error(p.err, PA_DEVERR_TIMEOUT);
+      }
+    }
     return;
   }
 
@@ -948,10 +963,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
   while (it.valid) {
     // ---- one fragment: units j0 .. jend-1 of segment (s, kvh)
-    if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
+    if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, p.wait_limit_ns)) {
       if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
       break;  // the producer stops feeding this ring when its empty barrier times out
     }
+    // 8-bit caches with a bf16 query: the products run in f16 (the widened
+    // cache values are exact f16), so the query group is brought into f16's
+    // range first.  Every element is multiplied by 2^qexp, the power of two
+    // that puts the group's largest |q| in [2^14, 2^15); the scores are
+    // multiplied back by 2^-qexp.  Both steps are exact, and so is the f16
+    // rounding of every element within 2^28 of the group's largest (bf16 has 8
+    // significant bits, f16 11); smaller elements can lose bits as f16
+    // subnormals, an absolute error below 2^-38 of the largest element.
+    constexpr bool q_rescale = k8bit && std::is_same<QT, bf16_t>::value;
+    int qexp = 0;
     {
       // the query group rode on the fragment's first stage
       const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * STG + 2 * Tr::TILE;
@@ -968,11 +993,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           if (row_ok) {
             w0 = *reinterpret_cast<const uint32_t*>(qr + (row * D + d) * 2);
             w1 = *reinterpret_cast<const uint32_t*>(qr + (row * D + d2) * 2);
-          }
-          if constexpr (k8bit && std::is_same<QT, bf16_t>::value) {
-            const float2 f0 = widen2<bf16_t>(w0), f1 = widen2<bf16_t>(w1);
-            w0 = pack2<false>(f0.x, f0.y);
-            w1 = pack2<false>(f1.x, f1.y);
           }
           if (h == 0) {
             qa0[s] = w0;
@@ -991,8 +1011,41 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         }
       }
     }
+    if constexpr (q_rescale) {
+      // largest |q| of the group (bf16 halves read as floats), over the warp
+      auto amax2 = [](float a, uint32_t w) {
+        return fmaxf(a, fmaxf(__uint_as_float((w << 16) & 0x7fffffffu), __uint_as_float(w & 0x7fff0000u)));
+      };
+      float qmax = 0.f;
+#pragma unroll
+      for (int s = 0; s < Tr::KS; ++s) {
+        qmax = amax2(amax2(qmax, qa0[s]), qa1[s]);
+        if constexpr (NH == 2) qmax = amax2(amax2(qmax, qb0[s]), qb1[s]);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+      // qmax in [2^E, 2^(E+1)) -> qexp = 14 - E; all-zero groups keep qexp = 0;
+      // the clamp keeps both 2^qexp and the scale below normal float32 numbers
+      const int ebits = (__float_as_int(qmax) >> 23) & 0xff;
+      qexp = qmax > 0.f ? min(100, max(-100, 141 - ebits)) : 0;
+      const float mul = __int_as_float((127 + qexp) << 23);
+      auto narrow = [&](uint32_t w) {
+        const float2 f = widen2<bf16_t>(w);
+        return pack2<false>(f.x * mul, f.y * mul);
+      };
+#pragma unroll
+      for (int s = 0; s < Tr::KS; ++s) {
+        qa0[s] = narrow(qa0[s]);
+        qa1[s] = narrow(qa1[s]);
+        if constexpr (NH == 2) {
+          qb0[s] = narrow(qb0[s]);
+          qb1[s] = narrow(qb1[s]);
+        }
+      }
+    }
     score_scale = p.qk_scale_log2;
     if constexpr (k8bit) score_scale *= __ldg(p.k_scale + it.kvh);
+    if constexpr (q_rescale) score_scale *= __int_as_float((127 - qexp) << 23);
     if constexpr (std::is_same<KVT, i8_t>::value) {
       const uint32_t zk = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.k_zero_point + it.kvh))));
       const uint32_t zv = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.v_zero_point + it.kvh))));
@@ -1034,7 +1087,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
       if (it.j + 1 == it.jend) break;
       ++it.j;
-      if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, kWaitLimitNs)) {
+      if (!mbar_wait_bounded(wbase_u32 + Tr::OFF_FULL + 8 * cst, cpar, p.wait_limit_ns)) {
         if (lane == 0) raise_error(p.err, PA_DEVERR_TIMEOUT);
         timed_out = true;
         break;

@@ -9,6 +9,11 @@
 
 namespace pa {
 
+// Default limit of every wait on a decode pipeline barrier; a wait that runs
+// out records PA_DEVERR_TIMEOUT instead of hanging.  The wait for a CTA's own
+// copies in flight before it exits always uses this limit.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
 // K/V TMA boxes are min(unit rows, block_size) whole rows; both are
 // multiples of this (one 128-byte-swizzle atom is 8 x 128 bytes).
 constexpr int kBoxRowQuantum = 8;
@@ -82,6 +87,8 @@ struct DecodeParams {
   int pending_cap;
   unsigned int* err;            // per-device error word
   int stages;                   // K/V pipeline stages per warp
+  uint64_t wait_limit_ns;       // limit of every wait on a pipeline barrier (PA_DEVERR_TIMEOUT after it)
+  int withhold_copies;          // testing hook: the producer issues no copy, so every consumer wait runs out
 };
 
 // Compile-time variant of the decode kernel.

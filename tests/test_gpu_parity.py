@@ -265,3 +265,23 @@ def test_seq_len_beyond_table_capacity_flags_error():
     b.seq_lens[0] = b.max_blocks_per_seq * 16 + 100
     _, _, _, err = run_gpu(b, v)
     assert err & pa.PA_DEVERR_SEQ_LEN
+
+
+@pytest.mark.parametrize("wl", ["fp8_mix", "int8_mix"])
+@pytest.mark.parametrize("e", [17, -20])
+def test_8bit_cache_bf16_query_outside_f16_range(wl, e):
+    """bf16 queries beyond f16's range on 8-bit caches, whose products run in f16: q = N(0,1)·2^e with the
+    softmax scale 2^-e/√d, so the scores are those of an ordinary batch while every |q| is above 65504
+    somewhere (e = 17) or below f16's smallest normal 2^-14 everywhere (e = -20)."""
+    b = workloads.make_batch(wl, seed=13, num_seqs=6, lengths=("lognormal", 6.0, 1.0, 16, 1200))
+    b.scale = float(np.float32(2.0 ** -e / np.sqrt(128.0)))
+    v = workloads.host_values(b, seed=13)
+    q = oracle.bf16_bits_to_f64(v["q"]) * 2.0 ** e          # exact: a power of two times a bf16 value
+    v["q"] = workloads.bf16_bits_from_f32(q.astype(np.float32))
+    assert np.array_equal(oracle.bf16_bits_to_f64(v["q"]), q)
+    aq = np.abs(q)
+    if e > 0:
+        assert aq.max() > 65504.0
+    else:
+        assert aq.max() < 2.0 ** -14
+    _check(b, v)
