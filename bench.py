@@ -110,31 +110,64 @@ def load_traffic(workload: str):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi sampled every 50 ms from before the timed regions to after them.
+
+    The sampler selects the GPU by UUID (the CUDA device index and nvidia-smi's index differ when
+    CUDA_VISIBLE_DEVICES is set); if that form yields no sample it retries with the index.  start()
+    returns once the first sample has been written, so that a short timed region is still covered.
+    """
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_uuid: str | None):
+    def __init__(self, device_uuid: str | None, device_index: int):
         self.proc = None
+        self.fh = None
         self.out = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
-        if device_uuid:
-            cmd[1:1] = ["-i", device_uuid]
-        try:
-            self.fh = open(self.out, "w")
-            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
+        self.selectors = [s for s in (device_uuid, str(device_index)) if s]
+        self.note = None
+
+    def _spawn(self, sel):
+        cmd = ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        self.fh = open(self.out, "w")
+        self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+
+    def _kill(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
             self.proc = None
+        if self.fh is not None:
+            self.fh.close()
+            self.fh = None
+
+    def start(self, timeout_s: float = 5.0):
+        for sel in self.selectors:
+            try:
+                self._spawn(sel)
+            except (OSError, FileNotFoundError):
+                self.proc = None
+                self.note = "nvidia-smi not available"
+                return self
+            t0 = time.time()
+            while time.time() - t0 < timeout_s:
+                if os.path.getsize(self.out) > 0:
+                    self.note = f"nvidia-smi -i {sel}"
+                    return self
+                if self.proc.poll() is not None:
+                    break
+                time.sleep(0.02)
+            self._kill()
+        self.note = "nvidia-smi gave no sample"
+        return self
 
     def stop(self) -> dict | None:
         if self.proc is None:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.fh.close()
+        self._kill()
         rows = []
         with open(self.out) as f:
             for line in f:
@@ -144,23 +177,31 @@ class ClockSampler:
         os.unlink(self.out)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        power = [num(r[3]) for r in rows]
         reasons = set()
         for r in rows:
             for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+        pairs = [(c, w) for c, w in zip(sm, power) if c is not None]
         # samples under load: power above the midpoint of the observed range
-        if power:
-            thr = (min(power) + max(power)) / 2
-            loaded = [c for c, p in zip(sm, power) if p >= thr] or sm
+        if pairs and all(w is not None for _, w in pairs):
+            lo, hi = min(w for _, w in pairs), max(w for _, w in pairs)
+            loaded = [c for c, w in pairs if w >= (lo + hi) / 2]
         else:
-            loaded = sm
+            loaded = [c for c, _ in pairs]
         return {"sm_mhz": float(np.median(loaded)) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "source": self.note}
 
 
 # ----------------------------------------------------------------------------- CPU oracle baseline
@@ -303,6 +344,113 @@ def barrier(world_size: int):
         dist.barrier()
 
 
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal bandwidth (~8 TB/s), the basis the ">= 70 %" target is stated on
+MIN_TIMED_S = 1.0          # every timed loop is repeated until its repeats cover at least this long
+
+
+def lead_gpu(torch, us: float = 300.0):
+    """Keep the stream busy for about `us` microseconds before a timed region starts (outside it), so that the
+    host has enqueued the region's first launches by the time the GPU reaches it: the region then times the
+    device, not the host's latency to its first launch."""
+    torch.cuda._sleep(int(us * 2.2e3))  # cycles; at most 2.07 GHz here, so at least `us`
+
+
+def repeat_until(one, world: int, min_s: float = MIN_TIMED_S):
+    """Run one() (the milliseconds of one timed repeat) until the repeats cover min_s seconds.  The repeat
+    count is fixed after the first repeat and agreed across ranks (max), so every rank runs the same loops."""
+    first = one()
+    n = max(1, math.ceil(min_s * 1e3 / max(first, 1e-6)))
+    n = int(max_over_ranks(float(min(n, 100000)), world))
+    return [first] + [one() for _ in range(n - 1)]
+
+
+def spread(times_ms, per: int) -> dict:
+    a = np.asarray(times_ms, dtype=np.float64) / per
+    return {"n": int(a.size), "median_ms": round(float(np.median(a)), 6), "min_ms": round(float(a.min()), 6),
+            "max_ms": round(float(a.max()), 6)}
+
+
+class DecodeCase:
+    """One workload resident on the device: rotating KV pool replicas (> 4x L2 together), tables, lengths,
+    queries, the new token's rows and slots, the output and the split workspace."""
+
+    def __init__(self, pa, torch, dev, workload, seed, *, q_len=1, partition_size=0, replicas=0, block_size=None):
+        ov = {} if block_size is None else {"block_size": block_size}
+        self.batch = b = workloads.make_batch(workload, seed=seed, **ov)
+        vals = workloads.device_values(b, seed, dev)
+        B, Hkv, D, S, Hq = b.block_size, b.num_kv_heads, b.head_dim, b.num_seqs, b.num_heads
+        self.kz, self.vz = vals.get("k_zero_point"), vals.get("v_zero_point")
+        if b.kv_fmt in ("e4m3", "i8"):
+            pa.reshape_and_cache(vals["k_src"], vals["v_src"], vals["k_cache"], vals["v_cache"], vals["src_slots"], B,
+                                 k_inv_scale=vals["k_inv_scale"], v_inv_scale=vals["v_inv_scale"],
+                                 k_zero_point=self.kz, v_zero_point=self.vz)
+            del vals["k_src"], vals["v_src"]
+        self.pool_bytes = 2 * vals["k_cache"].numel() * vals["k_cache"].element_size()
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.replicas = replicas or max(2, math.ceil(4 * self.l2 / self.pool_bytes) + 1)
+        self.caches = [(vals["k_cache"], vals["v_cache"])] + [
+            (vals["k_cache"].clone(), vals["v_cache"].clone()) for _ in range(self.replicas - 1)]
+        self.tables = torch.from_numpy(b.block_tables).to(dev)
+        self.lens = torch.from_numpy(b.seq_lens).to(dev)
+        self.slots = torch.from_numpy(b.new_slots).to(dev)
+        self.q, self.k_new, self.v_new = vals["q"], vals["k_new"], vals["v_new"]
+        self.ks, self.vs = vals.get("k_scale"), vals.get("v_scale")
+        self.kis, self.vis = vals.get("k_inv_scale"), vals.get("v_inv_scale")
+        self.q_len, self.partition_size = q_len, partition_size
+        if q_len > 1:   # the q_len newest positions are queries: [S, L, H_q, d]
+            gq = torch.Generator(device=dev)
+            gq.manual_seed(seed * 7 + 3)
+            self.q = torch.randn((S, q_len, Hq, D), generator=gq, device=dev, dtype=torch.float32).to(self.q.dtype)
+        self.out = torch.empty(self.q.shape, dtype=self.q.dtype, device=dev)
+        nws = pa.decode_workspace_bytes(S, Hq, Hkv, D, B, b.max_blocks_per_seq, partition_size,
+                                        pa.dtype_code(vals["k_cache"]), q_len=q_len)
+        self.ws = pa.new_workspace(nws, dev) if nws else None
+        self.geometry = pa.pa_decode_launch_config(S, Hq, Hkv, D, B, b.max_blocks_per_seq, partition_size,
+                                                   pa.dtype_code(self.q), pa.dtype_code(vals["k_cache"]))
+
+    def decode(self, pa, i, stream, *, window=0, pdl=False, fused=False, q=None, tables=None, lens=None,
+               k_new=None, v_new=None):
+        kc, vc = self.caches[i % self.replicas]
+        b = self.batch
+        extra = {}
+        if fused:
+            extra = dict(k_new=self.k_new if k_new is None else k_new, v_new=self.v_new if v_new is None else v_new,
+                         k_inv_scale=self.kis, v_inv_scale=self.vis)
+        pa.decode(self.out, self.q if q is None else q, kc, vc, self.tables if tables is None else tables,
+                  self.lens if lens is None else lens, b.num_kv_heads, b.scale, b.block_size, k_scale=self.ks,
+                  v_scale=self.vs, partition_size=self.partition_size, workspace=self.ws, stream=stream,
+                  window=window, k_zero_point=self.kz, v_zero_point=self.vz, pdl=pdl, **extra)
+
+    def cache_write(self, pa, i, stream, *, pdl=False, k=None, v=None, slots=None):
+        kc, vc = self.caches[i % self.replicas]
+        pa.reshape_and_cache(self.k_new if k is None else k, self.v_new if v is None else v, kc, vc,
+                             self.slots if slots is None else slots, self.batch.block_size, k_inv_scale=self.kis,
+                             v_inv_scale=self.vis, k_zero_point=self.kz, v_zero_point=self.vz, stream=stream, pdl=pdl)
+
+    def time_decode_alone(self, pa, torch, stream, K, world, *, window=0, fused=False):
+        """Repeats of K decode launches, each an ordinary launch between two events on the launching stream.
+        Returns the per-repeat mean launch time (ms) of every repeat."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        ctr = [0]
+
+        def one():
+            barrier(world)
+            torch.cuda.synchronize()
+            lead_gpu(torch)
+            for i in range(K):
+                ev[i][0].record(stream)
+                self.decode(pa, ctr[0], stream, window=window, fused=fused)
+                ev[i][1].record(stream)
+                ctr[0] += 1
+            torch.cuda.synchronize()
+            barrier(world)
+            return float(np.sum([a.elapsed_time(b_) for a, b_ in ev]))
+
+        for i in range(3):
+            self.decode(pa, i, stream, window=window, fused=fused)
+        return [t / K for t in repeat_until(one, world)]
+
+
 def run_ours(args):
     import torch
     import paged_kv_cache_144_gb300 as pa
@@ -310,75 +458,33 @@ def run_ours(args):
     rank, world, local = setup_distributed()
     dev = torch.device("cuda", local)
     pa.load()
-    batch = workloads.make_batch(args.workload, seed=args.seed + 1000 * rank)
-    vals = workloads.device_values(batch, args.seed + 1000 * rank, dev)
+    c = DecodeCase(pa, torch, dev, args.workload, args.seed + 1000 * rank, q_len=args.q_len,
+                   partition_size=args.partition_size, replicas=args.replicas, block_size=args.block_size)
+    batch = c.batch
     B, Hkv, D, S, Hq = batch.block_size, batch.num_kv_heads, batch.head_dim, batch.num_seqs, batch.num_heads
-    kz, vz = vals.get("k_zero_point"), vals.get("v_zero_point")
-    if batch.kv_fmt in ("e4m3", "i8"):
-        pa.reshape_and_cache(vals["k_src"], vals["v_src"], vals["k_cache"], vals["v_cache"], vals["src_slots"], B,
-                             k_inv_scale=vals["k_inv_scale"], v_inv_scale=vals["v_inv_scale"], k_zero_point=kz,
-                             v_zero_point=vz)
-        del vals["k_src"], vals["v_src"]
-    pool_bytes = 2 * vals["k_cache"].numel() * vals["k_cache"].element_size()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    replicas = args.replicas or max(2, math.ceil(4 * l2 / pool_bytes) + 1)
-    caches = [(vals["k_cache"], vals["v_cache"])] + [(vals["k_cache"].clone(), vals["v_cache"].clone())
-                                                     for _ in range(replicas - 1)]
-    tables = torch.from_numpy(batch.block_tables).to(dev)
-    lens = torch.from_numpy(batch.seq_lens).to(dev)
-    slots = torch.from_numpy(batch.new_slots).to(dev)
-    q, k_new, v_new = vals["q"], vals["k_new"], vals["v_new"]
-    ks, vs = vals.get("k_scale"), vals.get("v_scale")
-    kis, vis = vals.get("k_inv_scale"), vals.get("v_inv_scale")
-    if args.q_len > 1:   # the q_len newest positions are queries: [S, L, H_q, d]
-        gq = torch.Generator(device=dev)
-        gq.manual_seed(args.seed * 7 + 3)
-        q = torch.randn((S, args.q_len, Hq, D), generator=gq, device=dev, dtype=torch.float32).to(q.dtype)
-    out = torch.empty(q.shape, dtype=q.dtype, device=dev)
-    nws = pa.decode_workspace_bytes(S, Hq, Hkv, D, B, batch.max_blocks_per_seq, args.partition_size,
-                                    pa.dtype_code(vals["k_cache"]), q_len=args.q_len)
-    ws = pa.new_workspace(nws, dev) if nws else None
-    geometry = pa.pa_decode_launch_config(S, Hq, Hkv, D, B, batch.max_blocks_per_seq, args.partition_size,
-                                          pa.dtype_code(q), pa.dtype_code(vals["k_cache"]))
     no_pairs = torch.empty((0, 2), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-
     pdl = not args.no_pdl
 
     def step(i):
         # one step as a serving loop issues it: nothing between its launches, so the decode's set-up
         # (lengths, prefix sums, block-table prefetch) overlaps the launch before it (pdl)
-        kc, vc = caches[i % replicas]
         if args.fused:
             # one launch: the cache write of the new rows fused into the decode
-            pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                      partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                      k_zero_point=kz, v_zero_point=vz, k_new=k_new, v_new=v_new, k_inv_scale=kis,
-                      v_inv_scale=vis, pdl=pdl)
+            c.decode(pa, i, stream, window=args.window, pdl=pdl, fused=True)
             return
-        pa.reshape_and_cache(k_new, v_new, kc, vc, slots, B, k_inv_scale=kis, v_inv_scale=vis, k_zero_point=kz,
-                             v_zero_point=vz, stream=stream, pdl=pdl)
+        c.cache_write(pa, i, stream, pdl=pdl)
+        kc, vc = c.caches[i % c.replicas]
         pa.copy_blocks(kc, vc, no_pairs, stream=stream)          # no shared block is written: no launch
-        pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                  partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                  k_zero_point=kz, v_zero_point=vz, pdl=pdl)
+        c.decode(pa, i, stream, window=args.window, pdl=pdl)
 
-    def decode_alone(i, ev):
-        # the decode kernel by itself, an ordinary launch between two events (the roofline's duration)
-        kc, vc = caches[i % replicas]
-        extra = dict(k_new=k_new, v_new=v_new, k_inv_scale=kis, v_inv_scale=vis) if args.fused else {}
-        ev[0].record(stream)
-        pa.decode(out, q, kc, vc, tables, lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                  partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                  k_zero_point=kz, v_zero_point=vz, **extra)
-        ev[1].record(stream)
-
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        uuid = None
-    sampler = ClockSampler(uuid) if rank == 0 else None
+    sampler = None
+    if rank == 0:
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            uuid = None
+        sampler = ClockSampler(uuid, local).start()
 
     for i in range(args.warmup):
         step(i)
@@ -386,39 +492,52 @@ def run_ours(args):
     if pa.get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
     K = args.steps
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(K):
-        step(args.warmup + i)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    elapsed_ms = t_start.elapsed_time(t_end)
+    ctr = [args.warmup]
+
+    def step_repeat():
+        # exactly K steps between two events, barrier + synchronize on both sides
+        barrier(world)
+        torch.cuda.synchronize()
+        lead_gpu(torch)
+        t_start.record(stream)
+        for _ in range(K):
+            step(ctr[0])
+            ctr[0] += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return t_start.elapsed_time(t_end)
+
+    step_times = repeat_until(step_repeat, world)
     # second timed region: K decode launches alone, each between two events on the launching stream
-    for i in range(3):
-        decode_alone(i, dec_ev[0])
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(K):
-        decode_alone(args.warmup + i, dec_ev[i])
-    torch.cuda.synchronize()
-    barrier(world)
+    dec_times = c.time_decode_alone(pa, torch, stream, K, world, window=args.window, fused=args.fused)
+    # the two headline configurations' decode kernels, timed the same way (1 GPU)
+    per_config = []
+    if world == 1 and not args.no_per_config:
+        for wl, kw in (("long_32k", {}), ("fp8_mix", {"block_size": 16})):
+            if wl == args.workload and not kw:
+                continue
+            pc = DecodeCase(pa, torch, dev, wl, args.seed, **kw)
+            t = pc.time_decode_alone(pa, torch, stream, K, world)
+            ab = algorithmic_bytes(pc.batch)["decode"]
+            per_config.append((wl, pc.batch, t, ab))
+            del pc
+            torch.cuda.empty_cache()
     clocks = sampler.stop() if sampler else None
-    dec_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in dec_ev])), world)
     err = pa.get_device_error()
     if err != 0:
         raise RuntimeError(f"device error bits {err} in the timed region")
+    ms_step = max_over_ranks(float(np.median(step_times)) / K, world)
+    dec_ms = max_over_ranks(float(np.median(dec_times)), world)
 
     # end to end through the public API: pinned host inputs -> device, step, result -> host
     e2e = None
     if not args.no_e2e:
-        h_q = q.cpu().pin_memory()
-        h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-        h_slots, h_tables, h_lens = slots.cpu().pin_memory(), tables.cpu().pin_memory(), lens.cpu().pin_memory()
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_q = c.q.cpu().pin_memory()
+        h_k, h_v = c.k_new.cpu().pin_memory(), c.v_new.cpu().pin_memory()
+        h_slots, h_tables, h_lens = c.slots.cpu().pin_memory(), c.tables.cpu().pin_memory(), c.lens.cpu().pin_memory()
+        h_out = torch.empty(c.out.shape, dtype=c.out.dtype).pin_memory()
         # The step's inputs are staged in one pinned host buffer and cross in one copy, as a serving loop
         # stages them; each tensor sits at a 256-byte aligned offset (the library wants 16-byte bases).
         parts = (h_q, h_k, h_v, h_slots, h_tables, h_lens)
@@ -438,53 +557,49 @@ def run_ours(args):
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step(i):
-            kc, vc = caches[i % replicas]
             d_stage.copy_(h_stage, non_blocking=True)
             if args.fused:
-                pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                          partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                          k_zero_point=kz, v_zero_point=vz, k_new=d_k, v_new=d_v, k_inv_scale=kis,
-                          v_inv_scale=vis, pdl=pdl)
+                c.decode(pa, i, stream, window=args.window, pdl=pdl, fused=True, q=d_q, tables=d_tables, lens=d_lens,
+                         k_new=d_k, v_new=d_v)
             else:
-                pa.reshape_and_cache(d_k, d_v, kc, vc, d_slots, B, k_inv_scale=kis, v_inv_scale=vis,
-                                     k_zero_point=kz, v_zero_point=vz, stream=stream, pdl=pdl)
-                pa.decode(out, d_q, kc, vc, d_tables, d_lens, Hkv, batch.scale, B, k_scale=ks, v_scale=vs,
-                          partition_size=args.partition_size, workspace=ws, stream=stream, window=args.window,
-                          k_zero_point=kz, v_zero_point=vz, pdl=pdl)
-            h_out.copy_(out, non_blocking=True)
+                c.cache_write(pa, i, stream, pdl=pdl, k=d_k, v=d_v, slots=d_slots)
+                c.decode(pa, i, stream, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens)
+            h_out.copy_(c.out, non_blocking=True)
             stream.synchronize()
 
         for i in range(args.warmup):
             e2e_step(i)
-        barrier(world)
-        t0 = time.perf_counter()
-        for i in range(K):
-            e2e_step(i)
-        e2e_s = time.perf_counter() - t0
-        barrier(world)
-        e2e_s = max_over_ranks(e2e_s, world)
-        e2e = (e2e_s, h2d, d2h)
+
+        def e2e_repeat():
+            barrier(world)
+            t0 = time.perf_counter()
+            for i in range(K):
+                e2e_step(i)
+            dt = time.perf_counter() - t0
+            barrier(world)
+            return dt * 1e3
+
+        e2e_times = repeat_until(e2e_repeat, world)
+        e2e = (max_over_ranks(float(np.median(e2e_times)) / K, world), h2d, d2h, e2e_times)
 
     ab = algorithmic_bytes(batch, args.window, args.q_len)
-    elapsed_ms = max_over_ranks(elapsed_ms, world)
     total_step_bytes = sum_over_ranks(float(ab["step"]), world)
     total_kv = sum_over_ranks(float(ab["kv"]), world)
     total_seqs = sum_over_ranks(float(S), world)
     total_ctx = sum_over_ranks(float(batch.seq_lens.sum()), world)
-    ms_step = elapsed_ms / K
     peaks = load_peaks()
     value = total_step_bytes / (ms_step * 1e-3) / 1e9
     kernel_bytes = ab["step"] if args.fused else ab["decode"]   # fused: the launch also moves the new rows
     achieved = kernel_bytes / (dec_ms * 1e-3) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_rate(batch, {"q": q, "k_cache": caches[0][0], "v_cache": caches[0][1], "k_scale": ks,
-                                  "v_scale": vs}, target_s=args.cpu_seconds, seed=args.seed)
+        cpu = oracle_rate(batch, {"q": c.q, "k_cache": c.caches[0][0], "v_cache": c.caches[0][1], "k_scale": c.ks,
+                                  "v_scale": c.vs}, target_s=args.cpu_seconds, seed=args.seed)
     if rank != 0:
         return
     # the committed counters were taken on the plain launch of the workload; a window, several queries or
     # the fused append change what the kernel moves, so those runs report no traffic
-    plain = not args.fused and args.q_len == 1 and not args.window
+    plain = not args.fused and args.q_len == 1 and not args.window and args.block_size is None
     traffic = load_traffic(args.workload) if plain else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -501,30 +616,50 @@ def run_ours(args):
                      else "reshape_and_cache(1 new token/seq) + pa_decode") +
                     ((", launched with programmatic dependent launch" if args.fused
                       else ", both launched with programmatic dependent launch") if pdl else ""),
-            "kernel_timing": "a second timed loop of K decode launches alone (ordinary launches), "
-                             "CUDA events around each on the launching stream, same KV rotation",
-            "l2": f"{replicas} rotating KV pools ({replicas * pool_bytes / 1e9:.2f} GB) > L2 ({l2 / 1e6:.0f} MB)",
+            "timing": f"value: repeats of exactly K={K} steps back to back (so each step's launches overlap the one "
+                      f"before through programmatic dependent launch), CUDA events on the stream, barrier + "
+                      f"synchronize around each repeat, repeated until >= {MIN_TIMED_S:.0f} s, median repeat; "
+                      "roofline: a second loop of decode launches alone (ordinary launches, no overlap), an event "
+                      "pair around each launch, repeated the same way. The two loops differ in shape, so the "
+                      "step can be shorter than the decode launch alone.",
+            "l2": f"{c.replicas} rotating KV pools ({c.replicas * c.pool_bytes / 1e9:.2f} GB) > L2 "
+                  f"({c.l2 / 1e6:.0f} MB): inputs larger than L2, no flush",
             "seed": args.seed,
-            "launch": geometry,
+            "launch": c.geometry,
         },
+        "repeats": {"step": spread(step_times, K), "decode_alone": spread(dec_times, 1)},
         "pct_of_hbm_peak": round(100.0 * value / peaks["hbm_gbs"], 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
         "kv_read_gbps": round(total_kv / (ms_step * 1e-3) / 1e9, 2),
         "decode_tokens_per_s": round(total_seqs * args.q_len / (ms_step * 1e-3), 1),
         "context_tokens_per_s": round(total_ctx / (ms_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (pa_decode, one launch)",
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 6),
                      "traffic": traffic},
+        "per_config": [
+            {"workload": f"{wl}: {WORKLOAD_TEXT.get(wl, '')}" + (f" (block_size {pb.block_size})" if wl == "fp8_mix" else ""),
+             "avg_launch_ms": round(float(np.median(t)), 6), "repeats": spread(t, 1),
+             "algorithmic_bytes": abytes,
+             "achieved_gbs": round(abytes / (float(np.median(t)) * 1e-3) / 1e9, 2),
+             "frac": round(abytes / (float(np.median(t)) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+             "frac_of_nominal_8tbs": round(abytes / (float(np.median(t)) * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+             "traffic": load_traffic(wl) if pb.block_size == 16 else None}
+            for wl, pb, t, abytes in per_config],
         "cpu_baseline": cpu,
-        "gpu_launches": (1 if args.fused else 2) * K,
+        # launches of this library's kernels inside the timed regions (warm-ups excluded)
+        "gpu_launches": (1 if args.fused else 2) * K * len(step_times) + K * len(dec_times) +
+                        sum(K * len(t) for _, _, t, _ in per_config) +
+                        (0 if e2e is None else (1 if args.fused else 2) * K * len(e2e[3])),
         "clocks": clocks,
     }
     if e2e is not None:
-        e2e_s, h2d, d2h = e2e
-        line["e2e"] = {"value": round(total_step_bytes / (e2e_s / K) / 1e9, 2), "unit": UNIT,
+        e2e_ms, h2d, d2h, e2e_times = e2e
+        line["e2e"] = {"value": round(total_step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": round(1e3 * e2e_s / K, 6)}
+                       "ms_per_step": round(e2e_ms, 6), "repeats": spread(e2e_times, K)}
     print(json.dumps(line), flush=True)
     if args.json_out:
         with open(args.json_out, "w") as f:
@@ -608,10 +743,12 @@ def run_beam(args):
         ev[1].record(stream)
 
     sampler = None
-    try:
-        sampler = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid)) if rank == 0 else None
-    except Exception:
-        sampler = None
+    if rank == 0:
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            uuid = None
+        sampler = ClockSampler(uuid, local).start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -620,27 +757,41 @@ def run_beam(args):
     K = args.steps
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(K):
-        step(args.warmup + i)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    ctr = [args.warmup]
+
+    def step_repeat():
+        barrier(world)
+        torch.cuda.synchronize()
+        lead_gpu(torch)
+        t_start.record(stream)
+        for _ in range(K):
+            step(ctr[0])
+            ctr[0] += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return t_start.elapsed_time(t_end)
+
+    def dec_repeat():
+        barrier(world)
+        torch.cuda.synchronize()
+        lead_gpu(torch)
+        for i in range(K):
+            decode_alone(ctr[0], dec_ev[i])
+            ctr[0] += 1
+        torch.cuda.synchronize()
+        barrier(world)
+        return float(np.sum([a_.elapsed_time(b_) for a_, b_ in dec_ev]))
+
+    step_times = repeat_until(step_repeat, world)
     for i in range(3):
         decode_alone(i, dec_ev[0])
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(K):
-        decode_alone(args.warmup + i, dec_ev[i])
-    torch.cuda.synchronize()
-    barrier(world)
+    dec_times = [t / K for t in repeat_until(dec_repeat, world)]
     clocks = sampler.stop() if sampler else None
     if pa.get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
-    ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / K
-    dec_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in dec_ev])), world)
+    ms_step = max_over_ranks(float(np.median(step_times)), world) / K
+    dec_ms = max_over_ranks(float(np.median(dec_times)), world)
     peaks = load_peaks()
     total_step = sum_over_ranks(float(decode_bytes + append_bytes), world)
     value = total_step / (ms_step * 1e-3) / 1e9
@@ -669,8 +820,9 @@ def run_beam(args):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
                      "algorithmic_bytes_per_launch": decode_bytes, "bytes_basis": "unique KV rows",
                      "avg_launch_ms": round(dec_ms, 6), "traffic": load_traffic("beam_cow")},
+        "repeats": {"step": spread(step_times, K), "decode_alone": spread(dec_times, 1)},
         "cpu_baseline": None,
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K * len(step_times) + K * len(dec_times),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -764,6 +916,9 @@ def main():
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window decode over the last W positions (bytes counted over the window)")
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--block-size", type=int, default=None, help="override the workload's block size")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the decode timing of the long_32k and fp8_mix configurations")
     ap.add_argument("--replicas", type=int, default=0, help="KV pool replicas to rotate (0 = enough for > 4x L2)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-pdl", action="store_true",
