@@ -36,7 +36,7 @@
  *    8-bit (FP8, INT8) caches; block_size a power of two from 8 to 1024 (16
  *    and 32 are the usual sizes); num_heads = G * num_kv_heads with
  *    1 <= G <= 8; with q_len queries per sequence (pa_decode_ex),
- *    q_len * G <= 16.
+ *    q_len * G <= 64.
  */
 #ifndef PAGEDATTN_PA_H
 #define PAGEDATTN_PA_H
@@ -188,8 +188,10 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            head_dim elements per sequence, out packed) and query i attends
  *            to positions up to its own, T-L+i (with a window: the last
  *            `window` of them).  A query whose position is negative (T < L)
- *            gets out = 0.  L * (num_heads / num_kv_heads) <= 16, else
- *            PA_ERR_UNSUPPORTED.  This is the verification step of
+ *            gets out = 0.  L * (num_heads / num_kv_heads) <= 64, else
+ *            PA_ERR_UNSUPPORTED (up to 16 (query, head) rows are served by
+ *            one consumer warp per K/V stage, more by 2-4 warps that share
+ *            each stage, 16 rows each).  This is the verification step of
  *            speculative decoding, which the explainer names alongside paged
  *            KV memory.
  *   pdl      nonzero: launch with programmatic dependent launch, so that the

@@ -45,6 +45,7 @@ int cuda_status(cudaError_t e, const char* where) {
 }
 
 constexpr int kMaxSeqs = 16384;  // prefix sums of the batch live in shared memory
+constexpr int kMaxQueryRows = 64;  // q_len * G: up to four 16-row consumer warps share a ring
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -155,8 +156,11 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
   plan->key.q_dtype = q_dtype;
   plan->key.kv_dtype = kv_dtype;
   plan->key.head_dim = head_dim;
-  // several queries per sequence are served by the 16-row variants only
+  // several queries per sequence are served by the 16-row variants only, 16
+  // rows per consumer warp: ceil(q_len * G / 16) warps share a ring
   plan->key.gmax = q_len > 1 ? 16 : gmax_for_rows(num_heads / num_kv_heads);
+  const int rows = q_len * (num_heads / num_kv_heads);
+  plan->key.row_groups = q_len > 1 ? (rows + 15) / 16 : 1;
   plan->key.unit_rows = unit_rows_for(kv_dtype, block_size, plan->key.gmax, append);
   if (!pa::decode_geometry(plan->key, num_seqs, &plan->geo)) return PA_ERR_UNSUPPORTED;
   const int ur = plan->geo.unit_rows;
@@ -173,18 +177,21 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     plan->bytes = 0;
     return PA_OK;
   }
-  plan->counters_bytes = (static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int) + 255) / 256 * 256;
+  // arrival counters and records are per (segment, row group of its ring)
+  const int nc = plan->geo.row_groups;
+  plan->counters_bytes = (static_cast<size_t>(num_seqs) * num_kv_heads * nc * sizeof(int) + 255) / 256 * 256;
   const size_t warps = static_cast<size_t>(plan->geo.ctas) * plan->geo.warps_per_cta;
+  const size_t rings = warps / nc;
   if (pu == 0) {
-    // balanced split: only the first and the last fragment of a warp's range
+    // balanced split: only the first and the last fragment of a ring's range
     // can be part of a split segment
     plan->records = 2 * warps;
     plan->pending_cap = 2;
   } else {
-    // fixed partitions: dealt round-robin over the warps
+    // fixed partitions: dealt round-robin over the rings
     const size_t parts = static_cast<size_t>(num_seqs) * num_kv_heads * ((max_units + pu - 1) / pu);
-    plan->records = parts;
-    plan->pending_cap = static_cast<int>((parts + warps - 1) / warps);
+    plan->records = parts * nc;
+    plan->pending_cap = static_cast<int>((parts + rings - 1) / rings);
   }
   plan->pending_offset = plan->counters_bytes + (plan->records * plan->geo.record_floats * sizeof(float) + 255) / 256 * 256;
   plan->bytes = plan->pending_offset + warps * plan->pending_cap * sizeof(int);
@@ -221,7 +228,7 @@ PA_EXPORT size_t pa_decode_workspace_bytes_ex(int num_seqs, int num_heads, int n
     memcpy(&o, opt, opt->struct_size < sizeof(o) ? opt->struct_size : sizeof(o));
   }
   const int q_len = o.q_len <= 0 ? 1 : o.q_len;
-  if (num_kv_heads > 0 && q_len * (num_heads / num_kv_heads) > 16) return static_cast<size_t>(-1);
+  if (num_kv_heads > 0 && q_len * (num_heads / num_kv_heads) > kMaxQueryRows) return static_cast<size_t>(-1);
   if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                          partition_size, kv_dtype) != PA_OK)
     return static_cast<size_t>(-1);
@@ -297,7 +304,7 @@ int prepare_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtyp
   }
   if (o.window < 0 || o.q_len < 0) return PA_ERR_SHAPE;
   const int q_len = o.q_len == 0 ? 1 : o.q_len;
-  if (num_kv_heads > 0 && q_len * (num_heads / num_kv_heads) > 16) return PA_ERR_UNSUPPORTED;
+  if (num_kv_heads > 0 && q_len * (num_heads / num_kv_heads) > kMaxQueryRows) return PA_ERR_UNSUPPORTED;
   const bool append = o.k_new != nullptr || o.v_new != nullptr;
   if (append && q_len != 1) return PA_ERR_UNSUPPORTED;
   if (append) {
@@ -363,6 +370,18 @@ int prepare_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtyp
   p.block_size = block_size;
   p.block_shift = __builtin_ctz(static_cast<unsigned>(block_size));
   p.partition_units = plan.partition_units;
+  // Balanced split: every fragment (one ring's share of one segment) is
+  // charged frag_cost units of work besides its own units (query set-up, the
+  // masked last unit, the output or the record).  Measured per ring on the
+  // GB300 with the plain split, a fragment cost 3.2 us against 1.6 us per unit
+  // for FP8 (64-row units), 4.9 against 2.3 for INT8 and 1.1 against 0.9 for
+  // bf16 (32-row units); charges of 0..4 units timed on the three mixes gave
+  // their best at 2..3, so every cache type is charged 3.
+  // PA_DECODE_FRAG_COST overrides it (tuning).
+  {
+    const int env = pa::tuning_override("PA_DECODE_FRAG_COST");
+    p.frag_cost = plan.partition_units != 0 ? 0 : (env >= 0 && env <= 64 ? env : 3);
+  }
   p.window = o.window;
   p.q_len = q_len;
   p.k_new = append ? o.k_new : nullptr;
@@ -374,6 +393,8 @@ int prepare_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtyp
   p.k_cache = const_cast<void*>(k_cache);
   p.v_cache = const_cast<void*>(v_cache);
   p.stages = plan.geo.stages;
+  p.row_groups = plan.geo.row_groups;
+  p.stage_bytes = plan.geo.stage_bytes;
   p.seg_counters = plan.bytes ? static_cast<int*>(workspace) : nullptr;
   p.pending = plan.bytes ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + plan.pending_offset) : nullptr;
   p.pending_cap = plan.pending_cap;

@@ -140,6 +140,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Barrier among `threads` threads (whole warps) of the CTA on named barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Prefetch of the 128-byte line holding addr into L2.
 __device__ __forceinline__ void prefetch_l2(const void* addr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));

@@ -142,9 +142,10 @@ struct WorkIter {
   int frag_idx;   // ordinal of the current fragment within this warp
   int slot;       // partial-record slot, -1 when the fragment is a whole segment
   bool valid;
-  // balanced mode
-  long long u, u1;  // unit index of unit j0 of the current fragment; end of the warp's range
-  int gw;           // global warp id
+  // balanced mode: positions in the cost order (see frag_balanced)
+  long long u, u1;  // start of the current fragment; end of the ring's range
+  long long fend;   // end of the current fragment
+  int gw;           // global ring id
   // fixed mode
   int r, rstride, R;
 };
@@ -166,26 +167,59 @@ __device__ __forceinline__ int window_lo(const DecodeParams& p, int T) {
   return (p.window > 0 && first > p.window) ? first - p.window : 0;
 }
 
-__device__ __forceinline__ void frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
+// Balanced split in cost order.  The units of the batch are laid out
+// segment by segment, (s, kvh) in order, each segment charged its nu
+// attended units plus p.frag_cost for the work a fragment costs besides its
+// units (query set-up, the last partial unit, the output or record): segment
+// x occupies positions [c_x, c_x + frag_cost + nu), its unit j at
+// c_x + frag_cost + j.  The positions are split into equal contiguous
+// ranges, one per ring, and a ring owns the units whose positions fall in its
+// range, so a ring whose range crosses many short segments gets fewer units.
+// A range boundary inside a segment's leading overhead assigns the whole
+// segment to the later ring.  prefix[s] = position of sequence s's first
+// segment (its H_kv segments are consecutive, each of the same cost).
+//
+// Fills the fragment starting at it.u (the first of its units at or after
+// it.u); returns false when the ring's range holds no further unit.
+__device__ __forceinline__ bool frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
   const int Hkv = p.num_kv_heads;
-  const int s = find_seq(prefix, p.num_seqs, it.u);
-  const int nu = (prefix[s + 1] - prefix[s]) / Hkv;
-  const int r = static_cast<int>(it.u - prefix[s]);  // < 2^31: unit counts are int32
-  it.s = s;
-  it.nu = nu;
-  it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
-  it.lo = window_lo(p, it.T);
-  it.ulo = it.lo >> ur_shift;
-  it.kvh = r / nu;
-  it.j0 = it.ulo + (r - it.kvh * nu);
-  it.j = it.j0;
-  const long long seg_start = prefix[s] + static_cast<long long>(it.kvh) * nu;
-  const long long seg_end = seg_start + nu;
-  const long long fend = min(it.u1, seg_end);
-  it.jend = it.j0 + static_cast<int>(fend - it.u);
-  const bool whole = (it.u == seg_start) && (fend == seg_end);
-  it.slot = whole ? -1 : it.gw * 2 + (it.frag_idx == 0 ? 0 : 1);
-  it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
+  const int beta = p.frag_cost;
+  while (it.u < it.u1) {
+    const int s = find_seq(prefix, p.num_seqs, it.u);
+    const int seg = (prefix[s + 1] - prefix[s]) / Hkv;  // frag_cost + nu of each segment of sequence s
+    const int r = static_cast<int>(it.u - prefix[s]);  // < 2^31: positions are int32
+    const int kvh = r / seg;
+    const int off = r - kvh * seg;
+    const long long seg_start = prefix[s] + static_cast<long long>(kvh) * seg;
+    const long long fend = min(it.u1, seg_start + seg);
+    const int ja = max(0, off - beta);                        // first unit of the segment in the range
+    const int jb = static_cast<int>(fend - seg_start) - beta;  // units of the segment before fend
+    if (jb <= ja) {  // the range ends inside the segment's overhead: none of its units
+      it.u = fend;
+      continue;
+    }
+    const int nu = seg - beta;
+    it.s = s;
+    it.nu = nu;
+    it.T = prefix[p.num_seqs + 1 + s];  // clamped length, cached by the prologue
+    it.lo = window_lo(p, it.T);
+    it.ulo = it.lo >> ur_shift;
+    it.kvh = kvh;
+    it.j0 = it.ulo + ja;
+    it.j = it.j0;
+    it.jend = it.ulo + jb;
+    it.fend = fend;
+    const bool whole = ja == 0 && jb == nu;
+    it.slot = whole ? -1 : it.gw * 2 + (it.frag_idx == 0 ? 0 : 1);
+    it.nblk = (it.T + p.block_size - 1) >> p.block_shift;
+    return true;
+  }
+  return false;
+}
+
+// Ring containing cost position x of a balanced split of C positions over nw rings.
+__device__ __forceinline__ int ring_of(long long x, long long C, int nw) {
+  return static_cast<int>(((x + 1) * nw - 1) / C);
 }
 
 __device__ __forceinline__ void frag_fixed(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
@@ -216,9 +250,8 @@ __device__ __forceinline__ void iter_next_fragment(WorkIter& it, const int* pref
     if (it.r >= it.R) { it.valid = false; return; }
     frag_fixed(it, prefix, p, ur_shift);
   } else {
-    it.u += it.jend - it.j0;
-    if (it.u >= it.u1) { it.valid = false; return; }
-    frag_balanced(it, prefix, p, ur_shift);
+    it.u = it.fend;
+    if (!frag_balanced(it, prefix, p, ur_shift)) it.valid = false;
   }
 }
 
@@ -227,20 +260,21 @@ struct MergeSlots {
   bool fixed;
   int fixed_base;       // fixed partitions: slot of partition 0 of the segment
   int first_w;          // balanced split: global warp id of the first fragment
-  long long U;          // balanced split: total units
-  int nw_eff;           // balanced split: warps sharing the units
+  long long U;          // balanced split: total cost positions
+  int nw_eff;           // balanced split: rings sharing them
   long long seg_start;  // balanced split: first unit of the segment
+  int nc, rg;           // warps per ring and this warp's row group: records are per warp
   __device__ __forceinline__ int slot(int f) const {
-    if (fixed) return fixed_base + f;
+    if (fixed) return (fixed_base + f) * nc + rg;
     const int w = first_w + f;
     const long long rs = static_cast<long long>(w) * U / nw_eff;
-    return 2 * w + (rs < seg_start ? 1 : 0);
+    return (2 * w + (rs < seg_start ? 1 : 0)) * nc + rg;
   }
 };
 
 // Merges the nfr partial (m, l, acc) records of one segment with the
-// online-softmax recurrence and writes the output rows of its R = q_len * G
-// (query, head) rows.  Run by the warp that arrived last, after its unit
+// online-softmax recurrence and writes the output rows of its R (query, head)
+// rows row0 .. row0 + R - 1 (of the segment's q_len * G rows).  Run by the warp that arrived last, after its unit
 // loop, when its own pipeline stages are idle: the records are copied into
 // those stages (buf / bufp, room for cap records) a batch at a time with
 // cp.async, every copy of a batch in flight at once, and folded from shared
@@ -252,7 +286,8 @@ struct MergeSlots {
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
                                               int G, int num_heads, float vs, void* out, int out_dtype,
-                                              int64_t seq_row0, uint32_t buf, const float* bufp, int cap) {
+                                              int64_t seq_row0, int row0, uint32_t buf, const float* bufp,
+                                              int cap) {
   constexpr int EPL = D / 32;       // columns per lane
   constexpr int CH = REC / 4;       // 16-byte chunks of one record
   static_assert(REC % 4 == 0, "records are whole 16-byte chunks");
@@ -326,8 +361,9 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     if (g < R) {
-      // row g = (query g / G, head g % G) of the group
-      const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>(g / G) * num_heads + g % G : seq_row0 + g;
+      // row row0 + g = (query (row0 + g) / G, head (row0 + g) % G) of the group
+      const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>((row0 + g) / G) * num_heads + (row0 + g) % G
+                                  : seq_row0 + g;
       const float inv = L > 0.f ? vs / L : 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, orow * D + lane + 32 * e, o[e][g] * inv);
@@ -362,17 +398,24 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   const int bpu_shift = unit_in_block ? 0 : Tr::UR_SHIFT - p.block_shift;  // log2(blocks per unit)
   const bool fixed = p.partition_units > 0;
 
-  const int NS = p.stages;  // pipeline depth per consumer
+  const int NS = p.stages;  // pipeline depth per ring
   // fused append (AP): stages also carry the new K/V rows
   constexpr bool append = AP != 0;
-  constexpr int STG = append ? Tr::STAGE_APPEND : Tr::STAGE;
+  // Several queries per sequence (16-row variants): the R = q_len * G rows of
+  // a segment are served by NC = ceil(R / 16) consumer warps that share one
+  // ring, warp k of the ring taking rows 16k .. 16k + 15 of every unit; the
+  // stage's query area holds all 16 * NC rows.  Otherwise one warp per ring.
+  constexpr bool kMQ = GM > 8;
+  const int NC = kMQ ? p.row_groups : 1;
+  const int RW = W / NC;  // rings per CTA, each fed by producer lane 0 .. RW-1
+  const int STG = kMQ ? p.stage_bytes : (append ? Tr::STAGE_APPEND : Tr::STAGE);
   const int wsm = Tr::warp_smem(NS, STG);
   // shared: prefix[S+1] (units before sequence s), lens[S] (clamped seq_lens),
-  // scan scratch, then the producer's block-table ring (16 ints per consumer)
-  int* prefix = reinterpret_cast<int*>(base + W * wsm);
+  // scan scratch, then the producer's block-table ring (16 ints per ring)
+  int* prefix = reinterpret_cast<int*>(base + RW * wsm);
   int* lens = prefix + (S + 1);
   int* scan_tmp = lens + S;
-  const uint32_t table_ring_u32 = base_u32 + W * wsm + align_up_c((2 * S + 1 + NWARP) * 4, 16);
+  const uint32_t table_ring_u32 = base_u32 + RW * wsm + align_up_c((2 * S + 1 + NWARP) * 4, 16);
 
   // A kernel launched after this one with programmatic serialization (the
   // next step's cache write) may be scheduled now; it waits for this grid
@@ -406,7 +449,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         const int T = clamped_len(p, s, blockIdx.x == 0);
         lens[s] = T;
         const int nu = ((T + UR - 1) >> Tr::UR_SHIFT) - (window_lo(p, T) >> Tr::UR_SHIFT);
-        units = (fixed ? (nu + p.partition_units - 1) / p.partition_units : nu) * Hkv;
+        // fixed: partitions; balanced: cost positions (units + fragment overhead)
+        units = (fixed ? (nu + p.partition_units - 1) / p.partition_units : (nu > 0 ? nu + p.frag_cost : 0)) * Hkv;
       }
       int x = units;
 #pragma unroll
@@ -429,13 +473,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     if (threadIdx.x == 0) prefix[S] = carry;
   }
 
-  // ---- 2. barriers of every consumer ring
+  // ---- 2. barriers of every ring: a stage is full once its copies land and
+  // empty once each of the ring's NC consumer warps has released it
   if (threadIdx.x == 0) {
-    for (int c = 0; c < W; ++c) {
+    for (int c = 0; c < RW; ++c) {
       const uint32_t cb = base_u32 + c * wsm;
       for (int i = 0; i < NS; ++i) {
         mbar_init(cb + Tr::OFF_FULL + 8 * i, 1);
-        mbar_init(cb + Tr::OFF_EMPTY + 8 * i, 1);
+        mbar_init(cb + Tr::OFF_EMPTY + 8 * i, NC);
       }
     }
     fence_mbar_init();
@@ -443,10 +488,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   }
   __syncthreads();
 
-  // ---- 3. the share of consumer c (global consumer id gc)
-  const int nw_total = gridDim.x * W;
-  const long long U = prefix[S];
-  long long want = (U + kMinUnitsPerWarp - 1) / kMinUnitsPerWarp;
+  // ---- 3. the share of ring c (global ring id gc)
+  const int nw_total = gridDim.x * RW;
+  const long long U = prefix[S];  // partitions (fixed) or cost positions (balanced) of the batch
+  const int min_share = kMinUnitsPerWarp + (fixed ? 0 : p.frag_cost);
+  long long want = (U + min_share - 1) / min_share;
   const int nw_eff = fixed ? nw_total : static_cast<int>(want < 1 ? 1 : (want < nw_total ? want : nw_total));
   auto start_iter = [&](WorkIter& w, int gc) {
     w.frag_idx = 0;
@@ -460,7 +506,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     } else if (U > 0 && gc < nw_eff) {
       w.u = gc * U / nw_eff;
       w.u1 = (gc + 1) * U / nw_eff;
-      if (w.u < w.u1) { w.valid = true; frag_balanced(w, prefix, p, Tr::UR_SHIFT); }
+      w.valid = frag_balanced(w, prefix, p, Tr::UR_SHIFT);
     }
   };
 
@@ -472,10 +518,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     // unit is issued, so that a table read never stalls the warp.
     WorkIter it, ah;  // next unit to issue; next unit whose table entries to fetch
     it.valid = false;
-    if (lane < W) start_iter(it, blockIdx.x * W + lane);
+    if (lane < RW) start_iter(it, blockIdx.x * RW + lane);
     ah = it;
-    const uint32_t cbase = base_u32 + (lane < W ? lane : 0) * wsm;
-    const uint32_t ring = table_ring_u32 + (lane < W ? lane : 0) * 64;  // 4 units x 4 entries
+    const uint32_t cbase = base_u32 + (lane < RW ? lane : 0) * wsm;
+    const uint32_t ring = table_ring_u32 + (lane < RW ? lane : 0) * 64;  // 4 units x 4 entries
     int pst = 0, pph = 1, issued = 0;
     int pf = 0, rs_use = 0, rs_pf = 0;  // units fetched ahead; ring slots to read / fill
     uint64_t wait_since = 0;
@@ -605,7 +651,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     // ring to complete, with the full limit (a copy lands within
     // microseconds; only a broken copy engine would exhaust it).
     cp_async_wait<0>();
-    if (lane < W) {
+    if (lane < RW) {
       for (int i = 0; i < NS; ++i) {
         const int n_i = issued / NS + (i < issued % NS ? 1 : 0);  // phases started on stage i
         if (n_i > 0 && !mbar_wait_bounded(cbase + Tr::OFF_FULL + 8 * i, (n_i - 1) & 1, kDefaultWaitLimitNs))
@@ -618,15 +664,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // ===================================================================== consumer
   constexpr bool MB = Tr::MMA_BF16;
   const int c = warp - 1;
+  const int ring_id = c / NC;  // the ring this warp consumes
+  const int rg = c - ring_id * NC;  // its 16-row group of the segment's rows (several queries)
+  if (ring_id >= RW) return;
   WorkIter it;
-  start_iter(it, blockIdx.x * W + c);
+  start_iter(it, blockIdx.x * RW + ring_id);
   if (!it.valid) return;
   // Under a programmatic dependent launch this CTA may be resident long
   // before the kernel before it has finished; the bounded waits below start
   // counting only after it has (at once otherwise).
   griddep_wait();
-  const uint8_t* wbase = base + c * wsm;
-  const uint32_t wbase_u32 = base_u32 + c * wsm;
+  const uint8_t* wbase = base + ring_id * wsm;
+  const uint32_t wbase_u32 = base_u32 + ring_id * wsm;
   int cst = 0, cpar = 0;
   const int gid = lane >> 2;  // fragment row group: query head of S^T, column of O^T
   const int tig = lane & 3;
@@ -683,7 +732,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   constexpr int NH = GM > 8 ? 2 : 1;
   constexpr bool MQ = GM > 8;
   const int QL = MQ ? p.q_len : 1;
-  const int R = QL * G;
+  const int R = QL * G;                          // rows of the segment
+  const int row0 = MQ ? 16 * rg : 0;             // this warp's first row of them
+  const int Rw = MQ ? min(16, R - row0) : R;     // and how many it owns
   uint32_t qa0[Tr::KS], qa1[Tr::KS];  // A operand, row g (zero when g >= R)
   uint32_t qb0[Tr::KS], qb1[Tr::KS];  // A operand, row g + 8 (NH == 2)
   float m[NH], l[NH];                 // running max / sum of rows g, g + 8 (log2 domain)
@@ -945,20 +996,25 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     ms.nw_eff = nw_eff;
     ms.seg_start = prefix[s] + static_cast<long long>(kvh) * per;
     ms.first_w = 0;
+    ms.nc = NC;
+    ms.rg = rg;
     int nfr = per;
     if (!fixed) {
-      const long long seg_last = ms.seg_start + per - 1;
-      ms.first_w = static_cast<int>(((ms.seg_start + 1) * nw_eff - 1) / U);
-      nfr = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U) - ms.first_w + 1;
+      // rings holding the segment's first and last units (positions seg_start + frag_cost, seg_start + per - 1)
+      ms.first_w = ring_of(ms.seg_start + p.frag_cost, U, nw_eff);
+      nfr = ring_of(ms.seg_start + per - 1, U, nw_eff) - ms.first_w + 1;
     }
     float vs = 1.f;
     if constexpr (k8bit) vs = __ldg(p.v_scale + kvh);
     const int64_t seq_row0 = static_cast<int64_t>(s) * QL * p.num_heads + static_cast<int64_t>(kvh) * G;
-    // this warp's stages are idle after its unit loop: the records are staged there
-    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, R, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
-                                  wbase_u32 + Tr::OFF_STAGES,
-                                  reinterpret_cast<const float*>(wbase + Tr::OFF_STAGES), (NS * STG) / (Tr::REC * 4));
-    if (lane == 0) p.seg_counters[x] = 0;
+    // the ring's stages are idle after the unit loop (every warp of the ring
+    // has passed the ring barrier): warp rg stages its records in its share
+    const int share = (NS * STG) / NC / (Tr::REC * 4) * (Tr::REC * 4);
+    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, Rw, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
+                                  row0, wbase_u32 + Tr::OFF_STAGES + rg * share,
+                                  reinterpret_cast<const float*>(wbase + Tr::OFF_STAGES + rg * share),
+                                  share / (Tr::REC * 4));
+    if (lane == 0) p.seg_counters[x * NC + rg] = 0;
   };
 
   while (it.valid) {
@@ -982,8 +1038,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * STG + 2 * Tr::TILE;
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        const int row = gid + 8 * h;
-        const bool row_ok = row < R;
+        const int row = gid + 8 * h;  // local row of the A operand
+        const bool row_ok = row < Rw;
 #pragma unroll
         for (int s = 0; s < Tr::KS; ++s) {
           // columns of k-step s held by this lane: (d, d+1) for a0/a1, (d2, d2+1) for a2/a3
@@ -991,8 +1047,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const int d2 = k8bit ? d + 2 : d + 8;
           uint32_t w0 = 0u, w1 = 0u;
           if (row_ok) {
-            w0 = *reinterpret_cast<const uint32_t*>(qr + (row * D + d) * 2);
-            w1 = *reinterpret_cast<const uint32_t*>(qr + (row * D + d2) * 2);
+            w0 = *reinterpret_cast<const uint32_t*>(qr + ((row0 + row) * D + d) * 2);
+            w1 = *reinterpret_cast<const uint32_t*>(qr + ((row0 + row) * D + d2) * 2);
           }
           if (h == 0) {
             qa0[s] = w0;
@@ -1005,7 +1061,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         // query i = row / G sits at position T - q_len + i and sees positions up to
         // it (and, under a window, the last `window` of them); padding rows see all
         if constexpr (MQ) {
-          const int qi = row < R ? row / G : QL - 1;
+          const int qi = row < Rw ? (row0 + row) / G : QL - 1;
           hi_abs[h] = it.T - QL + qi;
           lo_abs[h] = p.window > 0 ? hi_abs[h] - p.window + 1 : 0;
         }
@@ -1109,7 +1165,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       const int64_t seq_row0 = static_cast<int64_t>(it.s) * QL * p.num_heads + static_cast<int64_t>(it.kvh) * G;
       auto out_row = [&](int r) -> int64_t {
         if constexpr (!MQ) return seq_row0 + r;  // one query: row = head
-        return seq_row0 + static_cast<int64_t>(r / G) * p.num_heads + r % G;
+        return seq_row0 + static_cast<int64_t>((row0 + r) / G) * p.num_heads + (row0 + r) % G;
       };
       if (it.slot < 0) {
 #pragma unroll
@@ -1119,7 +1175,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const float l1 = __shfl_sync(0xffffffffu, lt[h], 8 * tig + 4);  // row r1
           const float i0 = l0 > 0.f ? vs / l0 : 0.f, i1 = l1 > 0.f ? vs / l1 : 0.f;  // a row that saw nothing: 0
           const int64_t o0 = out_row(r0) * D, o1 = out_row(r1) * D;
-          const bool w0 = r0 < R, w1 = r1 < R;
+          const bool w0 = r0 < Rw, w1 = r1 < Rw;
 #pragma unroll
           for (int i = 0; i < Tr::KS; ++i) {
 #pragma unroll
@@ -1131,7 +1187,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           }
         }
       } else {
-        float* rec = p.part_records + static_cast<int64_t>(it.slot) * Tr::REC;
+        float* rec = p.part_records + (static_cast<int64_t>(it.slot) * NC + rg) * Tr::REC;
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const int r0 = 8 * h + 2 * tig;
@@ -1159,13 +1215,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         if (fixed) {
           nfr = (prefix[it.s + 1] - prefix[it.s]) / Hkv;
         } else {
-          const long long seg_start = prefix[it.s] + static_cast<long long>(it.kvh) * it.nu;
-          const long long seg_last = seg_start + it.nu - 1;
-          nfr = static_cast<int>(((seg_last + 1) * nw_eff - 1) / U) - static_cast<int>(((seg_start + 1) * nw_eff - 1) / U) + 1;
+          const long long seg_start = prefix[it.s] + static_cast<long long>(it.kvh) * (it.nu + p.frag_cost);
+          nfr = ring_of(seg_start + p.frag_cost + it.nu - 1, U, nw_eff) - ring_of(seg_start + p.frag_cost, U, nw_eff) + 1;
         }
         settle();
         __syncwarp();  // every lane's record stores come before lane 0's release
-        if (lane == 0) arr_old = atom_add_release_gpu(p.seg_counters + it.s * Hkv + it.kvh, 1);
+        if (lane == 0) arr_old = atom_add_release_gpu(p.seg_counters + (it.s * Hkv + it.kvh) * NC + rg, 1);
         arr_x = it.s * Hkv + it.kvh;
         arr_nfr = nfr;
       }
@@ -1176,6 +1231,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
   // ---- the split merges this warp won
   settle();
+  // The ring's stages become merge staging space: every warp of a shared ring
+  // first waits until all of them have left the unit loop (named barrier
+  // 1 + ring, NC warps).  Each of them reaches it: a warp that stops early on
+  // a timeout stops releasing stages, so the others time out too.
+  if (MQ && NC > 1) named_barrier_sync(1 + ring_id, NC * 32);
   if (npend > 0) {
     // acquire: the other fragments' records, released by their arrivals.
     // Lane 0 observed those arrivals (its atomics' results); its fence, then
@@ -1195,17 +1255,21 @@ template <typename QT, typename KVT, int D, int GM, int UR, int AP>
 struct DecodeVariant {
   using Tr = DecodeTraits<QT, KVT, D, GM, UR>;
 
-  static size_t smem_bytes(int num_seqs, int warps, int stages, int stage) {
-    return 1024 + static_cast<size_t>(warps) * Tr::warp_smem(stages, stage) +
-           static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1) * 4, 16)) + static_cast<size_t>(warps) * 64;
+  static size_t smem_bytes(int num_seqs, int warps, int rings, int stages, int stage) {
+    return 1024 + static_cast<size_t>(rings) * Tr::warp_smem(stages, stage) +
+           static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1) * 4, 16)) + static_cast<size_t>(rings) * 64;
   }
 
-  // Launch geometry: pipeline depth (stages per consumer) and consumer warps
-  // per CTA (plus one producer warp).  Default depth keeps about
-  // kStageBytesPerWarp of K/V per consumer; the consumers per CTA maximise
-  // resident consumer warps per SM (ties: more per CTA, i.e. fewer producer
-  // warps).  PA_DECODE_STAGES / PA_DECODE_WARPS override both (tuning).
-  static bool geometry(int num_seqs, DecodeGeometry* g) {
+  // Launch geometry: pipeline depth (stages per ring) and consumer warps per
+  // CTA (plus one producer warp).  One warp per ring: the default depth keeps
+  // about kStageBytesPerWarp of K/V per consumer and the consumers per CTA
+  // maximise resident consumer warps per SM (ties: more per CTA, i.e. fewer
+  // producer warps).  Rings shared by nc warps (several queries per sequence,
+  // nc = ceil(q_len * G / 16)): the consumers per CTA are a multiple of nc and
+  // each choice takes the deepest ring that fits; the choice maximises the
+  // K/V stages in flight per SM (ties: more warps).  PA_DECODE_STAGES /
+  // PA_DECODE_WARPS override depth and warps (tuning).
+  static bool geometry(int num_seqs, int nc, DecodeGeometry* g) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     int sms = 0, optin = 0;
@@ -1215,28 +1279,49 @@ struct DecodeVariant {
     // allow every size the device allows, once: geometries of other batch
     // sizes are cached and launched later without touching the attribute
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess) return false;
-    const int stage = AP ? Tr::STAGE_APPEND : Tr::STAGE;
-    int ns = kStageBytesPerWarp / stage;
-    ns = ns < 2 ? 2 : (ns > Tr::MAX_NS ? Tr::MAX_NS : ns);
+    constexpr bool mq = GM > 8;
+    if (nc < 1 || (!mq && nc != 1) || nc > 4) return false;
+    // several queries: the stage's query area holds 16 * nc rows
+    const int stage = mq ? align_up_c(2 * Tr::TILE + 16 * nc * D * 2, 1024) : (AP ? Tr::STAGE_APPEND : Tr::STAGE);
     const int env_ns = tuning_override("PA_DECODE_STAGES");
-    if (env_ns >= 2 && env_ns <= Tr::MAX_NS) ns = env_ns;
     const int env_w = tuning_override("PA_DECODE_WARPS");
-    int best_w = 0, best_occ = 0, best_warps = 0;
-    for (int w = 1; w <= Tr::MAX_W; ++w) {
+    int best_w = 0, best_occ = 0, best_ns = 0;
+    long long best_score = 0;
+    for (int w = nc; w <= Tr::MAX_W; w += nc) {
       if (env_w > 0 && w != env_w) continue;
-      const size_t smem = smem_bytes(num_seqs, w, ns, stage);
-      if (smem > static_cast<size_t>(optin)) break;
+      const int rings = w / nc;
+      int ns;
+      if (env_ns >= 2 && env_ns <= Tr::MAX_NS) {
+        ns = env_ns;
+      } else if (!mq || nc == 1) {
+        ns = kStageBytesPerWarp / stage;
+        ns = ns < 2 ? 2 : (ns > Tr::MAX_NS ? Tr::MAX_NS : ns);
+      } else {
+        ns = Tr::MAX_NS;  // deepest ring that fits
+        while (ns > 2 && smem_bytes(num_seqs, w, rings, ns, stage) > static_cast<size_t>(optin)) --ns;
+      }
+      // the merges stage at least one record per warp in the ring's stages
+      if (static_cast<long long>(ns) * stage / nc < Tr::REC * 4) continue;
+      const size_t smem = smem_bytes(num_seqs, w, rings, ns, stage);
+      if (smem > static_cast<size_t>(optin)) continue;
       int occ = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (w + 1) * 32, smem) != cudaSuccess) return false;
-      if (occ * w >= best_warps && occ > 0) {
-        best_warps = occ * w;
+      if (occ <= 0) continue;
+      // one warp per ring: resident consumer warps; shared rings: K/V stages in flight
+      const long long score = (!mq || nc == 1) ? static_cast<long long>(occ) * w
+                                                : static_cast<long long>(occ) * rings * (ns - 1) * 16 + w;
+      if (score >= best_score) {
+        best_score = score;
         best_w = w;
         best_occ = occ;
+        best_ns = ns;
       }
     }
     if (best_w == 0) return false;
-    const size_t smem = smem_bytes(num_seqs, best_w, ns, stage);
+    const int ns = best_ns;
+    const size_t smem = smem_bytes(num_seqs, best_w, best_w / nc, ns, stage);
     g->warps_per_cta = best_w;
+    g->row_groups = nc;
     g->stage_bytes = stage;
     g->stages = ns;
     g->ctas = sms * best_occ;

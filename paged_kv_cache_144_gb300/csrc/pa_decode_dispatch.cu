@@ -49,7 +49,8 @@ template <> constexpr int dtype_code<i8_t>() { return PA_INT8; }
 namespace {
 bool compute_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
 #define PA_GEO(QT, KVT, D, GM, UR, AP) \
-  if (PA_MATCH(QT, KVT, D, GM, UR, AP)) return decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(num_seqs, geo);
+  if (PA_MATCH(QT, KVT, D, GM, UR, AP))                                                                            \
+    return decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(num_seqs, key.row_groups, geo);
   PA_DECODE_VARIANTS(PA_GEO)
 #undef PA_GEO
   return false;
@@ -67,7 +68,8 @@ bool decode_geometry(const DecodeKey& key, int num_seqs, DecodeGeometry* geo) {
                      (static_cast<uint64_t>(key.kv_dtype & 0xf) << 48) |
                      (static_cast<uint64_t>(key.head_dim & 0xfff) << 36) |
                      (static_cast<uint64_t>(key.gmax & 0xf) << 32) | (static_cast<uint64_t>(key.unit_rows & 0xff) << 24) |
-                     (static_cast<uint64_t>(key.append & 1) << 23) | static_cast<uint64_t>(num_seqs & 0x7fffff);
+                     (static_cast<uint64_t>(key.append & 1) << 23) | (static_cast<uint64_t>(key.row_groups & 7) << 20) |
+                     static_cast<uint64_t>(num_seqs & 0xfffff);
   static std::mutex mu;
   static std::unordered_map<uint64_t, DecodeGeometry> cache;
   {

@@ -37,7 +37,7 @@
   X(f16_t, i8_t, 128, 4, 16, 0) X(f16_t, i8_t, 128, 4, 32, 0) X(f16_t, i8_t, 128, 4, 64, 0) \
   X(f16_t, i8_t, 128, 8, 16, 0) X(f16_t, i8_t, 128, 8, 32, 0) X(f16_t, i8_t, 128, 8, 64, 0)
 
-// 16 A rows: several queries per sequence (q_len * G <= 16)
+// 16 A rows per warp: several queries per sequence (q_len * G <= 64, 16 rows per warp of a ring)
 #define PA_DECODE_VARIANTS_ROWS16(X) \
   X(f16_t, f16_t, 64, 16, 16, 0) X(f16_t, f16_t, 64, 16, 32, 0) X(f16_t, f16_t, 128, 16, 16, 0) \
   X(f16_t, f16_t, 128, 16, 32, 0) X(bf16_t, bf16_t, 64, 16, 16, 0) X(bf16_t, bf16_t, 64, 16, 32, 0) \
@@ -71,15 +71,15 @@
 // dispatcher sees only the declarations, so every kernel is instantiated and
 // registered in exactly one translation unit.
 #define PA_DECLARE_VARIANT(QT, KVT, D, GM, UR, AP)                                                 \
-  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(int num_seqs, DecodeGeometry* geo); \
+  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(int num_seqs, int nc, DecodeGeometry* geo); \
   cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(const DecodeGeometry& geo,    \
                                                               const DecodeParams& p,              \
                                                               const CUtensorMap& tk,              \
                                                               const CUtensorMap& tv, cudaStream_t stream, \
                                                               bool pdl);
 #define PA_DEFINE_VARIANT(QT, KVT, D, GM, UR, AP)                                                  \
-  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(int num_seqs, DecodeGeometry* geo) { \
-    return DecodeVariant<QT, KVT, D, GM, UR, AP>::geometry(num_seqs, geo);                         \
+  bool decode_geometry_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(int num_seqs, int nc, DecodeGeometry* geo) { \
+    return DecodeVariant<QT, KVT, D, GM, UR, AP>::geometry(num_seqs, nc, geo);                     \
   }                                                                                                \
   cudaError_t decode_launch_##QT##_##KVT##_##D##_##GM##_##UR##_##AP(const DecodeGeometry& geo,    \
                                                               const DecodeParams& p,              \

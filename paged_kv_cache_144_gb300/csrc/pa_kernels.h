@@ -70,6 +70,7 @@ struct DecodeParams {
   int block_size;               // tokens per cache block (a power of two >= 8)
   int block_shift;              // log2(block_size)
   int partition_units;          // 0: balanced split; >0: fixed partitions of this many units
+  int frag_cost;                // balanced split: cost of a fragment besides its units, in units
   int window;                   // > 0: attend to the last `window` positions only; 0: all
   int q_len;                    // queries per sequence (their positions are the q_len newest)
   // fused append (k_new == nullptr: off): the rows of position seq_len-1
@@ -87,6 +88,8 @@ struct DecodeParams {
   int pending_cap;
   unsigned int* err;            // per-device error word
   int stages;                   // K/V pipeline stages per warp
+  int row_groups;               // consumer warps per ring (16-row variants: ceil(q_len * G / 16)); else 1
+  int stage_bytes;              // bytes of one pipeline stage (the 16-row variants' query area varies)
   uint64_t wait_limit_ns;       // limit of every wait on a pipeline barrier (PA_DEVERR_TIMEOUT after it)
   int withhold_copies;          // testing hook: the producer issues no copy, so every consumer wait runs out
 };
@@ -99,6 +102,7 @@ struct DecodeKey {
   int gmax;       // 1 / 4 / 8 (query heads per KV head, rounded up)
   int unit_rows;  // 16 / 32 / 64 rows per work unit
   int append;     // 1: fused append (each stage also stages the new K/V rows)
+  int row_groups; // consumer warps sharing a ring (1; up to 4 for the 16-row variants)
 };
 
 // Launch geometry of one variant on the current device.
@@ -110,6 +114,7 @@ struct DecodeGeometry {
   int record_floats;   // floats per partial record
   int stage_bytes;     // bytes of one pipeline stage
   int unit_rows;       // rows per work unit (TMA box height = min(unit_rows, block_size))
+  int row_groups;      // consumer warps per ring
 };
 
 // Fills `geo` for `key` and `num_seqs` on the current device; false if the

@@ -2,9 +2,10 @@
 
 Query i of a sequence of length T sits at position T-L+i and attends to the
 positions up to its own (oracle.paged_multi_query_attention).  Shapes cover
-L * G from 2 to 16 A rows (so both the 8-row and the 16-row variants),
-16-bit and 8-bit caches, windows, both split modes and sequences shorter
-than their query count.
+L * G from 2 to 64 (query, head) rows: up to 16 rows one consumer warp per
+ring, beyond that 2, 3 or 4 warps sharing each ring, 16 rows each; 16-bit and
+8-bit caches, windows, both split modes and sequences shorter than their
+query count.
 """
 
 import numpy as np
@@ -74,7 +75,46 @@ def test_multi_query_sequences_shorter_than_query_count():
     _check(b, workloads.host_values(b, seed=65, q_len=4))
 
 
+@pytest.mark.parametrize("L", [3, 4, 6, 8])
+@pytest.mark.parametrize("mode", [0, 256])
+def test_multi_query_group8_shared_rings(L, mode):
+    """G = 8: 24, 32, 48 and 64 rows (2, 2, 3 and 4 warps per ring), logits x30 for the longest."""
+    b = workloads.make_batch("long_32k", seed=67, num_seqs=3, lengths=("uniform", 1, 1400))
+    _check(b, workloads.host_values(b, seed=67, q_len=L, q_mult=30.0 if L == 8 else 1.0), partition_size=mode)
+
+
+@pytest.mark.parametrize("L", [5, 8, 16])
+def test_multi_query_gqa4_shared_rings(L):
+    b = workloads.make_batch("gqa_32x4k", seed=68, num_seqs=6, lengths=("uniform", 1, 900))
+    _check(b, workloads.host_values(b, seed=68, q_len=L))
+
+
+@pytest.mark.parametrize("L", [17, 40, 64])
+def test_multi_query_mha_shared_rings(L):
+    b = workloads.make_batch("tiny", seed=69, num_seqs=5, lengths=("uniform", 1, 200), pool=("slack", 0.1))
+    _check(b, workloads.host_values(b, seed=69, q_len=L))
+
+
+@pytest.mark.parametrize("kv", ["fp8_mix", "int8_mix"])
+@pytest.mark.parametrize("L", [8, 16])
+def test_multi_query_8bit_shared_rings(kv, L):
+    b = workloads.make_batch(kv, seed=70, num_seqs=6, lengths=("lognormal", 6.0, 1.0, 16, 1000))
+    _check(b, workloads.host_values(b, seed=70, q_len=L))
+
+
+@pytest.mark.parametrize("W", [1, 33])
+def test_multi_query_shared_rings_with_window(W):
+    b = workloads.make_batch("long_32k", seed=71, num_seqs=4, lengths=("uniform", 1, 600))
+    _check(b, workloads.host_values(b, seed=71, q_len=5), window=W)
+
+
+def test_multi_query_shared_rings_short_sequences():
+    """T < L with 4 warps per ring: queries at negative positions give 0."""
+    b = workloads.make_batch("long_32k", seed=72, num_seqs=5, lengths=("uniform", 1, 6))
+    _check(b, workloads.host_values(b, seed=72, q_len=8))
+
+
 def test_multi_query_rejects_too_many_rows():
     b = workloads.make_batch("gqa_32x4k", seed=66, num_seqs=2, lengths=("uniform", 5, 9))
     with pytest.raises(pa.PagedAttnError):
-        run_gpu(b, workloads.host_values(b, seed=66, q_len=5))   # 5 * G(4) = 20 rows > 16
+        run_gpu(b, workloads.host_values(b, seed=66, q_len=17))   # 17 * G(4) = 68 rows > 64

@@ -104,8 +104,8 @@ def test_decode_ex_options_validation(lib):
 
 
 def test_decode_ex_multi_query_validation(lib):
-    # 32 q heads / 8 KV heads: G = 4, so q_len 4 fills 16 A rows and q_len 5 is too many
-    assert _decode_ex(pa.DecodeOptions(q_len=5), q_stride=5 * 32 * 128) == pa.PA_ERR_UNSUPPORTED
+    # 32 q heads / 8 KV heads: G = 4, so q_len 16 fills 64 (query, head) rows and q_len 17 is too many
+    assert _decode_ex(pa.DecodeOptions(q_len=17), q_stride=17 * 32 * 128) == pa.PA_ERR_UNSUPPORTED
     assert _decode_ex(pa.DecodeOptions(q_len=4), q_stride=3 * 32 * 128) == pa.PA_ERR_SHAPE
     assert _decode_ex(pa.DecodeOptions(q_len=-1)) == pa.PA_ERR_SHAPE
     assert _decode_ex(pa.DecodeOptions(q_len=2, k_new=0x10000, v_new=0x20000, new_dtype=pa.PA_BF16,
