@@ -556,16 +556,29 @@ def run_ours(args):
         d_q, d_k, d_v, d_slots, d_tables, d_lens = views
         d2h = h_out.numel() * h_out.element_size()
 
-        def e2e_step(i):
+        def e2e_body(i, pdl=pdl):
+            st = torch.cuda.current_stream()
             d_stage.copy_(h_stage, non_blocking=True)
             if args.fused:
-                c.decode(pa, i, stream, window=args.window, pdl=pdl, fused=True, q=d_q, tables=d_tables, lens=d_lens,
+                c.decode(pa, i, st, window=args.window, pdl=pdl, fused=True, q=d_q, tables=d_tables, lens=d_lens,
                          k_new=d_k, v_new=d_v)
             else:
-                c.cache_write(pa, i, stream, pdl=pdl, k=d_k, v=d_v, slots=d_slots)
-                c.decode(pa, i, stream, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens)
+                c.cache_write(pa, i, st, pdl=pdl, k=d_k, v=d_v, slots=d_slots)
+                c.decode(pa, i, st, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens)
             h_out.copy_(c.out, non_blocking=True)
-            stream.synchronize()
+
+        if args.e2e_eager:
+            def e2e_step(i):
+                e2e_body(i)
+                stream.synchronize()
+        else:
+            # the step as a serving loop with fixed buffers issues it: one CUDA graph per KV pool replica,
+            # recorded through the same library calls (pa.StepGraph), replayed once per step
+            graphs = [pa.StepGraph(lambda r=r: e2e_body(r)) for r in range(c.replicas)]
+
+            def e2e_step(i):
+                graphs[i % c.replicas].replay()
+                stream.synchronize()
 
         for i in range(args.warmup):
             e2e_step(i)
@@ -659,7 +672,11 @@ def run_ours(args):
         e2e_ms, h2d, d2h, e2e_times = e2e
         line["e2e"] = {"value": round(total_step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": round(e2e_ms, 6), "repeats": spread(e2e_times, K)}
+                       "ms_per_step": round(e2e_ms, 6), "repeats": spread(e2e_times, K),
+                       "how": ("each step issued call by call through the Python binding" if args.e2e_eager else
+                               "each step replays a CUDA graph recorded through the library's calls (pa.StepGraph): "
+                               "pinned host staging buffer -> device, cache write, decode, output -> pinned host") +
+                              ", then a host synchronisation; host wall clock over the steps"}
     print(json.dumps(line), flush=True)
     if args.json_out:
         with open(args.json_out, "w") as f:
@@ -924,6 +941,8 @@ def main():
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch the step's decode as an ordinary launch (no programmatic dependent launch)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-eager", action="store_true",
+                    help="end-to-end steps issued call by call instead of replaying a recorded CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--json-out", default=None)

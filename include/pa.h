@@ -33,7 +33,7 @@
  *    "PagedAttentionのメモリ管理": the block table maps logical blocks to
  *    physical blocks of B tokens).
  *  - Supported shapes: head_dim in {64, 128} for 16-bit caches, 128 for the
- *    8-bit (FP8, INT8) caches; block_size a power of two from 8 to 1024 (16
+ *    8-bit (FP8, INT8) caches, which also take at most 256 KV heads; block_size a power of two from 8 to 1024 (16
  *    and 32 are the usual sizes); num_heads = G * num_kv_heads with
  *    1 <= G <= 8; with q_len queries per sequence (pa_decode_ex),
  *    q_len * G <= 64.

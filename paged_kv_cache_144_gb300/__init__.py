@@ -19,3 +19,4 @@ from ._lib import (  # noqa: F401
     dtype_code,
 )
 from .block_manager import BlockManager  # noqa: F401
+from .step_graph import StepGraph  # noqa: F401

@@ -297,6 +297,12 @@ __device__ __forceinline__ int atom_add_release_gpu(int* addr, int v) {
 // release operations, this thread's later reads see what they released.
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Orders this thread's generic-proxy view of global memory before its later
+// async-proxy operations (bulk copies that read global memory).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void st_shared_s32(uint32_t addr, int v) {
   asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

@@ -110,8 +110,9 @@ struct DecodeTraits {
   // per-consumer shared memory: [full[MAX_NS] | empty[MAX_NS] | NS stages]
   static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + MAX_NS * 8;
+  static constexpr int OFF_MERGE = OFF_EMPTY + MAX_NS * 8;  // one barrier per warp of the ring: its merge copies
   static constexpr int OFF_STAGES = 1024;
-  static_assert(OFF_EMPTY + MAX_NS * 8 <= OFF_STAGES, "barriers");
+  static_assert(OFF_MERGE + 4 * 8 <= OFF_STAGES, "barriers");
   __host__ __device__ static constexpr int warp_smem(int ns, int stage) { return OFF_STAGES + ns * stage; }
   // partial record: acc as [D][GM] (head fastest), then m[GM], l[GM]
   static constexpr int REC = align_up_c(GM * (D + 2), 4);
@@ -276,8 +277,9 @@ struct MergeSlots {
 // online-softmax recurrence and writes the output rows of its R (query, head)
 // rows row0 .. row0 + R - 1 (of the segment's q_len * G rows).  Run by the warp that arrived last, after its unit
 // loop, when its own pipeline stages are idle: the records are copied into
-// those stages (buf / bufp, room for cap records) a batch at a time with
-// cp.async, every copy of a batch in flight at once, and folded from shared
+// those stages (buf / bufp, room for cap records) a batch at a time, lane k
+// issuing one bulk copy of record k, all completing on the warp's merge
+// barrier `mbar` (phase parity tracked in `mpar`), and folded from shared
 // memory.  Lane k holds record k's (m, l) of the batch and its weights
 // e^(m_k - M); a batch whose records raise the running maximum M rescales
 // what was folded before (the same recurrence across batches).  Lane i owns
@@ -287,9 +289,8 @@ template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
                                               int G, int num_heads, float vs, void* out, int out_dtype,
                                               int64_t seq_row0, int row0, uint32_t buf, const float* bufp,
-                                              int cap) {
+                                              int cap, uint32_t mbar, uint32_t& mpar, unsigned int* err) {
   constexpr int EPL = D / 32;       // columns per lane
-  constexpr int CH = REC / 4;       // 16-byte chunks of one record
   static_assert(REC % 4 == 0, "records are whole 16-byte chunks");
   cap = cap < 32 ? cap : 32;        // the records of a batch are held one per lane
   float M[GM], Lp[GM], o[EPL][GM];  // running max, this lane's share of the sum, accumulator
@@ -304,14 +305,13 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
   for (int f0 = 0; f0 < nfr; f0 += cap) {
     const int nb = min(cap, nfr - f0);
     const int my_slot = lane < nb ? ms.slot(f0 + lane) : 0;
-#pragma unroll 1
-    for (int k = 0; k < nb; ++k) {
-      const float* src = records + static_cast<int64_t>(__shfl_sync(0xffffffffu, my_slot, k)) * REC;
-      for (int ch = lane; ch < CH; ch += 32) cp_async16(buf + static_cast<uint32_t>(k * REC + ch * 4) * 4, src + ch * 4);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncwarp();  // every lane's copies have landed
+    if (lane == 0) mbar_arrive_expect_tx(mbar, static_cast<uint32_t>(nb * REC * 4));
+    __syncwarp();
+    if (lane < nb) bulk_load(buf + static_cast<uint32_t>(lane * REC) * 4, records + static_cast<int64_t>(my_slot) * REC,
+                             REC * 4, mbar);
+    if (!mbar_wait_bounded(mbar, mpar, kDefaultWaitLimitNs) && lane == 0) raise_error(err, PA_DEVERR_TIMEOUT);
+    mpar ^= 1;
+    __syncwarp();  // every lane sees the batch
     float wk[GM];  // lane k: weight of record k per row
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
@@ -415,7 +415,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   int* prefix = reinterpret_cast<int*>(base + RW * wsm);
   int* lens = prefix + (S + 1);
   int* scan_tmp = lens + S;
-  const uint32_t table_ring_u32 = base_u32 + RW * wsm + align_up_c((2 * S + 1 + NWARP) * 4, 16);
+  // 8-bit caches: the per-KV-head K scale, V scale and (INT8) zero-point
+  // constants, staged once per CTA so that no fragment waits on them
+  float* hp_ks = reinterpret_cast<float*>(scan_tmp + NWARP);
+  float* hp_vs = hp_ks + kMaxHeadParams;
+  uint32_t* hp_zk = reinterpret_cast<uint32_t*>(hp_vs + kMaxHeadParams);
+  uint32_t* hp_zv = hp_zk + kMaxHeadParams;
+  constexpr int kHeadWords = Tr::B8 ? 4 * kMaxHeadParams : 0;
+  const uint32_t table_ring_u32 = base_u32 + RW * wsm + align_up_c((2 * S + 1 + NWARP + kHeadWords) * 4, 16);
 
   // A kernel launched after this one with programmatic serialization (the
   // next step's cache write) may be scheduled now; it waits for this grid
@@ -482,6 +489,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         mbar_init(cb + Tr::OFF_FULL + 8 * i, 1);
         mbar_init(cb + Tr::OFF_EMPTY + 8 * i, NC);
       }
+      for (int k = 0; k < NC; ++k) mbar_init(cb + Tr::OFF_MERGE + 8 * k, 1);
     }
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -557,6 +565,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         const int64_t n = static_cast<int64_t>(p.q_len) * p.num_heads * D;
         for (int64_t i = 0; i < n; ++i) store_out(p.out, p.out_dtype, static_cast<int64_t>(s) * n + i, 0.f);
       }
+    }
+    // 8-bit caches: the per-head constants every consumer needs (read after
+    // the wait: they are inputs like q).  The warp barrier orders every lane's
+    // stores before each lane's first stage arrival, which the consumers
+    // acquire.
+    if constexpr (k8bit) {
+      for (int h = lane; h < Hkv; h += 32) {
+        hp_ks[h] = __ldg(p.k_scale + h);
+        hp_vs[h] = __ldg(p.v_scale + h);
+        if constexpr (std::is_same<KVT, i8_t>::value) {
+          const uint32_t zk = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.k_zero_point + h))));
+          const uint32_t zv = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.v_zero_point + h))));
+          hp_zk[h] = zk | (zk << 16);
+          hp_zv[h] = zv | (zv << 16);
+        }
+      }
+      __syncwarp();
     }
     if (p.withhold_copies) it.valid = false;  // testing hook: nothing is issued, every consumer wait runs out
     while (__any_sync(0xffffffffu, it.valid)) {
@@ -970,6 +995,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // loop costs the loop registers, and the arrival itself does not wait: its
   // atomic's result is looked at only at the next fragment end ("settle").
   int npend = 0;
+  uint32_t merge_par = 0;  // phase parity of this warp's merge barrier
   int* const pend = p.pending + static_cast<int64_t>(blockIdx.x * W + c) * p.pending_cap;
   int arr_old = 0, arr_x = -1, arr_nfr = 0;  // the arrival not settled yet (x < 0: none)
   auto settle = [&]() {
@@ -1005,7 +1031,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       nfr = ring_of(ms.seg_start + per - 1, U, nw_eff) - ms.first_w + 1;
     }
     float vs = 1.f;
-    if constexpr (k8bit) vs = __ldg(p.v_scale + kvh);
+    if constexpr (k8bit) vs = hp_vs[kvh];
     const int64_t seq_row0 = static_cast<int64_t>(s) * QL * p.num_heads + static_cast<int64_t>(kvh) * G;
     // the ring's stages are idle after the unit loop (every warp of the ring
     // has passed the ring barrier): warp rg stages its records in its share
@@ -1013,7 +1039,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, Rw, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
                                   row0, wbase_u32 + Tr::OFF_STAGES + rg * share,
                                   reinterpret_cast<const float*>(wbase + Tr::OFF_STAGES + rg * share),
-                                  share / (Tr::REC * 4));
+                                  share / (Tr::REC * 4), wbase_u32 + Tr::OFF_MERGE + 8 * rg, merge_par, p.err);
     if (lane == 0) p.seg_counters[x * NC + rg] = 0;
   };
 
@@ -1100,13 +1126,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
     }
     score_scale = p.qk_scale_log2;
-    if constexpr (k8bit) score_scale *= __ldg(p.k_scale + it.kvh);
+    if constexpr (k8bit) score_scale *= hp_ks[it.kvh];
     if constexpr (q_rescale) score_scale *= __int_as_float((127 - qexp) << 23);
     if constexpr (std::is_same<KVT, i8_t>::value) {
-      const uint32_t zk = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.k_zero_point + it.kvh))));
-      const uint32_t zv = __half_as_ushort(__float2half_rn(1152.f + static_cast<float>(__ldg(p.v_zero_point + it.kvh))));
-      zpk2 = zk | (zk << 16);
-      zpv2 = zv | (zv << 16);
+      zpk2 = hp_zk[it.kvh];
+      zpv2 = hp_zv[it.kvh];
     }
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
@@ -1160,7 +1184,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], 2);  // row gid + 8h's sum
       }
       float vs = 1.f;
-      if constexpr (k8bit) vs = __ldg(p.v_scale + it.kvh);
+      if constexpr (k8bit) vs = hp_vs[it.kvh];
       // output row of A row r: out[s][r / G][kvh * G + r % G]
       const int64_t seq_row0 = static_cast<int64_t>(it.s) * QL * p.num_heads + static_cast<int64_t>(it.kvh) * G;
       auto out_row = [&](int r) -> int64_t {
@@ -1244,6 +1268,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     // stall the unit loop.)
     fence_acq_rel_gpu();
     __syncwarp();
+    // the records are read by bulk copies (the async proxy): each lane orders
+    // them after its (acquired) view of global memory
+    fence_proxy_async_global();
     for (int i = 0; i < npend; ++i) merge_seg(pend[i]);
   }
 }
@@ -1256,8 +1283,10 @@ struct DecodeVariant {
   using Tr = DecodeTraits<QT, KVT, D, GM, UR>;
 
   static size_t smem_bytes(int num_seqs, int warps, int rings, int stages, int stage) {
+    constexpr int head_words = Tr::B8 ? 4 * kMaxHeadParams : 0;
     return 1024 + static_cast<size_t>(rings) * Tr::warp_smem(stages, stage) +
-           static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1) * 4, 16)) + static_cast<size_t>(rings) * 64;
+           static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1 + head_words) * 4, 16)) +
+           static_cast<size_t>(rings) * 64;
   }
 
   // Launch geometry: pipeline depth (stages per ring) and consumer warps per

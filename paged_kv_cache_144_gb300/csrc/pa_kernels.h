@@ -14,6 +14,10 @@ namespace pa {
 // copies in flight before it exits always uses this limit.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
+// 8-bit caches: KV heads whose dequantisation constants the decode stages in
+// shared memory (the most an 8-bit cache may have).
+constexpr int kMaxHeadParams = 256;
+
 // K/V TMA boxes are min(unit rows, block_size) whole rows; both are
 // multiples of this (one 128-byte-swizzle atom is 8 x 128 bytes).
 constexpr int kBoxRowQuantum = 8;
