@@ -346,6 +346,7 @@ def barrier(world_size: int):
 
 NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal bandwidth (~8 TB/s), the basis the ">= 70 %" target is stated on
 MIN_TIMED_S = 1.0          # every timed loop is repeated until its repeats cover at least this long
+MIN_TIME_S = [MIN_TIMED_S]  # as set by --min-time
 
 
 def lead_gpu(torch, us: float = 300.0):
@@ -355,9 +356,12 @@ def lead_gpu(torch, us: float = 300.0):
     torch.cuda._sleep(int(us * 2.2e3))  # cycles; at most 2.07 GHz here, so at least `us`
 
 
-def repeat_until(one, world: int, min_s: float = MIN_TIMED_S):
-    """Run one() (the milliseconds of one timed repeat) until the repeats cover min_s seconds.  The repeat
-    count is fixed after the first repeat and agreed across ranks (max), so every rank runs the same loops."""
+def repeat_until(one, world: int, min_s: float | None = None):
+    """Run one() (the milliseconds of one timed repeat) until the repeats cover min_s seconds (default: the
+    --min-time argument, else MIN_TIMED_S).  The repeat count is fixed after the first repeat and agreed across
+    ranks (max), so every rank runs the same loops."""
+    if min_s is None:
+        min_s = MIN_TIME_S[0]
     first = one()
     n = max(1, math.ceil(min_s * 1e3 / max(first, 1e-6)))
     n = int(max_over_ranks(float(min(n, 100000)), world))
@@ -631,7 +635,7 @@ def run_ours(args):
                       else ", both launched with programmatic dependent launch") if pdl else ""),
             "timing": f"value: repeats of exactly K={K} steps back to back (so each step's launches overlap the one "
                       f"before through programmatic dependent launch), CUDA events on the stream, barrier + "
-                      f"synchronize around each repeat, repeated until >= {MIN_TIMED_S:.0f} s, median repeat; "
+                      f"synchronize around each repeat, repeated until >= {MIN_TIME_S[0]:g} s, median repeat; "
                       "roofline: a second loop of decode launches alone (ordinary launches, no overlap), an event "
                       "pair around each launch, repeated the same way. The two loops differ in shape, so the "
                       "step can be shorter than the decode launch alone.",
@@ -945,8 +949,11 @@ def main():
                     help="end-to-end steps issued call by call instead of replaying a recorded CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--min-time", type=float, default=MIN_TIMED_S,
+                    help="repeat every timed loop until its repeats cover this many seconds (0: one repeat)")
     ap.add_argument("--json-out", default=None)
     args = ap.parse_args()
+    MIN_TIME_S[0] = args.min_time
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.q_len > 1 and args.fused:

@@ -278,6 +278,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held in the fragment layout
+// (lane (g, t) holds row g, elements 2t and 2t + 1): the result holds the
+// transposed matrix in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t r;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr) : "memory");

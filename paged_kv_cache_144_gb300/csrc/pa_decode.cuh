@@ -721,6 +721,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // (K) or m-tile s (V).  Matrices 0..3 = (rows 0-7, cols lo), (rows 0-7,
   // cols hi), (rows 8-15, cols lo), (rows 8-15, cols hi) of a 16x16 block.
   uint32_t moff[Tr::KS];
+  // single-query variants: K is the A operand of S = K Q^T (tokens as M);
+  // matrices 0..3 = (rows 0-7, cols lo), (rows 8-15, cols lo), (rows 0-7,
+  // cols hi), (rows 8-15, cols hi)
+  uint32_t moffA[Tr::KS];
   // 8-bit tiles: n-position j of an 8-token n-tile holds token j ^ 4(j & 1),
   // which keeps both the K and the V loads below free of bank conflicts.
   auto sigma = [](int j) { return j ^ ((j & 1) << 2); };
@@ -730,12 +734,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     const int lhi = (lane >> 3) & 1;
 #pragma unroll
     for (int s = 0; s < Tr::KS; ++s) moff[s] = chunk_off(lt, 2 * s + lhi);
-  } else {
-    // K: token sigma(gid) of each n-tile, chunks tig and 4 + tig (16 head_dim
-    // values each, consumed as 4 k-steps of 4 values).
-    const int sg = sigma(gid);
+    const int ltA = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int lhiA = lane >> 4;
 #pragma unroll
-    for (int g = 0; g < 2; ++g) kb8[g] = chunk_off(sg, 4 * g + tig);
+    for (int s = 0; s < Tr::KS; ++s) moffA[s] = chunk_off(ltA, 2 * s + lhiA);
+  } else {
+    if constexpr (GM > 8) {
+      // K as the B operand: token sigma(gid) of each n-tile, chunks tig and
+      // 4 + tig (16 head_dim values each, consumed as 4 k-steps of 4 values).
+      const int sg = sigma(gid);
+#pragma unroll
+      for (int g = 0; g < 2; ++g) kb8[g] = chunk_off(sg, 4 * g + tig);
+    } else {
+      // K as the A operand: m-row g of each 16-token m-tile holds token
+      // sigma(g) (row g + 8: 8 + sigma(g)); the lane reads chunks 2t and
+      // 2t + 1 of it, head_dim columns 32t .. 32t + 31, k-step s taking
+      // columns 32t + 4s .. 32t + 4s + 3 (the same order on the query side).
+      const int sg = sigma(gid);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) kb8[c] = chunk_off(sg, 2 * tig + c);
+    }
     // V: tokens sigma(2t), sigma(2t+1); 4 bytes at head_dim column 32 jj + 4 gid.
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -762,7 +780,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   const int Rw = MQ ? min(16, R - row0) : R;     // and how many it owns
   uint32_t qa0[Tr::KS], qa1[Tr::KS];  // A operand, row g (zero when g >= R)
   uint32_t qb0[Tr::KS], qb1[Tr::KS];  // A operand, row g + 8 (NH == 2)
-  float m[NH], l[NH];                 // running max / sum of rows g, g + 8 (log2 domain)
+  // softmax state rows of this lane: g and g + 8 (several queries), else
+  // 2t and 2t + 1 (the N columns of S = K Q^T)
+  constexpr int NR = MQ ? NH : 2;
+  float m[NR], l[NR];                 // running max / sum of those rows (log2 domain)
   float acc[Tr::KS][NH][4];           // O^T: rows = head_dim columns, cols = A rows 8h + 2t, 8h + 2t + 1
   int hi_abs[NH], lo_abs[NH];         // last / first position row g + 8h may see (MQ)
   float score_scale = p.qk_scale_log2;
@@ -773,103 +794,202 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   auto unit_step = [&](auto full_tag, uint32_t kt, int n_valid, int lo_rel, int j) {
     constexpr bool FULL = decltype(full_tag)::value;
     const uint32_t vt = kt + Tr::TILE;
-    float sc[Tr::NT][4];
+    // P^T as the B operand of each 16-token k-step of O^T += V^T P^T, split hi + lo
+    uint32_t ph[Tr::NSB][NH][2], pl[Tr::NSB][NH][2];
+    if constexpr (!MQ) {
+      // ---- scores S = K Q^T: tokens as M (16 per m-tile), the G <= 8 query
+      // rows as N.  Lane (g, t) holds the scores of m-rows g and g + 8 (tokens
+      // g, g + 8; 8-bit: sigma(g), 8 + sigma(g)) for rows 2t and 2t + 1.
+      constexpr int NMT = Tr::NSB;
+      float sc[NMT][4];
 #pragma unroll
-    for (int nt = 0; nt < Tr::NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-    // ---- scores
-    if constexpr (!k8bit) {
+      for (int mt = 0; mt < NMT; ++mt) sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+      if constexpr (!k8bit) {
 #pragma unroll
-      for (int sb = 0; sb < Tr::NSB; ++sb) {
+        for (int mt = 0; mt < NMT; ++mt) {
 #pragma unroll
-        for (int s = 0; s < Tr::KS; ++s) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + sb * sub_delta + moff[s], b0, b1, b2, b3);
-          const uint32_t a1 = NH == 2 ? qb0[s] : 0u, a3 = NH == 2 ? qb1[s] : 0u;
-          mma16816<MB>(sc[2 * sb], qa0[s], a1, qa1[s], a3, b0, b1);
-          mma16816<MB>(sc[2 * sb + 1], qa0[s], a1, qa1[s], a3, b2, b3);
+          for (int s = 0; s < Tr::KS; ++s) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kt + mt * sub_delta + moffA[s], a0, a1, a2, a3);
+            mma16816<MB>(sc[mt], a0, a1, a2, a3, qa0[s], qa1[s]);
+          }
         }
-      }
-    } else {
+      } else {
 #pragma unroll
-      for (int nt = 0; nt < Tr::NT; ++nt) {
+        for (int mt = 0; mt < NMT; ++mt) {
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint4 w = lds128(kt + nt * 1024 + kb8[g]);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          for (int c = 0; c < 2; ++c) {
+            const uint4 w0 = lds128(kt + mt * 2048 + kb8[c]);         // token sigma(g)
+            const uint4 w1 = lds128(kt + mt * 2048 + 1024 + kb8[c]);  // token 8 + sigma(g)
+            const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t x1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int s = 4 * g + r;
-            uint32_t b0, b1;
-            widen4<KVT>(ws[r], zpk2, b0, b1);
-            mma16816<false>(sc[nt], qa0[s], NH == 2 ? qb0[s] : 0u, qa1[s], NH == 2 ? qb1[s] : 0u, b0, b1);
+            for (int r = 0; r < 4; ++r) {
+              const int s = 4 * c + r;
+              uint32_t a0, a1, a2, a3;
+              widen4<KVT>(x0[r], zpk2, a0, a2);
+              widen4<KVT>(x1[r], zpk2, a1, a3);
+              mma16816<false>(sc[mt], a0, a1, a2, a3, qa0[s], qa1[s]);
+            }
           }
         }
       }
-    }
-    // ---- online softmax per row (the quad of lanes g*4 .. g*4+3 shares rows g, g+8)
-    float mx[NH];
+      // ---- online softmax: rows 2t (elements 0, 2) and 2t + 1 (1, 3), each
+      // reduced over the 8 lanes of equal t
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      mx[h] = -INFINITY;
-      int hr = 0, lr = 0;  // this row's bounds in the unit (several queries per sequence)
-      if constexpr (MQ) {
-        hr = hi_abs[h] - j * UR;
-        lr = lo_abs[h] - j * UR;
-      }
+      for (int mt = 0; mt < NMT; ++mt) {
 #pragma unroll
-      for (int nt = 0; nt < Tr::NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float x = sc[nt][2 * h + e] * score_scale;
+        for (int e = 0; e < 4; ++e) {
+          float x = sc[mt][e] * score_scale;
           if constexpr (!FULL) {
-            const int tok = nt * 8 + (k8bit ? sigma(2 * tig + e) : 2 * tig + e);
-            bool ok = tok < n_valid && tok >= lo_rel;
-            if constexpr (MQ) ok = ok && tok <= hr && tok >= lr;
-            x = ok ? x : -INFINITY;
+            const int tok = 16 * mt + 8 * (e >> 1) + (k8bit ? sigma(gid) : gid);
+            x = (tok < n_valid && tok >= lo_rel) ? x : -INFINITY;
           }
-          sc[nt][2 * h + e] = x;
-          mx[h] = fmaxf(mx[h], x);
+          sc[mt][e] = x;
+          if (e & 1) {
+            mx1 = fmaxf(mx1, x);
+          } else {
+            mx0 = fmaxf(mx0, x);
+          }
         }
       }
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-    }
-    bool up = mx[0] > m[0];
-    if constexpr (NH == 2) up |= mx[1] > m[1];
-    if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float mn = fmaxf(m[h], mx[h]);
-        // a row that has seen nothing yet keeps alpha = 1 (its state is still empty);
-        // single-query rows see a token in every unit they process
-        const float alpha = (MQ && mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
-        m[h] = mn;
-        l[h] *= alpha;
-        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);      // row 8h + 2t
-        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);  // row 8h + 2t + 1
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      // every row sees a token in every unit it processes: the new maxima are finite
+      if (__any_sync(0xffffffffu, mx0 > m[0] || mx1 > m[1])) {
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float a0 = fast_exp2(m[0] - mn0), a1 = fast_exp2(m[1] - mn1);
+        m[0] = mn0;
+        m[1] = mn1;
+        l[0] *= a0;
+        l[1] *= a1;
 #pragma unroll
         for (int i = 0; i < Tr::KS; ++i) {
-          acc[i][h][0] *= a0;
-          acc[i][h][1] *= a1;
-          acc[i][h][2] *= a0;
-          acc[i][h][3] *= a1;
+          acc[i][0][0] *= a0;
+          acc[i][0][1] *= a1;
+          acc[i][0][2] *= a0;
+          acc[i][0][3] *= a1;
         }
       }
-    }
-    // P^T as the B operand of each 16-token k-step, per row half, split hi + lo
-    uint32_t ph[Tr::NSB][NH][2], pl[Tr::NSB][NH][2];
+      // P, then its transposes: m-rows g (g + 8) of S become k-rows 2t, 2t + 1
+      // (2t + 8, 2t + 9) of P^T, the token order the V loads use
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const float ms = (MQ && m[h] == -INFINITY) ? 0.f : m[h];  // exp2(-inf - ms) = 0 for an empty row
+      for (int mt = 0; mt < NMT; ++mt) {
+        const float p0 = fast_exp2(sc[mt][0] - m[0]);
+        const float p1 = fast_exp2(sc[mt][1] - m[1]);
+        const float p2 = fast_exp2(sc[mt][2] - m[0]);
+        const float p3 = fast_exp2(sc[mt][3] - m[1]);
+        l[0] += p0 + p2;
+        l[1] += p1 + p3;
+        const uint32_t h01 = pack2<MB>(p0, p1), h23 = pack2<MB>(p2, p3);
+        const float2 f01 = unpack2<MB>(h01), f23 = unpack2<MB>(h23);
+        ph[mt][0][0] = movmatrix_trans(h01);
+        ph[mt][0][1] = movmatrix_trans(h23);
+        pl[mt][0][0] = movmatrix_trans(pack2<MB>(p0 - f01.x, p1 - f01.y));
+        pl[mt][0][1] = movmatrix_trans(pack2<MB>(p2 - f23.x, p3 - f23.y));
+      }
+    } else {
+      float sc[Tr::NT][4];
 #pragma unroll
-      for (int nt = 0; nt < Tr::NT; ++nt) {
-        const float p0 = fast_exp2(sc[nt][2 * h] - ms);
-        const float p1 = fast_exp2(sc[nt][2 * h + 1] - ms);
-        l[h] += p0 + p1;
-        const uint32_t hp = pack2<MB>(p0, p1);
-        const float2 hf = unpack2<MB>(hp);
-        ph[nt >> 1][h][nt & 1] = hp;
-        pl[nt >> 1][h][nt & 1] = pack2<MB>(p0 - hf.x, p1 - hf.y);
+      for (int nt = 0; nt < Tr::NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      // ---- scores
+      if constexpr (!k8bit) {
+#pragma unroll
+        for (int sb = 0; sb < Tr::NSB; ++sb) {
+#pragma unroll
+          for (int s = 0; s < Tr::KS; ++s) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + sb * sub_delta + moff[s], b0, b1, b2, b3);
+            const uint32_t a1 = NH == 2 ? qb0[s] : 0u, a3 = NH == 2 ? qb1[s] : 0u;
+            mma16816<MB>(sc[2 * sb], qa0[s], a1, qa1[s], a3, b0, b1);
+            mma16816<MB>(sc[2 * sb + 1], qa0[s], a1, qa1[s], a3, b2, b3);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < Tr::NT; ++nt) {
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const uint4 w = lds128(kt + nt * 1024 + kb8[g]);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int s = 4 * g + r;
+              uint32_t b0, b1;
+              widen4<KVT>(ws[r], zpk2, b0, b1);
+              mma16816<false>(sc[nt], qa0[s], NH == 2 ? qb0[s] : 0u, qa1[s], NH == 2 ? qb1[s] : 0u, b0, b1);
+            }
+          }
+        }
+      }
+      // ---- online softmax per row (the quad of lanes g*4 .. g*4+3 shares rows g, g+8)
+      float mx[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        mx[h] = -INFINITY;
+        int hr = 0, lr = 0;  // this row's bounds in the unit (several queries per sequence)
+        if constexpr (MQ) {
+          hr = hi_abs[h] - j * UR;
+          lr = lo_abs[h] - j * UR;
+        }
+#pragma unroll
+        for (int nt = 0; nt < Tr::NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x = sc[nt][2 * h + e] * score_scale;
+            if constexpr (!FULL) {
+              const int tok = nt * 8 + (k8bit ? sigma(2 * tig + e) : 2 * tig + e);
+              bool ok = tok < n_valid && tok >= lo_rel;
+              if constexpr (MQ) ok = ok && tok <= hr && tok >= lr;
+              x = ok ? x : -INFINITY;
+            }
+            sc[nt][2 * h + e] = x;
+            mx[h] = fmaxf(mx[h], x);
+          }
+        }
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+      }
+      bool up = mx[0] > m[0];
+      if constexpr (NH == 2) up |= mx[1] > m[1];
+      if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float mn = fmaxf(m[h], mx[h]);
+          // a row that has seen nothing yet keeps alpha = 1 (its state is still empty);
+          // single-query rows see a token in every unit they process
+          const float alpha = (MQ && mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
+          m[h] = mn;
+          l[h] *= alpha;
+          const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);      // row 8h + 2t
+          const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);  // row 8h + 2t + 1
+#pragma unroll
+          for (int i = 0; i < Tr::KS; ++i) {
+            acc[i][h][0] *= a0;
+            acc[i][h][1] *= a1;
+            acc[i][h][2] *= a0;
+            acc[i][h][3] *= a1;
+          }
+        }
+      }
+      // P^T as the B operand of each 16-token k-step, per row half, split hi + lo
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float ms = (MQ && m[h] == -INFINITY) ? 0.f : m[h];  // exp2(-inf - ms) = 0 for an empty row
+#pragma unroll
+        for (int nt = 0; nt < Tr::NT; ++nt) {
+          const float p0 = fast_exp2(sc[nt][2 * h] - ms);
+          const float p1 = fast_exp2(sc[nt][2 * h + 1] - ms);
+          l[h] += p0 + p1;
+          const uint32_t hp = pack2<MB>(p0, p1);
+          const float2 hf = unpack2<MB>(hp);
+          ph[nt >> 1][h][nt & 1] = hp;
+          pl[nt >> 1][h][nt & 1] = pack2<MB>(p0 - hf.x, p1 - hf.y);
+        }
       }
     }
     // rows past the end of the sequence, and rows before a sliding window,
@@ -1069,7 +1189,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
         for (int s = 0; s < Tr::KS; ++s) {
           // columns of k-step s held by this lane: (d, d+1) for a0/a1, (d2, d2+1) for a2/a3
-          const int d = k8bit ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 16 * s + 2 * tig;
+          const int d = k8bit ? (MQ ? 16 * (4 * (s >> 2) + tig) + 4 * (s & 3) : 32 * tig + 4 * s) : 16 * s + 2 * tig;
           const int d2 = k8bit ? d + 2 : d + 8;
           uint32_t w0 = 0u, w1 = 0u;
           if (row_ok) {
@@ -1133,9 +1253,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       zpv2 = hp_zv[it.kvh];
     }
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
+    for (int h = 0; h < NR; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
 #pragma unroll
       for (int i = 0; i < Tr::KS; ++i) acc[i][h][0] = acc[i][h][1] = acc[i][h][2] = acc[i][h][3] = 0.f;
     }
@@ -1177,11 +1300,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
     // ---- end of fragment: write the output or a partial record
     {
-      float lt[NH];
+      // sums of this lane's softmax rows: several queries: rows g, g + 8
+      // (over the quad); else rows 2t, 2t + 1 (over the 8 lanes of equal t)
+      float lt[NR];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        lt[h] = l[h] + __shfl_xor_sync(0xffffffffu, l[h], 1);
-        lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], 2);  // row gid + 8h's sum
+      for (int h = 0; h < NR; ++h) {
+        if constexpr (MQ) {
+          lt[h] = l[h] + __shfl_xor_sync(0xffffffffu, l[h], 1);
+          lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], 2);
+        } else {
+          lt[h] = l[h];
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], off);
+        }
       }
       float vs = 1.f;
       if constexpr (k8bit) vs = hp_vs[it.kvh];
@@ -1195,8 +1326,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const int r0 = 8 * h + 2 * tig, r1 = r0 + 1;
-          const float l0 = __shfl_sync(0xffffffffu, lt[h], 8 * tig);      // row r0
-          const float l1 = __shfl_sync(0xffffffffu, lt[h], 8 * tig + 4);  // row r1
+          float l0, l1;  // sums of rows r0, r1
+          if constexpr (MQ) {
+            l0 = __shfl_sync(0xffffffffu, lt[h], 8 * tig);
+            l1 = __shfl_sync(0xffffffffu, lt[h], 8 * tig + 4);
+          } else {
+            l0 = lt[0];
+            l1 = lt[1];
+          }
           const float i0 = l0 > 0.f ? vs / l0 : 0.f, i1 = l1 > 0.f ? vs / l1 : 0.f;  // a row that saw nothing: 0
           const int64_t o0 = out_row(r0) * D, o1 = out_row(r1) * D;
           const bool w0 = r0 < Rw, w1 = r1 < Rw;
@@ -1228,10 +1365,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
               }
             }
           }
-          const int row = gid + 8 * h;
-          if (tig == 0 && row < GM) {
-            rec[GM * D + row] = m[h];
-            rec[GM * D + GM + row] = lt[h];
+          if constexpr (MQ) {
+            const int row = gid + 8 * h;
+            if (tig == 0 && row < GM) {
+              rec[GM * D + row] = m[h];
+              rec[GM * D + GM + row] = lt[h];
+            }
+          }
+        }
+        if constexpr (!MQ) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int row = 2 * tig + e;
+            if (gid == 0 && row < GM) {
+              rec[GM * D + row] = m[e];
+              rec[GM * D + GM + row] = lt[e];
+            }
           }
         }
         // fragments of this segment
