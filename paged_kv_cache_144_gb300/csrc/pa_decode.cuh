@@ -181,12 +181,16 @@ __device__ __forceinline__ int window_lo(const DecodeParams& p, int T) {
 // segment (its H_kv segments are consecutive, each of the same cost).
 //
 // Fills the fragment starting at it.u (the first of its units at or after
-// it.u); returns false when the ring's range holds no further unit.
+// it.u); returns false when the ring's range holds no further unit.  it.s is
+// a sequence with prefix[it.s] <= it.u (the ring's positions only grow): the
+// sequence of it.u is found by scanning forward from it, one or two
+// shared-memory reads per fragment, not a search over the whole batch.
 __device__ __forceinline__ bool frag_balanced(WorkIter& it, const int* prefix, const DecodeParams& p, int ur_shift) {
   const int Hkv = p.num_kv_heads;
   const int beta = p.frag_cost;
+  int s = it.s;
   while (it.u < it.u1) {
-    const int s = find_seq(prefix, p.num_seqs, it.u);
+    while (s + 1 < p.num_seqs && prefix[s + 1] <= it.u) ++s;  // last s with prefix[s] <= u
     const int seg = (prefix[s + 1] - prefix[s]) / Hkv;  // frag_cost + nu of each segment of sequence s
     const int r = static_cast<int>(it.u - prefix[s]);  // < 2^31: positions are int32
     const int kvh = r / seg;
@@ -514,6 +518,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     } else if (U > 0 && gc < nw_eff) {
       w.u = gc * U / nw_eff;
       w.u1 = (gc + 1) * U / nw_eff;
+      w.s = find_seq(prefix, S, w.u);
       w.valid = frag_balanced(w, prefix, p, Tr::UR_SHIFT);
     }
   };
