@@ -408,6 +408,31 @@ __device__ __forceinline__ void store_out(void* out, int dtype, int64_t i, float
   }
 }
 
+// Four consecutive outputs from element i (a multiple of 4); one 16-byte (F32)
+// or 8-byte (F16/BF16) store when `aligned` (the buffer is 16-byte aligned).
+__device__ __forceinline__ void store_out4(void* out, int dtype, int64_t i, float4 v, bool aligned) {
+  if (!aligned) {
+    store_out(out, dtype, i, v.x);
+    store_out(out, dtype, i + 1, v.y);
+    store_out(out, dtype, i + 2, v.z);
+    store_out(out, dtype, i + 3, v.w);
+  } else if (dtype == PA_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + i) = v;
+  } else if (dtype == PA_F16) {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&a);
+    w.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(out) + i) = w;
+  } else {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&a);
+    w.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + i) = w;
+  }
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 r;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

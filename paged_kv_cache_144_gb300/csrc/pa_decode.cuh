@@ -279,32 +279,35 @@ struct MergeSlots {
 
 // Merges the nfr partial (m, l, acc) records of one segment with the
 // online-softmax recurrence and writes the output rows of its R (query, head)
-// rows row0 .. row0 + R - 1 (of the segment's q_len * G rows).  Run by the warp that arrived last, after its unit
-// loop, when its own pipeline stages are idle: the records are copied into
-// those stages (buf / bufp, room for cap records) a batch at a time, lane k
-// issuing one bulk copy of record k, all completing on the warp's merge
-// barrier `mbar` (phase parity tracked in `mpar`), and folded from shared
-// memory.  Lane k holds record k's (m, l) of the batch and its weights
-// e^(m_k - M); a batch whose records raise the running maximum M rescales
-// what was folded before (the same recurrence across batches).  Lane i owns
-// head_dim columns i, i + 32, ... of every row.  Records are folded in
-// fragment order, so the result does not depend on which warp merges.
+// rows row0 .. row0 + R - 1 (of the segment's q_len * G rows).  Run by the
+// warp that arrived last, after its unit loop, when its own pipeline stages
+// are idle: the records are copied into those stages (buf / bufp, room for
+// cap records) a batch at a time, lane k issuing one bulk copy of record k,
+// all completing on the warp's merge barrier `mbar` (phase parity tracked in
+// `mpar`), and folded from shared memory.
+//
+// A record's accumulator is [D][GM] floats (row fastest), so element
+// lane + 32 j of it belongs to row lane % GM: each lane folds one row (its
+// running maximum M, sum L and D * GM / 32 elements of it) and reads the
+// batch with consecutive lanes on consecutive words (no bank conflicts, no
+// shuffles: a lane computes its row's weights e^(m_k - M) itself).  A batch
+// that raises M rescales what was folded before (the same recurrence across
+// batches).  Records are folded in fragment order, so the result does not
+// depend on which warp merges.  The rows leave through shared memory
+// (swizzled by 16-byte chunk) as whole rows, 16 bytes per lane.
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
                                               int G, int num_heads, float vs, void* out, int out_dtype,
-                                              int64_t seq_row0, int row0, uint32_t buf, const float* bufp,
+                                              int64_t seq_row0, int row0, uint32_t buf, float* bufp,
                                               int cap, uint32_t mbar, uint32_t& mpar, unsigned int* err) {
-  constexpr int EPL = D / 32;       // columns per lane
+  constexpr int PER = GM * D / 32;  // accumulator elements per lane
   static_assert(REC % 4 == 0, "records are whole 16-byte chunks");
-  cap = cap < 32 ? cap : 32;        // the records of a batch are held one per lane
-  float M[GM], Lp[GM], o[EPL][GM];  // running max, this lane's share of the sum, accumulator
+  static_assert(32 % GM == 0 && D % 32 == 0 && GM * D <= REC, "one row per lane; output staging fits a record");
+  cap = cap < 32 ? cap : 32;  // one bulk copy per lane
+  const int g = lane % GM;    // the row this lane folds
+  float M = -INFINITY, L = 0.f, o[PER];
 #pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    M[g] = -INFINITY;
-    Lp[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e][g] = 0.f;
-  }
+  for (int j = 0; j < PER; ++j) o[j] = 0.f;
 #pragma unroll 1
   for (int f0 = 0; f0 < nfr; f0 += cap) {
     const int nb = min(cap, nfr - f0);
@@ -316,63 +319,48 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
     if (!mbar_wait_bounded(mbar, mpar, kDefaultWaitLimitNs) && lane == 0) raise_error(err, PA_DEVERR_TIMEOUT);
     mpar ^= 1;
     __syncwarp();  // every lane sees the batch
-    float wk[GM];  // lane k: weight of record k per row
+    float mb = -INFINITY;
+    for (int k = 0; k < nb; ++k) mb = fmaxf(mb, bufp[k * REC + GM * D + g]);
+    const float mn = fmaxf(M, mb);
+    const float resc = M == -INFINITY ? 0.f : exp2f(M - mn);  // nothing folded yet: 0
+    L *= resc;
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      const float mk = lane < nb ? bufp[lane * REC + GM * D + g] : -INFINITY;
-      const float lk = lane < nb ? bufp[lane * REC + GM * D + GM + g] : 0.f;
-      float mb = mk;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-      const float mn = fmaxf(M[g], mb);
-      const float resc = M[g] == -INFINITY ? 0.f : exp2f(M[g] - mn);  // nothing folded yet: 0
-      Lp[g] *= resc;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) o[e][g] *= resc;
-      M[g] = mn;
-      // an empty record (m = -inf: its rows saw nothing) weighs 0
-      wk[g] = mk == -INFINITY ? 0.f : exp2f(mk - mn);
-      Lp[g] = fmaf(wk[g], lk, Lp[g]);
-    }
+    for (int j = 0; j < PER; ++j) o[j] *= resc;
+    M = mn;
 #pragma unroll 2
     for (int k = 0; k < nb; ++k) {
-      const float* rk = bufp + k * REC + lane * GM;  // acc[d][0..GM) of column d = lane (+ 32 e)
-      float w[GM];
+      const float* rk = bufp + k * REC;
+      const float mk = rk[GM * D + g];
+      const float w = mk == -INFINITY ? 0.f : exp2f(mk - mn);  // an empty record (its rows saw nothing) weighs 0
+      L = fmaf(w, rk[GM * D + GM + g], L);
 #pragma unroll
-      for (int g = 0; g < GM; ++g) w[g] = __shfl_sync(0xffffffffu, wk[g], k);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        if constexpr (GM % 4 == 0) {
-#pragma unroll
-          for (int g = 0; g < GM; g += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(rk + 32 * e * GM + g);
-            o[e][g] = fmaf(w[g], x.x, o[e][g]);
-            o[e][g + 1] = fmaf(w[g + 1], x.y, o[e][g + 1]);
-            o[e][g + 2] = fmaf(w[g + 2], x.z, o[e][g + 2]);
-            o[e][g + 3] = fmaf(w[g + 3], x.w, o[e][g + 3]);
-          }
-        } else {
-#pragma unroll
-          for (int g = 0; g < GM; ++g) o[e][g] = fmaf(w[g], rk[32 * e * GM + g], o[e][g]);
-        }
-      }
+      for (int j = 0; j < PER; ++j) o[j] = fmaf(w, rk[lane + 32 * j], o[j]);
     }
     __syncwarp();  // every lane has read the batch before the next one overwrites it
   }
+  // rows through shared memory: element (row g, column d) at row g, 16-byte
+  // chunk (d / 4) ^ (g % 8), so that both the writes and the row reads below
+  // spread over the banks
+  const float inv = L > 0.f ? vs / L : 0.f;
 #pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    float L = Lp[g];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (g < R) {
-      // row row0 + g = (query (row0 + g) / G, head (row0 + g) % G) of the group
-      const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>((row0 + g) / G) * num_heads + (row0 + g) % G
-                                  : seq_row0 + g;
-      const float inv = L > 0.f ? vs / L : 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) store_out(out, out_dtype, orow * D + lane + 32 * e, o[e][g] * inv);
+  for (int j = 0; j < PER; ++j) {
+    const int d = (lane + 32 * j) / GM;
+    bufp[g * D + ((((d >> 2) ^ (g & 7)) << 2) | (d & 3))] = o[j] * inv;
+  }
+  __syncwarp();
+  const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  for (int r = 0; r < R; ++r) {
+    // row row0 + r = (query (row0 + r) / G, head (row0 + r) % G) of the group
+    const int64_t orow = GM > 8 ? seq_row0 + static_cast<int64_t>((row0 + r) / G) * num_heads + (row0 + r) % G
+                                : seq_row0 + r;
+    for (int c = lane; c < D / 4; c += 32) {
+      const float4 v = *reinterpret_cast<const float4*>(bufp + r * D + ((c ^ (r & 7)) << 2));
+      store_out4(out, out_dtype, orow * D + 4 * c, v, vec);
     }
   }
+  // the next merge's bulk copies overwrite this staging area
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
 }
 
 template <typename QT, typename KVT, int D, int GM, int UR_, int AP>
@@ -1163,7 +1151,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     const int share = (NS * STG) / NC / (Tr::REC * 4) * (Tr::REC * 4);
     merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, Rw, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
                                   row0, wbase_u32 + Tr::OFF_STAGES + rg * share,
-                                  reinterpret_cast<const float*>(wbase + Tr::OFF_STAGES + rg * share),
+                                  reinterpret_cast<float*>(const_cast<uint8_t*>(wbase) + Tr::OFF_STAGES + rg * share),
                                   share / (Tr::REC * 4), wbase_u32 + Tr::OFF_MERGE + 8 * rg, merge_par, p.err);
     if (lane == 0) p.seg_counters[x * NC + rg] = 0;
   };
