@@ -48,7 +48,29 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
   const int h = static_cast<int>(th % num_kv_heads);
   const int64_t n = th / num_kv_heads;
 
+  const void* src = which ? v : k;
+  const int64_t src_elem = n * (which ? v_stride : k_stride) + static_cast<int64_t>(h) * D + lane * EPL;
+  // The source row (and the quantisation constants) do not depend on the
+  // slot: all of them are loaded before the slot is examined, so the row
+  // costs one memory round trip, not two (the step's decode waits for it).
   const int64_t slot = slot_mapping[n];
+  uint32_t raw[EPL / 2];  // kCopy: the row's 16-bit values as they are
+  float x[EPL];           // quantising modes: float32(value) * inv_scale
+  int zp = 0;
+  if constexpr (MODE == kCopy) {
+    if constexpr (EPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + src_elem);
+      raw[0] = w.x;
+      raw[1] = w.y;
+    } else {
+      raw[0] = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(src) + src_elem);
+    }
+  } else {
+    const float inv = (which ? v_inv_scale : k_inv_scale)[h];
+    if constexpr (MODE == kToInt8) zp = (which ? v_zero_point : k_zero_point)[h];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) x[i] = __fmul_rn(load_scalar<SRC>(src, src_elem + i), inv);
+  }
   if (slot < 0) return;  // padding token
   if (slot >= num_blocks * block_size) {
     if (lane == 0) raise_error(err, PA_DEVERR_SLOT);
@@ -57,25 +79,19 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
   const int64_t blk = slot / block_size;
   const int64_t off = slot - blk * block_size;
   const int64_t dst_elem = ((blk * num_kv_heads + h) * block_size + off) * D + lane * EPL;
-  const void* src = which ? v : k;
-  const int64_t src_elem = n * (which ? v_stride : k_stride) + static_cast<int64_t>(h) * D + lane * EPL;
   void* cache = which ? v_cache : k_cache;
 
   if constexpr (MODE == kCopy) {
     if constexpr (EPL == 4) {
-      const uint2 x = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + src_elem);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(cache) + dst_elem) = x;
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(cache) + dst_elem) = make_uint2(raw[0], raw[1]);
     } else {
-      const uint32_t x = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(src) + src_elem);
-      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(cache) + dst_elem) = x;
+      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(cache) + dst_elem) = raw[0];
     }
   } else if constexpr (MODE == kToInt8) {
-    const float inv = (which ? v_inv_scale : k_inv_scale)[h];
-    const int zp = (which ? v_zero_point : k_zero_point)[h];
     uint32_t packed = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      const int c = int8_code(__fmul_rn(load_scalar<SRC>(src, src_elem + i), inv), zp);
+      const int c = int8_code(x[i], zp);
       packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * i);
     }
     uint8_t* dst = static_cast<uint8_t*>(cache) + dst_elem;
@@ -85,10 +101,6 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
       *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
     }
   } else {
-    const float inv = (which ? v_inv_scale : k_inv_scale)[h];
-    float x[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) x[i] = __fmul_rn(load_scalar<SRC>(src, src_elem + i), inv);
     uint8_t* dst = static_cast<uint8_t*>(cache) + dst_elem;
     if constexpr (EPL == 4) {
       const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3);

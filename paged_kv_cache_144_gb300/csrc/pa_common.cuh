@@ -302,6 +302,14 @@ __device__ __forceinline__ int atom_add_release_gpu(int* addr, int v) {
   return old;
 }
 
+// atomic add with acquire-release semantics at GPU scope: as above, and this
+// thread's later reads see what the arrivals before it released
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // Acquire-release fence at GPU scope: after observing values written by
 // release operations, this thread's later reads see what they released.
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }

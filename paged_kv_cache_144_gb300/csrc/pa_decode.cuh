@@ -327,7 +327,8 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
 #pragma unroll
     for (int j = 0; j < PER; ++j) o[j] *= resc;
     M = mn;
-#pragma unroll 2
+    constexpr int kUnrollRecords = GM > 8 ? 2 : 4;  // records folded together (registers: PER per record)
+#pragma unroll kUnrollRecords
     for (int k = 0; k < nb; ++k) {
       const float* rk = bufp + k * REC;
       const float mk = rk[GM * D + g];
@@ -1111,6 +1112,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   uint32_t merge_par = 0;  // phase parity of this warp's merge barrier
   int* const pend = p.pending + static_cast<int64_t>(blockIdx.x * W + c) * p.pending_cap;
   int arr_old = 0, arr_x = -1, arr_nfr = 0;  // the arrival not settled yet (x < 0: none)
+  bool arr_acq = false;    // that arrival was an acquire (the ring's final fragment)
+  bool pend_fence = false;  // a pending merge was won by a release-only arrival
   auto settle = [&]() {
     if (arr_x >= 0) {
       const int old = __shfl_sync(0xffffffffu, arr_old, 0);
@@ -1118,6 +1121,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         if (npend < p.pending_cap) {
           if (lane == 0) pend[npend] = arr_x;
           ++npend;
+          pend_fence = pend_fence || !arr_acq;
         } else if (lane == 0) {
           raise_error(p.err, PA_DEVERR_INTERNAL);
         }
@@ -1386,9 +1390,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         }
         settle();
         __syncwarp();  // every lane's record stores come before lane 0's release
-        if (lane == 0) arr_old = atom_add_release_gpu(p.seg_counters + (it.s * Hkv + it.kvh) * NC + rg, 1);
+        // The ring's final fragment (no unit after it to stall) arrives with
+        // an acquire too, so a merge it wins needs no fence after the loop.
+        // (Conservative: a range that ends in a later segment's overhead
+        // arrives with a release and its merge takes the fence.)
+        const bool final_frag = fixed ? it.r + it.rstride >= it.R : it.fend >= it.u1;
+        int* const ctr = p.seg_counters + (it.s * Hkv + it.kvh) * NC + rg;
+        if (lane == 0) arr_old = final_frag ? atom_add_acq_rel_gpu(ctr, 1) : atom_add_release_gpu(ctr, 1);
         arr_x = it.s * Hkv + it.kvh;
         arr_nfr = nfr;
+        arr_acq = final_frag;
       }
     }
     ++it.j;
@@ -1404,11 +1415,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   if (MQ && NC > 1) named_barrier_sync(1 + ring_id, NC * 32);
   if (npend > 0) {
     // acquire: the other fragments' records, released by their arrivals.
-    // Lane 0 observed those arrivals (its atomics' results); its fence, then
-    // the warp barrier, order every lane's reads after them.  (An acquire on
-    // every arrival would order the next unit's loads after the atomic and
-    // stall the unit loop.)
-    fence_acq_rel_gpu();
+    // Lane 0 observed those arrivals (its atomics' results); its fence (or
+    // the final fragment's acquiring arrival), then the warp barrier, order
+    // every lane's reads after them.  (An acquire on every arrival would
+    // order the next unit's loads after the atomic and stall the unit loop.)
+    if (pend_fence) fence_acq_rel_gpu();
     __syncwarp();
     // the records are read by bulk copies (the async proxy): each lane orders
     // them after its (acquired) view of global memory
