@@ -105,23 +105,17 @@ int gmax_for_rows(int rows) { return rows <= 1 ? 1 : (rows <= 4 ? 4 : (rows <= 8
 // d = 128), 64 for 8-bit caches with B >= 16 (the same 16 KB per stage, half
 // the refills per byte of 32 rows).  A unit spans at most four blocks, so
 // 64-row units need B >= 16.  Several queries per sequence (16 rows per
-// consumer warp, nc warps sharing a ring): 32-row units for 8-bit caches;
-// for 16-bit caches 32-row units when one or four warps share a ring and
-// 16-row units when two or three do (measured on the GB300 at d = 128:
-// q_len*G = 8 and 16 rows 78 -> 72 and 80 -> 74 us, 64 rows 197 -> 147 and
-// 636 -> 414 us with 32-row units, but 32 and 48 rows 127 -> 135 and 357 ->
-// 377 us).  PA_DECODE_UNIT_ROWS (16, 32; 64 for 8-bit caches) overrides it
-// (tuning).
-int unit_rows_for(int kv_dtype, int block_size, int gmax, bool append, int rows) {
+// consumer warp, nc warps sharing a ring, the query rows in one buffer per
+// ring): 32-row units (measured on the GB300 at d = 128 against 16-row
+// units: 32 rows per KV head on 8 x 32K tokens 227 -> 208 us, on the 32 x 4K
+// GQA batch 84 -> 77 us).  PA_DECODE_UNIT_ROWS (32; 64 for 8-bit caches with
+// B >= 16) overrides it (tuning).
+int unit_rows_for(int kv_dtype, int block_size, int gmax, bool append) {
   const bool q8 = kv_dtype == PA_FP8_E4M3 || kv_dtype == PA_INT8;  // 8-bit cache
   const int env = append ? -1 : pa::tuning_override("PA_DECODE_UNIT_ROWS");  // fused append: defaults only
-  if (env == 16 || env == 32) return env;
+  if (env == 32) return env;
   if (env == 64 && q8 && block_size >= 16 && gmax <= 8) return 64;
-  if (gmax > 8) {
-    if (q8) return 32;
-    const int nc = (rows + 15) / 16;
-    return (nc == 2 || nc == 3) ? 16 : 32;
-  }
+  if (gmax > 8) return 32;
   return q8 && block_size >= 16 ? 64 : 32;
 }
 
@@ -169,7 +163,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
   plan->key.gmax = q_len > 1 ? 16 : gmax_for_rows(num_heads / num_kv_heads);
   const int rows = q_len * (num_heads / num_kv_heads);
   plan->key.row_groups = q_len > 1 ? (rows + 15) / 16 : 1;
-  plan->key.unit_rows = unit_rows_for(kv_dtype, block_size, plan->key.gmax, append, rows);
+  plan->key.unit_rows = unit_rows_for(kv_dtype, block_size, plan->key.gmax, append);
   if (!pa::decode_geometry(plan->key, num_seqs, &plan->geo)) return PA_ERR_UNSUPPORTED;
   const int ur = plan->geo.unit_rows;
   const int max_units = static_cast<int>((static_cast<int64_t>(max_blocks_per_seq) * block_size + ur - 1) / ur);

@@ -87,9 +87,9 @@ struct DecodeTraits {
   static constexpr int KVB = elem<KVT>::bytes;
   static constexpr int ROW = D * KVB;  // bytes of one cache row
   static_assert(ROW == 128 || ROW == 256, "cache rows must be 128 or 256 bytes");
-  static constexpr int UR = UR_;                 // rows per work unit (16, 32; 64 for 8-bit caches)
-  static_assert(UR == 16 || UR == 32 || (UR == 64 && KVB == 1), "unit rows");
-  static constexpr int UR_SHIFT = UR == 64 ? 6 : (UR == 32 ? 5 : 4);
+  static constexpr int UR = UR_;                 // rows per work unit (32; 64 for 8-bit caches)
+  static_assert(UR == 32 || (UR == 64 && KVB == 1), "unit rows");
+  static constexpr int UR_SHIFT = UR == 64 ? 6 : 5;
   static constexpr int NSUB = ROW / 128;         // 128-byte halves per row
   static constexpr int TILE = UR * ROW;          // bytes of one unit of K (or V)
   static constexpr int QRAW = GM * D * 2;        // bytes of one raw query group
@@ -111,8 +111,13 @@ struct DecodeTraits {
   static constexpr int OFF_FULL = 0;
   static constexpr int OFF_EMPTY = OFF_FULL + MAX_NS * 8;
   static constexpr int OFF_MERGE = OFF_EMPTY + MAX_NS * 8;  // one barrier per warp of the ring: its merge copies
+  static constexpr int OFF_QEMPTY = OFF_MERGE + 4 * 8;      // several queries: the ring's query buffer is free
   static constexpr int OFF_STAGES = 1024;
-  static_assert(OFF_MERGE + 4 * 8 <= OFF_STAGES, "barriers");
+  static_assert(OFF_QEMPTY + 8 <= OFF_STAGES, "barriers");
+  // Several queries per sequence (16-row variants): the query rows of a
+  // fragment (16 per consumer warp of the ring) live in one buffer per ring,
+  // after its stages, instead of an area in every stage.
+  __host__ __device__ static constexpr int qbuf_bytes(int nc) { return GM > 8 ? align_up_c(16 * nc * D * 2, 1024) : 0; }
   __host__ __device__ static constexpr int warp_smem(int ns, int stage) { return OFF_STAGES + ns * stage; }
   // partial record: acc as [D][GM] (head fastest), then m[GM], l[GM]
   static constexpr int REC = align_up_c(GM * (D + 2), 4);
@@ -397,12 +402,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
   // Several queries per sequence (16-row variants): the R = q_len * G rows of
   // a segment are served by NC = ceil(R / 16) consumer warps that share one
   // ring, warp k of the ring taking rows 16k .. 16k + 15 of every unit; the
-  // stage's query area holds all 16 * NC rows.  Otherwise one warp per ring.
+  // ring's query buffer holds all 16 * NC rows.  Otherwise one warp per ring.
   constexpr bool kMQ = GM > 8;
   const int NC = kMQ ? p.row_groups : 1;
   const int RW = W / NC;  // rings per CTA, each fed by producer lane 0 .. RW-1
   const int STG = kMQ ? p.stage_bytes : (append ? Tr::STAGE_APPEND : Tr::STAGE);
-  const int wsm = Tr::warp_smem(NS, STG);
+  const int OFF_QBUF = Tr::warp_smem(NS, STG);       // several queries: the ring's query buffer
+  const int wsm = OFF_QBUF + Tr::qbuf_bytes(NC);      // bytes per ring (a multiple of 1024)
   // shared: prefix[S+1] (units before sequence s), lens[S] (clamped seq_lens),
   // scan scratch, then the producer's block-table ring (16 ints per ring)
   int* prefix = reinterpret_cast<int*>(base + RW * wsm);
@@ -483,6 +489,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         mbar_init(cb + Tr::OFF_EMPTY + 8 * i, NC);
       }
       for (int k = 0; k < NC; ++k) mbar_init(cb + Tr::OFF_MERGE + 8 * k, 1);
+      if (kMQ) mbar_init(cb + Tr::OFF_QEMPTY, NC);
     }
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -578,10 +585,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       __syncwarp();
     }
     if (p.withhold_copies) it.valid = false;  // testing hook: nothing is issued, every consumer wait runs out
+    int nq = 0;  // several queries: query loads issued into this lane's ring buffer
     while (__any_sync(0xffffffffu, it.valid)) {
       bool did = false;
       if (it.valid) {
         bool ready = issued < NS || mbar_test_wait(cbase + Tr::OFF_EMPTY + 8 * pst, pph);
+        // several queries: a fragment's first unit also needs the ring's query
+        // buffer, free once every consumer of the ring has read the last load
+        if (kMQ && ready && it.j == it.j0 && nq > 0) ready = mbar_test_wait(cbase + Tr::OFF_QEMPTY, (nq - 1) & 1);
         if (!ready) {
           const uint64_t now = global_timer_ns();
           if (wait_since == 0) {
@@ -638,13 +649,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             }
           }
           if (new_frag) {
-            // rows (query i, head g) of the group, query-major: [q_len][G][D]
+            // rows (query i, head g) of the group, query-major: [q_len][G][D],
+            // into the stage (one query) or the ring's query buffer (several)
+            const uint32_t qdst = kMQ ? cbase + OFF_QBUF : kdst + 2 * Tr::TILE;
             for (int i = 0; i < qlen; ++i) {
               const uint8_t* qsrc =
                   static_cast<const uint8_t*>(p.q) +
                   (static_cast<int64_t>(it.s) * p.q_stride + (static_cast<int64_t>(i) * p.num_heads + it.kvh * G) * D) * 2;
-              bulk_load(kdst + 2 * Tr::TILE + i * G * D * 2, qsrc, G * D * 2, bar);
+              bulk_load(qdst + i * G * D * 2, qsrc, G * D * 2, bar);
             }
+            ++nq;
           }
           if (has_new) {
             const int64_t off = (static_cast<int64_t>(it.s) * p.new_stride + static_cast<int64_t>(it.kvh) * D) * 2;
@@ -1177,8 +1191,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     constexpr bool q_rescale = k8bit && std::is_same<QT, bf16_t>::value;
     int qexp = 0;
     {
-      // the query group rode on the fragment's first stage
-      const uint8_t* qr = wbase + Tr::OFF_STAGES + cst * STG + 2 * Tr::TILE;
+      // the query group rode on the fragment's first stage (into the ring's
+      // query buffer with several queries)
+      const uint8_t* qr = kMQ ? wbase + OFF_QBUF : wbase + Tr::OFF_STAGES + cst * STG + 2 * Tr::TILE;
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const int row = gid + 8 * h;  // local row of the A operand
@@ -1209,6 +1224,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           lo_abs[h] = p.window > 0 ? hi_abs[h] - p.window + 1 : 0;
         }
       }
+    }
+    if constexpr (MQ) {
+      // every lane's query rows are in registers: the ring's query buffer may
+      // be refilled (each of the ring's NC warps arrives once per fragment)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wbase_u32 + Tr::OFF_QEMPTY);
     }
     if constexpr (q_rescale) {
       // largest |q| of the group (bf16 halves read as floats), over the warp
@@ -1437,7 +1458,7 @@ struct DecodeVariant {
 
   static size_t smem_bytes(int num_seqs, int warps, int rings, int stages, int stage) {
     constexpr int head_words = Tr::B8 ? 4 * kMaxHeadParams : 0;
-    return 1024 + static_cast<size_t>(rings) * Tr::warp_smem(stages, stage) +
+    return 1024 + static_cast<size_t>(rings) * (Tr::warp_smem(stages, stage) + Tr::qbuf_bytes(warps / rings)) +
            static_cast<size_t>(align_up_c((2 * num_seqs + 1 + warps + 1 + head_words) * 4, 16)) +
            static_cast<size_t>(rings) * 64;
   }
@@ -1463,8 +1484,8 @@ struct DecodeVariant {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess) return false;
     constexpr bool mq = GM > 8;
     if (nc < 1 || (!mq && nc != 1) || nc > 4) return false;
-    // several queries: the stage's query area holds 16 * nc rows
-    const int stage = mq ? align_up_c(2 * Tr::TILE + 16 * nc * D * 2, 1024) : (AP ? Tr::STAGE_APPEND : Tr::STAGE);
+    // several queries: K and V only (the query rows have a buffer per ring)
+    const int stage = mq ? align_up_c(2 * Tr::TILE, 1024) : (AP ? Tr::STAGE_APPEND : Tr::STAGE);
     const int env_ns = tuning_override("PA_DECODE_STAGES");
     const int env_w = tuning_override("PA_DECODE_WARPS");
     int best_w = 0, best_occ = 0, best_ns = 0;
