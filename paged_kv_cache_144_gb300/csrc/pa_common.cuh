@@ -361,6 +361,16 @@ __device__ __forceinline__ void widen4<i8_t>(uint32_t w, uint32_t zp2, uint32_t&
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(zp2));
 }
 
+// Four INT8 codes -> f16 (1152 + code), exact (an integer below 2048): the
+// widening above without its subtraction.  Used for V, whose zero point and
+// bias leave the output once, (1152 + zp) * v_scale after the divide by the
+// row sum (the product sum and the row sum carry the same weights).
+__device__ __forceinline__ void widen4_i8_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = prmt(u, 0x64646464u, 0x5140u);
+  hi = prmt(u, 0x64646464u, 0x7362u);
+}
+
 // float32 y (= x * inv_scale, already rounded to float32) -> INT8 code:
 // nearest integer (ties to even) plus the zero point, saturated to the int8
 // range; NaN saturates upward.

@@ -227,6 +227,13 @@ __device__ __forceinline__ bool frag_balanced(WorkIter& it, const int* prefix, c
   return false;
 }
 
+// INT8 caches: (1152 + zp) * v_scale, from the staged f16x2(1152 + zp) word
+// (1152 + zp is exact in f16).  V enters the products as 1152 + code, so the
+// output is acc * v_scale / l minus this.
+__device__ __forceinline__ float v_bias_offset(uint32_t zp2, float vs) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(zp2 & 0xffffu))) * vs;
+}
+
 // Ring containing cost position x of a balanced split of C positions over nw rings.
 __device__ __forceinline__ int ring_of(long long x, long long C, int nw) {
   return static_cast<int>(((x + 1) * nw - 1) / C);
@@ -302,7 +309,7 @@ struct MergeSlots {
 // (swizzled by 16-byte chunk) as whole rows, 16 bytes per lane.
 template <int GM, int D, int REC>
 __device__ __forceinline__ void merge_segment(const float* records, const MergeSlots& ms, int nfr, int lane, int R,
-                                              int G, int num_heads, float vs, void* out, int out_dtype,
+                                              int G, int num_heads, float vs, float voff, void* out, int out_dtype,
                                               int64_t seq_row0, int row0, uint32_t buf, float* bufp,
                                               int cap, uint32_t mbar, uint32_t& mpar, unsigned int* err) {
   constexpr int PER = GM * D / 32;  // accumulator elements per lane
@@ -347,11 +354,11 @@ __device__ __forceinline__ void merge_segment(const float* records, const MergeS
   // rows through shared memory: element (row g, column d) at row g, 16-byte
   // chunk (d / 4) ^ (g % 8), so that both the writes and the row reads below
   // spread over the banks
-  const float inv = L > 0.f ? vs / L : 0.f;
+  const float inv = L > 0.f ? vs / L : 0.f, off = L > 0.f ? voff : 0.f;  // a row that saw nothing: 0
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int d = (lane + 32 * j) / GM;
-    bufp[g * D + ((((d >> 2) ^ (g & 7)) << 2) | (d & 3))] = o[j] * inv;
+    bufp[g * D + ((((d >> 2) ^ (g & 7)) << 2) | (d & 3))] = fmaf(o[j], inv, -off);
   }
   __syncwarp();
   const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
@@ -1042,10 +1049,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           const uint32_t lo01 = prmt(x0, x1, 0x5140u), lo23 = prmt(x0, x1, 0x7362u);
           const uint32_t hi01 = prmt(y0, y1, 0x5140u), hi23 = prmt(y0, y1, 0x7362u);
           uint32_t d0l, d1l, d2l, d3l, d0h, d1h, d2h, d3h;
-          widen4<KVT>(lo01, zpv2, d0l, d1l);
-          widen4<KVT>(lo23, zpv2, d2l, d3l);
-          widen4<KVT>(hi01, zpv2, d0h, d1h);
-          widen4<KVT>(hi23, zpv2, d2h, d3h);
+          if constexpr (std::is_same<KVT, i8_t>::value) {
+            // 1152 + code: the output subtracts (1152 + zp) * v_scale once
+            widen4_i8_biased(lo01, d0l, d1l);
+            widen4_i8_biased(lo23, d2l, d3l);
+            widen4_i8_biased(hi01, d0h, d1h);
+            widen4_i8_biased(hi23, d2h, d3h);
+          } else {
+            widen4<KVT>(lo01, zpv2, d0l, d1l);
+            widen4<KVT>(lo23, zpv2, d2l, d3l);
+            widen4<KVT>(hi01, zpv2, d0h, d1h);
+            widen4<KVT>(hi23, zpv2, d2h, d3h);
+          }
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             mma16816<false>(acc[2 * jj][h], d0l, d1l, d0h, d1h, ph[sb][h][0], ph[sb][h][1]);
@@ -1161,13 +1176,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       ms.first_w = ring_of(ms.seg_start + p.frag_cost, U, nw_eff);
       nfr = ring_of(ms.seg_start + per - 1, U, nw_eff) - ms.first_w + 1;
     }
-    float vs = 1.f;
+    float vs = 1.f, voff = 0.f;
     if constexpr (k8bit) vs = hp_vs[kvh];
+    if constexpr (std::is_same<KVT, i8_t>::value) voff = v_bias_offset(hp_zv[kvh], vs);
     const int64_t seq_row0 = static_cast<int64_t>(s) * QL * p.num_heads + static_cast<int64_t>(kvh) * G;
     // the ring's stages are idle after the unit loop (every warp of the ring
     // has passed the ring barrier): warp rg stages its records in its share
     const int share = (NS * STG) / NC / (Tr::REC * 4) * (Tr::REC * 4);
-    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, Rw, G, p.num_heads, vs, p.out, p.out_dtype, seq_row0,
+    merge_segment<GM, D, Tr::REC>(p.part_records, ms, nfr, lane, Rw, G, p.num_heads, vs, voff, p.out, p.out_dtype, seq_row0,
                                   row0, wbase_u32 + Tr::OFF_STAGES + rg * share,
                                   reinterpret_cast<float*>(const_cast<uint8_t*>(wbase) + Tr::OFF_STAGES + rg * share),
                                   share / (Tr::REC * 4), wbase_u32 + Tr::OFF_MERGE + 8 * rg, merge_par, p.err);
@@ -1332,8 +1348,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           for (int off = 4; off < 32; off <<= 1) lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], off);
         }
       }
-      float vs = 1.f;
+      float vs = 1.f, voff = 0.f;  // out = acc * vs / l - voff (INT8: V entered as 1152 + code)
       if constexpr (k8bit) vs = hp_vs[it.kvh];
+      if constexpr (std::is_same<KVT, i8_t>::value) voff = v_bias_offset(hp_zv[it.kvh], vs);
       // output row of A row r: out[s][r / G][kvh * G + r % G]
       const int64_t seq_row0 = static_cast<int64_t>(it.s) * QL * p.num_heads + static_cast<int64_t>(it.kvh) * G;
       auto out_row = [&](int r) -> int64_t {
@@ -1353,6 +1370,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             l1 = lt[1];
           }
           const float i0 = l0 > 0.f ? vs / l0 : 0.f, i1 = l1 > 0.f ? vs / l1 : 0.f;  // a row that saw nothing: 0
+          const float b0 = l0 > 0.f ? voff : 0.f, b1 = l1 > 0.f ? voff : 0.f;
           const int64_t o0 = out_row(r0) * D, o1 = out_row(r1) * D;
           const bool w0 = r0 < Rw, w1 = r1 < Rw;
 #pragma unroll
@@ -1360,8 +1378,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               const int d = dim_of(i, hf);
-              if (w0) store_out(p.out, p.out_dtype, o0 + d, acc[i][h][2 * hf] * i0);
-              if (w1) store_out(p.out, p.out_dtype, o1 + d, acc[i][h][2 * hf + 1] * i1);
+              if (w0) store_out(p.out, p.out_dtype, o0 + d, fmaf(acc[i][h][2 * hf], i0, -b0));
+              if (w1) store_out(p.out, p.out_dtype, o1 + d, fmaf(acc[i][h][2 * hf + 1], i1, -b1));
             }
           }
         }
