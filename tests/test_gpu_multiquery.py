@@ -118,3 +118,12 @@ def test_multi_query_rejects_too_many_rows():
     b = workloads.make_batch("gqa_32x4k", seed=66, num_seqs=2, lengths=("uniform", 5, 9))
     with pytest.raises(pa.PagedAttnError):
         run_gpu(b, workloads.host_values(b, seed=66, q_len=17))   # 17 * G(4) = 68 rows > 64
+
+
+@pytest.mark.parametrize("name,L", [("gqa_32x4k", 4), ("gqa_32x4k", 8), ("long_32k", 4), ("int8_mix", 4)])
+def test_multi_query_many_fragments_per_ring(name, L):
+    """Several hundred short sequences: every ring crosses many segments, so the
+    ring's query buffer is refilled at each of its fragments (one warp per ring
+    at 16 rows, two at 32)."""
+    b = workloads.make_batch(name, seed=73, num_seqs=400, lengths=("uniform", 1, 120))
+    _check(b, workloads.host_values(b, seed=73, q_len=L))
