@@ -413,7 +413,7 @@ class DecodeCase:
                                                    pa.dtype_code(self.q), pa.dtype_code(vals["k_cache"]))
 
     def decode(self, pa, i, stream, *, window=0, pdl=False, fused=False, q=None, tables=None, lens=None,
-               k_new=None, v_new=None):
+               k_new=None, v_new=None, early_kv=False):
         kc, vc = self.caches[i % self.replicas]
         b = self.batch
         extra = {}
@@ -423,7 +423,7 @@ class DecodeCase:
         pa.decode(self.out, self.q if q is None else q, kc, vc, self.tables if tables is None else tables,
                   self.lens if lens is None else lens, b.num_kv_heads, b.scale, b.block_size, k_scale=self.ks,
                   v_scale=self.vs, partition_size=self.partition_size, workspace=self.ws, stream=stream,
-                  window=window, k_zero_point=self.kz, v_zero_point=self.vz, pdl=pdl, **extra)
+                  window=window, k_zero_point=self.kz, v_zero_point=self.vz, pdl=pdl, early_kv=early_kv, **extra)
 
     def cache_write(self, pa, i, stream, *, pdl=False, k=None, v=None, slots=None):
         kc, vc = self.caches[i % self.replicas]
@@ -469,6 +469,7 @@ def run_ours(args):
     no_pairs = torch.empty((0, 2), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     pdl = not args.no_pdl
+    early_kv = pdl and batch.kv_fmt in ("f16", "bf16")
 
     def step(i):
         # one step as a serving loop issues it: nothing between its launches, so the decode's set-up
@@ -480,7 +481,11 @@ def run_ours(args):
         c.cache_write(pa, i, stream, pdl=pdl)
         kc, vc = c.caches[i % c.replicas]
         pa.copy_blocks(kc, vc, no_pairs, stream=stream)          # no shared block is written: no launch
-        c.decode(pa, i, stream, window=args.window, pdl=pdl)
+        # the kernel before the decode is that cache write, which writes each sequence's newest row only:
+        # the decode may start copying the other rows before it has finished (early_kv; 16-bit caches:
+        # with the 8-bit mixes the early copies slowed the quantising write of 256 sequences more than
+        # they saved, 169.6 -> 170.9 us per step on one box)
+        c.decode(pa, i, stream, window=args.window, pdl=pdl, early_kv=early_kv)
 
     sampler = None
     if rank == 0:
@@ -568,7 +573,8 @@ def run_ours(args):
                          k_new=d_k, v_new=d_v)
             else:
                 c.cache_write(pa, i, st, pdl=pdl, k=d_k, v=d_v, slots=d_slots)
-                c.decode(pa, i, st, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens)
+                c.decode(pa, i, st, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens,
+                         early_kv=early_kv)
             h_out.copy_(c.out, non_blocking=True)
 
         if args.e2e_eager:
@@ -632,7 +638,10 @@ def run_ours(args):
             "step": ("pa_decode_ex with the new token's cache write fused (one launch)" if args.fused
                      else "reshape_and_cache(1 new token/seq) + pa_decode") +
                     ((", launched with programmatic dependent launch" if args.fused
-                      else ", both launched with programmatic dependent launch") if pdl else ""),
+                      else ", both launched with programmatic dependent launch" +
+                           ("; the decode's early_kv option lets it copy the rows other than each sequence's "
+                            "newest before the cache write ends" if early_kv else ""))
+                     if pdl else ""),
             "timing": f"value: repeats of exactly K={K} steps back to back (so each step's launches overlap the one "
                       f"before through programmatic dependent launch), CUDA events on the stream, barrier + "
                       f"synchronize around each repeat, repeated until >= {MIN_TIME_S[0]:g} s, median repeat; "

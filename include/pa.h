@@ -208,6 +208,16 @@ int pa_decode(void* out, pa_dtype out_dtype,
  *            (pa_reshape_and_cache_ex with pdl) be scheduled at once; that
  *            kernel waits for the decode before it touches memory.
  *            Engineering addition with no counterpart in the pages.
+ *   early_kv nonzero (with pdl, one query per sequence, no fused append):
+ *            the caller guarantees that the kernel launched just before this
+ *            call writes no row of k_cache / v_cache except the newest one of
+ *            each sequence (position seq_lens[s]-1), as pa_reshape_and_cache
+ *            of the same step does.  The decode then starts copying the K/V
+ *            rows of its first units that hold none of those positions before
+ *            that kernel has finished; q, the scales and the newest rows are
+ *            still read only after it.  Ignored otherwise.  A caller that
+ *            breaks the guarantee gets attention over stale rows.  Engineering
+ *            addition with no counterpart in the pages.
  */
 typedef struct pa_decode_options {
   size_t struct_size;
@@ -222,6 +232,7 @@ typedef struct pa_decode_options {
   const float* v_inv_scale;
   int32_t q_len;
   int32_t pdl;
+  int32_t early_kv;
 } pa_decode_options;
 
 int pa_decode_ex(void* out, pa_dtype out_dtype,

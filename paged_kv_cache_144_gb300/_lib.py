@@ -29,7 +29,7 @@ class DecodeOptions(ctypes.Structure):
                 ("k_zero_point", ctypes.c_void_p), ("v_zero_point", ctypes.c_void_p),
                 ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("new_dtype", ctypes.c_int32),
                 ("new_stride", ctypes.c_int64), ("k_inv_scale", ctypes.c_void_p), ("v_inv_scale", ctypes.c_void_p),
-                ("q_len", ctypes.c_int32), ("pdl", ctypes.c_int32)]
+                ("q_len", ctypes.c_int32), ("pdl", ctypes.c_int32), ("early_kv", ctypes.c_int32)]
 
     def __init__(self, **kw):
         super().__init__(struct_size=ctypes.sizeof(DecodeOptions), **kw)
@@ -255,7 +255,7 @@ def new_workspace(nbytes: int, device):
 def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale, block_size, *,
            k_scale=None, v_scale=None, partition_size=0, workspace=None, stream=None, window=0,
            k_zero_point=None, v_zero_point=None, k_new=None, v_new=None, k_inv_scale=None, v_inv_scale=None,
-           pdl=False):
+           pdl=False, early_kv=False):
     """out[s,h] = softmax(scale * K_s q[s,h]) V_s through the block tables (pa_decode).
 
     window > 0: sliding-window decode over the last `window` positions (pa_decode_ex).
@@ -265,6 +265,8 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
     attended in the same launch (pa_decode_ex).
     pdl=True: programmatic dependent launch (pa_decode_ex): the set-up overlaps the kernel launched just
     before on the stream, so seq_lens and block_tables must not be written by that kernel.
+    early_kv=True (with pdl, one query, no fused append): that kernel also writes no cache row but each
+    sequence's newest one (the step's cache write), so K/V copies of the other rows start before it ends.
     """
     _require_cuda_all((("out", out), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
                        ("seq_lens", seq_lens), ("k_scale", k_scale), ("v_scale", v_scale),
@@ -300,7 +302,7 @@ def decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, scale
         opt = DecodeOptions(window=int(window), k_zero_point=_ptr(k_zero_point), v_zero_point=_ptr(v_zero_point),
                             k_new=_ptr(k_new), v_new=_ptr(v_new), new_dtype=new_dtype, new_stride=new_stride,
                             k_inv_scale=_ptr(k_inv_scale), v_inv_scale=_ptr(v_inv_scale), q_len=q_len,
-                            pdl=1 if pdl else 0)
+                            pdl=1 if pdl else 0, early_kv=1 if early_kv else 0)
         st = pa_decode_ex(*args, ctypes.byref(opt), _stream(stream))
         _check("pa_decode_ex", st)
     else:

@@ -405,6 +405,7 @@ int prepare_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtyp
   const uint64_t lim = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.wait_limit_ns = lim ? lim : pa::kDefaultWaitLimitNs;
   p.withhold_copies = g_withhold_copies.load(std::memory_order_relaxed);
+  p.early_kv = (o.early_kv != 0 && o.pdl != 0 && q_len == 1 && !append) ? 1 : 0;
   d->pdl = o.pdl != 0;
   return PA_OK;
 }

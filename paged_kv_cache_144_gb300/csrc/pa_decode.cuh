@@ -560,12 +560,105 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       if (++ah.j == ah.jend) iter_next_fragment(ah, prefix, p, fixed, Tr::UR_SHIFT);
     };
     while (ah.valid && pf < kTablePrefetch) fetch_tables();
+    int nq = 0;  // several queries: query loads issued into this lane's ring buffer
+    // Issues unit `it` into stage pst (its K/V boxes, the query group at a
+    // fragment start, the appended rows) and advances.  early: the grid
+    // before this one may still be running (early_kv), so the stage is only
+    // armed with its byte count; the query copy (early_q) and the producer's
+    // arrival, which releases the head constants written after the wait,
+    // come after the wait.
+    int n_early = 0;
+    int early_q[Tr::MAX_NS];  // per early stage: segment s * H_kv + kvh whose query group it carries, or -1
+    auto issue_unit = [&](bool early) {
+      const bool new_frag = (it.j == it.j0);
+      const uint32_t bar = cbase + Tr::OFF_FULL + 8 * pst;
+      const uint32_t kdst = cbase + Tr::OFF_STAGES + pst * STG;
+      const uint32_t vdst = kdst + Tr::TILE;
+      const int bj0 = unit_in_block ? (it.j >> upb_shift) : (it.j << bpu_shift);
+      const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
+      const int box0 = first_box(it, bj0);
+      const int row_in_block = unit_in_block ? (it.j - (bj0 << upb_shift)) * UR : 0;
+      const int qlen = GM > 8 ? p.q_len : 1;  // only 16-row variants serve several queries
+      const uint32_t qbytes = new_frag ? static_cast<uint32_t>(qlen * G * D * 2) : 0u;
+      // this unit's entries were fetched pf - 1 units before the newest fetch
+      if (pf >= 3) {
+        cp_async_wait<2>();
+      } else if (pf == 2) {
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      int phys[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        phys[i] = (i >= box0 && i < nbox) ? static_cast<int>(lds32(ring + (rs_use * 4 + i) * 4)) : 0;
+      rs_use = (rs_use + 1) & 3;
+      --pf;
+      // fused append: this unit holds position T-1; its new rows ride along
+      const bool has_new = append && it.j == ((it.T - 1) >> Tr::UR_SHIFT);
+      if (has_new) {
+        const int pb = phys[((it.T - 1) >> p.block_shift) - bj0];
+        st_shared_s32(kdst + Tr::OFF_NEW + 4 * D, (pb >= 0 && pb < p.num_blocks) ? pb : -1);
+      }
+      const uint32_t nbytes = has_new ? static_cast<uint32_t>(4 * D) : 0u;
+      const uint32_t bytes = 2u * (nbox - box0) * BOX * Tr::ROW + qbytes + nbytes;
+      if (early) {
+        mbar_expect_tx(bar, bytes);  // armed only: the query copy and the arrival follow the wait
+      } else {
+        mbar_arrive_expect_tx(bar, bytes);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i >= box0 && i < nbox) {
+          int pb = phys[i];
+          if (pb < 0 || pb >= p.num_blocks) {
+            raise_error(p.err, PA_DEVERR_BLOCK_ID);
+            pb = 0;
+          }
+          const int z = (pb * Hkv + it.kvh) * B + row_in_block;
+          tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, z, 0, bar);
+          tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, z, 0, bar);
+        }
+      }
+      if (early) {
+        early_q[n_early++] = new_frag ? it.s * Hkv + it.kvh : -1;
+      } else if (new_frag) {
+        // rows (query i, head g) of the group, query-major: [q_len][G][D],
+        // into the stage (one query) or the ring's query buffer (several)
+        const uint32_t qdst = kMQ ? cbase + OFF_QBUF : kdst + 2 * Tr::TILE;
+        for (int i = 0; i < qlen; ++i) {
+          const uint8_t* qsrc =
+              static_cast<const uint8_t*>(p.q) +
+              (static_cast<int64_t>(it.s) * p.q_stride + (static_cast<int64_t>(i) * p.num_heads + it.kvh * G) * D) * 2;
+          bulk_load(qdst + i * G * D * 2, qsrc, G * D * 2, bar);
+        }
+        ++nq;
+      }
+      if (has_new) {
+        const int64_t off = (static_cast<int64_t>(it.s) * p.new_stride + static_cast<int64_t>(it.kvh) * D) * 2;
+        bulk_load(kdst + Tr::OFF_NEW, static_cast<const uint8_t*>(p.k_new) + off, 2 * D, bar);
+        bulk_load(kdst + Tr::OFF_NEW + 2 * D, static_cast<const uint8_t*>(p.v_new) + off, 2 * D, bar);
+      }
+      ++issued;
+      if (++pst == NS) {
+        pst = 0;
+        pph ^= 1;
+      }
+      if (ah.valid) fetch_tables();
+      if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
+    };
     // Everything above reads only seq_lens and block_tables.  Under a
     // programmatic dependent launch the grid before this one on the stream
-    // may still be running (it may be writing the cache, q or out); the first
-    // copy of K/V or q, and every write, comes after it has finished.  The
-    // consumers start only on data this warp copies, so they are ordered
-    // after this wait as well.
+    // may still be running (it may be writing the cache, q or out); every
+    // copy of q, of the scales and of the newest rows, and every write, comes
+    // after it has finished.  With early_kv the caller guarantees that it
+    // writes no cache row but each sequence's newest: the K/V of the ring's
+    // first units that hold none of those rows are copied now.  The consumers
+    // start only on stages this warp completes, so they are ordered after the
+    // wait as well.
+    if (p.early_kv && !append && !kMQ && !p.withhold_copies) {
+      while (it.valid && issued < NS && ((it.T - 1) >> Tr::UR_SHIFT) != it.j) issue_unit(true);
+    }
     griddep_wait();
     // empty sequences attend to nothing: their outputs are zero
     for (int s = blockIdx.x * 32 + lane; s < S; s += gridDim.x * 32) {
@@ -591,8 +684,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
       }
       __syncwarp();
     }
+    // the early stages: their query groups, then the arrival that completes them
+    for (int i = 0; i < n_early; ++i) {
+      const uint32_t bar = cbase + Tr::OFF_FULL + 8 * i;
+      const int x = early_q[i];
+      if (x >= 0) {
+        const int s = x / Hkv, kvh = x - (x / Hkv) * Hkv;
+        bulk_load(cbase + Tr::OFF_STAGES + i * STG + 2 * Tr::TILE,
+                  static_cast<const uint8_t*>(p.q) +
+                      (static_cast<int64_t>(s) * p.q_stride + static_cast<int64_t>(kvh) * G * D) * 2,
+                  G * D * 2, bar);
+      }
+      mbar_arrive(bar);
+    }
     if (p.withhold_copies) it.valid = false;  // testing hook: nothing is issued, every consumer wait runs out
-    int nq = 0;  // several queries: query loads issued into this lane's ring buffer
     while (__any_sync(0xffffffffu, it.valid)) {
       bool did = false;
       if (it.valid) {
@@ -610,75 +715,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
           }
         } else {
           wait_since = 0;
-          const bool new_frag = (it.j == it.j0);
-          const uint32_t bar = cbase + Tr::OFF_FULL + 8 * pst;
-          const uint32_t kdst = cbase + Tr::OFF_STAGES + pst * STG;
-          const uint32_t vdst = kdst + Tr::TILE;
-          const int bj0 = unit_in_block ? (it.j >> upb_shift) : (it.j << bpu_shift);
-          const int nbox = unit_in_block ? 1 : min(1 << bpu_shift, it.nblk - bj0);
-          const int box0 = first_box(it, bj0);
-          const int row_in_block = unit_in_block ? (it.j - (bj0 << upb_shift)) * UR : 0;
-          const int qlen = GM > 8 ? p.q_len : 1;  // only 16-row variants serve several queries
-          const uint32_t qbytes = new_frag ? static_cast<uint32_t>(qlen * G * D * 2) : 0u;
-          // this unit's entries were fetched pf - 1 units before the newest fetch
-          if (pf >= 3) {
-            cp_async_wait<2>();
-          } else if (pf == 2) {
-            cp_async_wait<1>();
-          } else {
-            cp_async_wait<0>();
-          }
-          int phys[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            phys[i] = (i >= box0 && i < nbox) ? static_cast<int>(lds32(ring + (rs_use * 4 + i) * 4)) : 0;
-          rs_use = (rs_use + 1) & 3;
-          --pf;
-          // fused append: this unit holds position T-1; its new rows ride along
-          const bool has_new = append && it.j == ((it.T - 1) >> Tr::UR_SHIFT);
-          if (has_new) {
-            const int pb = phys[((it.T - 1) >> p.block_shift) - bj0];
-            st_shared_s32(kdst + Tr::OFF_NEW + 4 * D, (pb >= 0 && pb < p.num_blocks) ? pb : -1);
-          }
-          const uint32_t nbytes = has_new ? static_cast<uint32_t>(4 * D) : 0u;
-          mbar_arrive_expect_tx(bar, 2u * (nbox - box0) * BOX * Tr::ROW + qbytes + nbytes);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (i >= box0 && i < nbox) {
-              int pb = phys[i];
-              if (pb < 0 || pb >= p.num_blocks) {
-                raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                pb = 0;
-              }
-              const int z = (pb * Hkv + it.kvh) * B + row_in_block;
-              tma_load_3d(kdst + i * BOX * Tr::ROW, &tmap_k, 0, z, 0, bar);
-              tma_load_3d(vdst + i * BOX * Tr::ROW, &tmap_v, 0, z, 0, bar);
-            }
-          }
-          if (new_frag) {
-            // rows (query i, head g) of the group, query-major: [q_len][G][D],
-            // into the stage (one query) or the ring's query buffer (several)
-            const uint32_t qdst = kMQ ? cbase + OFF_QBUF : kdst + 2 * Tr::TILE;
-            for (int i = 0; i < qlen; ++i) {
-              const uint8_t* qsrc =
-                  static_cast<const uint8_t*>(p.q) +
-                  (static_cast<int64_t>(it.s) * p.q_stride + (static_cast<int64_t>(i) * p.num_heads + it.kvh * G) * D) * 2;
-              bulk_load(qdst + i * G * D * 2, qsrc, G * D * 2, bar);
-            }
-            ++nq;
-          }
-          if (has_new) {
-            const int64_t off = (static_cast<int64_t>(it.s) * p.new_stride + static_cast<int64_t>(it.kvh) * D) * 2;
-            bulk_load(kdst + Tr::OFF_NEW, static_cast<const uint8_t*>(p.k_new) + off, 2 * D, bar);
-            bulk_load(kdst + Tr::OFF_NEW + 2 * D, static_cast<const uint8_t*>(p.v_new) + off, 2 * D, bar);
-          }
-          ++issued;
-          if (++pst == NS) {
-            pst = 0;
-            pph ^= 1;
-          }
-          if (ah.valid) fetch_tables();
-          if (++it.j == it.jend) iter_next_fragment(it, prefix, p, fixed, Tr::UR_SHIFT);
+          issue_unit(false);
           did = true;
         }
       }

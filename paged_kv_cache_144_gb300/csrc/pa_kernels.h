@@ -96,6 +96,7 @@ struct DecodeParams {
   int stage_bytes;              // bytes of one pipeline stage (the 16-row variants' query area varies)
   uint64_t wait_limit_ns;       // limit of every wait on a pipeline barrier (PA_DEVERR_TIMEOUT after it)
   int withhold_copies;          // testing hook: the producer issues no copy, so every consumer wait runs out
+  int early_kv;                 // K/V of units without a sequence's newest row may be copied before the wait
 };
 
 // Compile-time variant of the decode kernel.

@@ -43,7 +43,8 @@ def out_tolerance(ref: np.ndarray, out_fmt: str) -> np.ndarray:
     return PA_TOL + 0.5 * spacing
 
 
-def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda", window=0, pdl=False):
+def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", device="cuda", window=0, pdl=False,
+            early_kv=False):
     """Fill the cache (8-bit caches: quantising writes), append the new token, decode.
 
     q of shape [S, L, H_q, d] (L > 1) decodes L queries per sequence (pa_decode_ex q_len).
@@ -86,7 +87,8 @@ def run_gpu(batch, vals, *, out_fmt="f32", partition_size=0, workspace="auto", d
                                       batch.max_blocks_per_seq, partition_size, pa.dtype_code(kc), q_len=q_len)
         ws = pa.new_workspace(n, device) if n else None
     pa.decode(out, q, kc, vc, tables, lens, batch.num_kv_heads, batch.scale, B, k_scale=ks, v_scale=vs,
-              partition_size=partition_size, workspace=ws, window=window, k_zero_point=kz, v_zero_point=vz, pdl=pdl)
+              partition_size=partition_size, workspace=ws, window=window, k_zero_point=kz, v_zero_point=vz, pdl=pdl,
+              early_kv=early_kv)
     err = pa.get_device_error()
     return (out.float().cpu().numpy().astype(np.float64), to_numpy(kc, kv), to_numpy(vc, kv), err)
 

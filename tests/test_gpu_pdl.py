@@ -231,3 +231,34 @@ def test_pdl_chain_of_write_and_decode_steps(name, kw):
                                             q_fmt=b.q_fmt, kv_fmt=kv)
         assert np.max(np.abs(o.cpu().numpy().astype(np.float64) - ref)) <= PA_TOL
     assert bits_equal(to_numpy(kc, kv), rk) and bits_equal(to_numpy(vc, kv), rv)
+
+
+@pytest.mark.parametrize("name,kw,partition_size,window", [
+    ("gqa_32x4k", dict(num_seqs=8, lengths=("uniform", 1, 1500)), 0, 0),
+    ("gqa_32x4k", dict(num_seqs=8, lengths=("uniform", 1, 1500)), 512, 0),
+    ("gqa_32x4k", dict(num_seqs=8, lengths=("uniform", 1, 1500)), 0, 100),
+    ("gqa_32x4k", dict(num_seqs=40, lengths=("uniform", 1, 3)), 0, 0),
+    ("long_32k", dict(num_seqs=2, lengths=("const", 4000)), 0, 0),
+    ("fp8_mix", dict(num_seqs=8, lengths=("lognormal", 6.0, 1.0, 16, 1500)), 0, 0),
+    ("int8_mix", dict(num_seqs=8, lengths=("lognormal", 6.0, 1.0, 16, 1500)), 0, 0),
+])
+def test_early_kv_decode_after_the_steps_cache_write(name, kw, partition_size, window):
+    """The step as a serving loop issues it: the cache write of each sequence's newest row, then the decode
+    with pdl and early_kv, which copies the other rows before that write has finished.  Before the write the
+    newest rows' slots hold NaN (16-bit caches), so a decode that copied one of them early would not match;
+    sequences of 1-3 tokens have no unit without their newest row."""
+    b = workloads.make_batch(name, seed=16, **kw)
+    vals = workloads.host_values(b, seed=16)
+    if b.kv_fmt in NAN16:
+        blk, off = b.new_slots // b.block_size, b.new_slots % b.block_size
+        for c in ("k_cache", "v_cache"):
+            raw = vals[c].view(np.uint16)
+            raw[blk, :, off, :] = NAN16[b.kv_fmt]
+    ref, okc, ovc = run_oracle(b, vals, window=window)
+    out, kc, vc, err = run_gpu(b, vals, partition_size=partition_size, window=window, pdl=True, early_kv=True)
+    out0, _, _, err0 = run_gpu(b, vals, partition_size=partition_size, window=window, pdl=False)
+    assert err == 0 and err0 == 0
+    assert bits_equal(kc, okc) and bits_equal(vc, ovc)
+    assert np.isfinite(out).all()
+    assert np.max(np.abs(out - ref)) <= PA_TOL
+    assert bits_equal(out, out0)
