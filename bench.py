@@ -58,11 +58,37 @@ WORKLOAD_TEXT = {
 }
 
 
-def kernel_source_digest() -> str:
+def _code_only(text: str) -> str:
+    """C++/CUDA source without its comments and blank lines (string literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                                   # string literal: copied, escapes honoured
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
+def kernel_source_digest(root: str = ROOT) -> str:
+    """Digest of the code the decode kernel is built from (comments and blank lines excluded), which keys
+    the committed ncu traffic figures: counters taken on other code are not reported."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_144_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(root, "paged_kv_cache_144_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

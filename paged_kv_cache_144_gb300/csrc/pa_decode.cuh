@@ -12,7 +12,7 @@
 // recurrence runs in base 2 with log2(e) folded into the scale.
 //
 // How it is laid out on GB300 (this is not the pages' A100 kernel design):
-//  * Work unit = UR (16, 32; 64 for 8-bit caches) consecutive rows of one (sequence, KV head).
+//  * Work unit = UR (32; 64 for 8-bit caches) consecutive rows of one (sequence, KV head).
 //    A unit is filled by 3-D TMA boxes of min(UR, B) whole rows: part of one
 //    block when B >= UR, one box per block when a unit spans several blocks;
 //    one TMA instruction per box for K and one for V.  A box lands as
@@ -24,27 +24,34 @@
 //    Optionally each warp instead takes fixed partitions of P tokens.
 //  * Warp specialisation: each CTA has W consumer warps and one producer
 //    warp.  Consumer warp c owns a ring of stages in shared memory (one unit
-//    of K, of V and, at a segment start, the query group per stage).  Lane c
-//    of the producer warp walks consumer c's units: it waits for the stage's
-//    "empty" mbarrier, reads the block table, and issues the TMA copies
-//    (cp.async.bulk.tensor) plus a 1-D bulk copy of the query group, all
-//    completing on the stage's "full" mbarrier.  Consumers only wait, compute
-//    and release.  No CTA-wide barrier is used after the prologue.
+//    of K, of V and, at a segment start, the query group per stage; several
+//    queries per sequence keep their query rows in one buffer per ring).
+//    Lane c of the producer warp walks consumer c's units: it waits for the
+//    stage's "empty" mbarrier, reads the block table, and issues the TMA
+//    copies (cp.async.bulk.tensor) plus a 1-D bulk copy of the query group,
+//    all completing on the stage's "full" mbarrier.  Consumers only wait,
+//    compute and release.  No CTA-wide barrier is used after the prologue.
+//    Under a programmatic dependent launch the producer may issue the K/V of
+//    its first units before the kernel before has finished when the caller
+//    guarantees that kernel writes no row of them (early_kv).
 //  * The two contractions of a unit run on the tensor cores (mma.sync
-//    m16n8k16, fp32 accumulate) in the register layout of that instruction:
-//    S^T = Q K^T with the query group as the 16-row A operand (rows >= G are
-//    zero) and 8 tokens per n-tile, then O^T += V^T P^T with 16 head_dim
-//    columns per m-tile, whose B operand (P^T) is exactly the C fragment of
-//    S^T after the softmax.  At the GB300's ratio of issue slots to HBM bytes
-//    the fp32-FMA formulation of these products is instruction-bound; the
-//    tensor-core one is not.  The probabilities enter the second product as
-//    a hi + lo pair of 16-bit values (two MMAs), which keeps their rounding
-//    error near 2^-16 relative.
+//    m16n8k16, fp32 accumulate) in the register layout of that instruction.
+//    One query per sequence: S = K Q^T with 16 tokens per m-tile and the
+//    G <= 8 query rows as N; each 8 x 8 half of the probabilities is
+//    transposed in registers (movmatrix) into the B operand of
+//    O^T += V^T P^T (16 head_dim columns per m-tile).  Several queries:
+//    S^T = Q K^T with 16 (query, head) rows per warp as M, whose C fragment
+//    is the B operand of O^T += V^T P^T as it is.  At the GB300's ratio of
+//    issue slots to HBM bytes the fp32-FMA formulation of these products is
+//    instruction-bound; the tensor-core one is not.  The probabilities enter
+//    the second product as a hi + lo pair of 16-bit values (two MMAs), which
+//    keeps their rounding error near 2^-16 relative.
 //  * 16-bit caches feed the MMAs with ldmatrix (K) and ldmatrix.trans (V)
 //    straight from the swizzled tiles.  8-bit caches are widened in registers
-//    (e4m3 -> f16x2, or INT8 code - zero point -> f16x2, both exact) with the
-//    head_dim order of QK permuted so that a lane reads 16 contiguous bytes
-//    of a K row, and V transposed in registers with byte permutes; the
+//    (e4m3 -> f16x2; INT8 K as code - zero point, INT8 V as 1152 + code with
+//    (1152 + zero point) * v_scale subtracted from the output, all exact) with
+//    the head_dim order of QK permuted so that a lane reads 16 contiguous
+//    bytes of a K row, and V transposed in registers with byte permutes; the
 //    per-head K scale multiplies the scores, the V scale the final divide,
 //    and a bf16 query enters the f16 product scaled by a power of two that
 //    puts the group's largest element at 2^14 .. 2^15 (no overflow, no lost
@@ -52,8 +59,9 @@
 //  * Split segments: a warp whose range covers only part of a segment writes
 //    its (m, l, acc) record to the workspace and arrives on the segment's
 //    counter (a release atomic whose result it reads one fragment later, so
-//    arriving never stalls it); the warp that arrived last merges all records
-//    with the same recurrence after its own unit loop, writes
+//    arriving never stalls it; the ring's final fragment arrives with an
+//    acquire as well); the warp that arrived last merges all records with the
+//    same recurrence after its own unit loop, one row per lane, writes
 //    out[s, kvh*G .. kvh*G+G-1] and resets the counter.  Nothing waits on
 //    another warp, so the kernel cannot deadlock.
 //  * Every wait on an mbarrier is bounded by %globaltimer; on expiry the warp

@@ -93,7 +93,7 @@ struct DecodeParams {
   unsigned int* err;            // per-device error word
   int stages;                   // K/V pipeline stages per warp
   int row_groups;               // consumer warps per ring (16-row variants: ceil(q_len * G / 16)); else 1
-  int stage_bytes;              // bytes of one pipeline stage (the 16-row variants' query area varies)
+  int stage_bytes;              // bytes of one pipeline stage (several queries: K and V only)
   uint64_t wait_limit_ns;       // limit of every wait on a pipeline barrier (PA_DEVERR_TIMEOUT after it)
   int withhold_copies;          // testing hook: the producer issues no copy, so every consumer wait runs out
   int early_kv;                 // K/V of units without a sequence's newest row may be copied before the wait
