@@ -47,3 +47,24 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_zero():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and "rank 0 of 2" in d["cpu_baseline"]["sample"]
+
+
+def test_kernel_digest_ignores_comments_and_tracks_code(tmp_path):
+    """The digest that keys the committed ncu traffic figures: a comment or blank-line edit keeps it (the
+    compiled kernel is the same), a code edit changes it (the counters no longer describe the kernel)."""
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(ROOT, "paged_kv_cache_144_gb300", "csrc")
+    dst = tmp_path / "paged_kv_cache_144_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    base = bench.kernel_source_digest(str(tmp_path))
+    assert base == bench.kernel_source_digest()
+    f = dst / "pa_kernels.h"
+    text = f.read_text()
+    f.write_text("// an added comment\n\n" + text.replace("{", "{  /* inline comment */", 1) + "\n\n")
+    assert bench.kernel_source_digest(str(tmp_path)) == base
+    f.write_text(text.replace("{", "{ int added_field_for_the_test; ", 1))
+    assert bench.kernel_source_digest(str(tmp_path)) != base
+    # a string literal that looks like a comment is code
+    assert bench._code_only('const char* s = "a // b";  // c') == 'const char* s = "a // b";'
