@@ -598,9 +598,12 @@ def run_ours(args):
                 c.decode(pa, i, st, window=args.window, pdl=pdl, fused=True, q=d_q, tables=d_tables, lens=d_lens,
                          k_new=d_k, v_new=d_v)
             else:
+                # no early_kv here: a step launched on an idle GPU (after the host read of the last one)
+                # has the decode's early copies reach memory ahead of the cache write's few loads and
+                # delay it (GQA: 76.8 -> 79.3 us per end-to-end step, one box); back to back, the cache
+                # write's CTAs already wait on the SMs and the early copies pay (50.6 -> 49.3 us)
                 c.cache_write(pa, i, st, pdl=pdl, k=d_k, v=d_v, slots=d_slots)
-                c.decode(pa, i, st, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens,
-                         early_kv=early_kv)
+                c.decode(pa, i, st, window=args.window, pdl=pdl, q=d_q, tables=d_tables, lens=d_lens)
             h_out.copy_(c.out, non_blocking=True)
 
         if args.e2e_eager:
