@@ -129,3 +129,27 @@ def test_workload_batches_split_as_the_kernel_does():
     for name, ur in (("gqa_32x4k", 32), ("fp8_mix", 64), ("long_32k", 32)):
         b = workloads.make_batch(name, seed=0)
         assert _split([int(x) for x in b.seq_lens], b.num_kv_heads, ur, 3, 152 * 6) > 0
+
+
+@pytest.mark.parametrize("GM,D", [(4, 64), (4, 128), (8, 64), (8, 128), (16, 64), (16, 128)])
+def test_merge_output_staging_is_a_bijection_read_back_by_rows(GM, D):
+    """The split merge's output staging: lane l folds row l % GM, element l + 32 j of a record being
+    (column (l + 32 j) // GM, row l % GM); it stores that element at row * D + ((col // 4) ^ (row % 8)) * 4
+    + col % 4, and the rows are then read 16 bytes per lane, lane c taking physical chunk c ^ (row % 8).
+    Every element lands once, inside GM * D words, and every row reads back its own columns in order."""
+    per = GM * D // 32
+    where = {}
+    for lane in range(32):
+        g = lane % GM
+        for j in range(per):
+            d = (lane + 32 * j) // GM
+            assert (lane + 32 * j) % GM == g
+            addr = g * D + ((((d >> 2) ^ (g & 7)) << 2) | (d & 3))
+            assert 0 <= addr < GM * D and addr not in where.values()
+            where[(g, d)] = addr
+    assert len(where) == GM * D
+    inv = {a: k for k, a in where.items()}
+    for r in range(GM):
+        for c in range(D // 4):
+            base = r * D + ((c ^ (r & 7)) << 2)
+            assert [inv[base + k] for k in range(4)] == [(r, 4 * c + k) for k in range(4)]
